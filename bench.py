@@ -1,0 +1,364 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA hot path on GB300: prefill tokens/s (T=8192, H=96, d=128, bf16) and
+decode state GB/s (N=256, H=96), against the HBM roofline.
+
+One step = one kda_prefill of the 8192-token, 96-head workload (inputs resident in HBM).
+The decode (256 sequences x 96 heads, 1.6 GB fp32 state updated in place) and a checkpoint
+restore (kda_state_copy of 64 states) are timed in the same run and reported beside it.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+N > 1 runs under torchrun: every rank processes its own copy of the workload (the heads and
+sequences of the path are independent, so ranks exchange nothing); value = all ranks'
+tokens / the slowest rank's time.  --impl reference times the fp64 CPU oracle instead.
+The pages report no throughput or kernel measurement for KDA, so vs_baseline is null.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s at H=96,d=128; decode state HBM GB/s vs peak"
+PUBLISHED = "none: the pages report no KDA throughput, latency or kernel measurement"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+H, D = 96, 128
+T1 = 8192                      # prefill workload: one sequence of 8192 tokens
+N_DEC = 256                    # decode workload: 256 sequences
+FLOP_PER_TOKEN_HEAD = 6 * D * D + 8 * 16 * D        # 114,688 (chunk C = 16 accounting)
+BYTES_PER_TOKEN_HEAD = 5 * D * 2 + 2                # q, k, v, g, o bf16 + beta = 1,282
+STATE_BYTES = D * D * 4                             # 65,536 per (sequence, head)
+DECODE_BYTES_PER_SEQ_HEAD = 2 * STATE_BYTES + 4 * D * 2 + 2 + D * 2   # 132,354
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="kda_clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        smax = max((float(r[2]) for r in rows if r[2].replace(".", "").isdigit()), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def cuda_time_ms(fn, steps, stream):
+    """CUDA-event time of `steps` calls of fn on `stream`, plus the per-call average."""
+    import torch
+
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    total = start.elapsed_time(stop)
+    return total, total / steps
+
+
+def oracle_sample(tokens: int, heads: int, seed: int = 1, threads=None):
+    """Run the fp64 oracle on the first `tokens` tokens of `heads` heads of the prefill
+    workload's distributions; returns (seconds, threads used)."""
+    import oracle
+    from kimi_delta_attention_13_gb300 import synth
+
+    x = synth.make_inputs([tokens], heads=heads, dtype="bf16", seed=seed, device="cpu")
+    orc = oracle.default()
+    nthreads = int(threads or os.cpu_count() or 1)
+    t0 = time.perf_counter()
+    orc.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], threads=nthreads)
+    return time.perf_counter() - t0, min(nthreads, heads)
+
+
+def cpu_baseline(target_s: float = 10.0):
+    """The oracle timed on a bounded sample of the T=8192, H=96 workload, scaled to tokens/s of
+    the full 96-head width."""
+    t_small, _ = oracle_sample(64, H)
+    tokens = int(max(64, min(T1, 64 * target_s / max(t_small, 1e-3))))
+    secs, cores = oracle_sample(tokens, H)
+    return {"value": tokens / secs, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle, first {tokens} tokens x all {H} heads of the T=8192 workload "
+                      f"({secs:.1f} s)"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    per_step_tokens = 256
+    for _ in range(args.warmup):
+        oracle_sample(per_step_tokens, H)
+    secs = []
+    cores = 1
+    for _ in range(args.steps):
+        s, cores = oracle_sample(per_step_tokens, H)
+        secs.append(s)
+    total = sum(secs)
+    value = per_step_tokens * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"prefill T={T1} H={H} d={D} (oracle sample: {per_step_tokens} tokens "
+                               f"x {H} heads per step)", "global_batch": 1, "seq_len": T1,
+                   "parallelism": "cpu threads"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {per_step_tokens} tokens x {H} heads per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "published": PUBLISHED,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gb300(args):
+    import torch
+
+    import kimi_delta_attention_13_gb300 as kda
+    from kimi_delta_attention_13_gb300 import build as kbuild
+    from kimi_delta_attention_13_gb300 import synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    kbuild.build()
+    kda.load()
+    peaks, peak_kind = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- prefill workload (inputs resident in HBM, 1.0 GB: larger than L2) -----------------
+    x = synth.make_inputs([T1], heads=H, dtype="bf16", seed=1, device=dev)
+    out = torch.empty(T1, H, D, device=dev, dtype=torch.bfloat16)
+    fin = torch.empty(1, H, D, D, device=dev, dtype=torch.float32)
+
+    def prefill_step():
+        kda.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], out=out, final_state=fin, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        prefill_step()
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    barrier()
+    clocks.start()
+    total_ms, per_ms = cuda_time_ms(prefill_step, args.steps, stream)
+    barrier()
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+        per_ms = total_ms / args.steps
+    tokens_per_s = world * T1 * args.steps / (total_ms / 1e3)
+    bytes_alg = T1 * H * BYTES_PER_TOKEN_HEAD + H * STATE_BYTES
+    flops_alg = T1 * H * FLOP_PER_TOKEN_HEAD
+    achieved_gbs = bytes_alg / (per_ms / 1e3) / 1e9
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    t_bytes = bytes_alg / (hbm_peak * 1e9)
+    t_flops = flops_alg / (float(peaks.get("bf16_tflops", 1900.0)) * 1e12)
+    path = "tensor-core chunked" if kda.prefill_path(D, D, torch.bfloat16) == 1 else "per-token"
+
+    # ---- end to end through the public API: pinned host inputs -> device -> host outputs -----
+    hx = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
+    h_out = torch.empty(T1, H, D, dtype=torch.bfloat16).pin_memory()
+    h_fin = torch.empty(1, H, D, D, dtype=torch.float32).pin_memory()
+    del x
+
+    def e2e_step():
+        d = {k: v.to(dev, non_blocking=True) for k, v in hx.items()}
+        o, f, _ = kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], stream=stream)
+        h_out.copy_(o, non_blocking=True)
+        h_fin.copy_(f, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e2e_ms, e2e_per = cuda_time_ms(e2e_step, max(3, args.steps // 2), stream)
+    h2d = sum(v.numel() * v.element_size() for v in hx.values())
+    d2h = h_out.numel() * 2 + h_fin.numel() * 4
+    del hx, h_out, h_fin
+    torch.cuda.empty_cache()
+
+    # ---- decode workload: 256 x 96 states (1.6 GB fp32), updated in place -----------------
+    d = synth.make_decode_inputs(N_DEC, heads=H, seed=3, device=dev)
+    dout = torch.empty(N_DEC, H, D, device=dev, dtype=torch.bfloat16)
+
+    def decode_step():
+        kda.decode(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state"], out=dout, stream=stream)
+
+    for _ in range(3):
+        decode_step()
+    _, dec_ms = cuda_time_ms(decode_step, max(5, args.steps), stream)
+    dec_bytes = N_DEC * H * DECODE_BYTES_PER_SEQ_HEAD
+    dec_gbs = dec_bytes / (dec_ms / 1e3) / 1e9
+    del d, dout
+    torch.cuda.empty_cache()
+
+    # ---- checkpoint restore: 64 states of 96 heads (403 MB) gathered by index --------------
+    src = torch.randn(64, H, D, D, device=dev)
+    dst = torch.empty_like(src)
+    idx = torch.randperm(64, device=dev)
+
+    def copy_step():
+        kda.state_copy(dst, src, idx, idx, stream=stream)
+
+    for _ in range(3):
+        copy_step()
+    _, cp_ms = cuda_time_ms(copy_step, 10, stream)
+    cp_gbs = 2 * src.numel() * 4 / (cp_ms / 1e3) / 1e9
+    assert kda.device_status() == 0
+    del src, dst
+    torch.cuda.empty_cache()
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    base = cpu_baseline() if (world == 1 and not args.no_cpu_baseline) else None
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "prefill_traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tr = json.load(f)
+        if tr.get("kernel_source_hash") == kbuild_source_hash():
+            traffic = tr.get("dram_bytes_per_launch")
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": per_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"prefill T={T1} H={H} d_k=d_v={D} bf16 in/out, fp32 state, zero "
+                               "initial state, final state written (one sequence)",
+                   "global_batch": world, "seq_len": T1, "heads": H, "head_dim": D,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (1.0 GB read per step), no flush needed",
+                   "prefill_kernel": path},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved_gbs / hbm_peak, "traffic": traffic,
+                     "peak_kind": f"{peak_kind} copy bandwidth (burst)",
+                     "bytes_alg_per_launch": bytes_alg, "flops_alg_per_launch": flops_alg,
+                     "t_bytes_us": t_bytes * 1e6, "t_flops_us": t_flops * 1e6,
+                     "roofline_fraction": max(t_bytes, t_flops) / (per_ms / 1e3)},
+        "e2e": {"value": world * T1 / (e2e_per / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_per},
+        "decode": {"workload": f"decode N={N_DEC} H={H} d={D}, fp32 state in place",
+                   "GB/s": dec_gbs, "peak": hbm_peak, "frac": dec_gbs / hbm_peak, "ms": dec_ms,
+                   "bytes_alg": dec_bytes},
+        "state_copy": {"workload": "64 states x 96 heads gathered by index (403 MB)",
+                       "GB/s": cp_gbs, "frac": cp_gbs / hbm_peak, "ms": cp_ms},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "cpu_baseline": base,
+        "published": PUBLISHED,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def kbuild_source_hash() -> str:
+    """Hash of the prefill kernel sources: a stored ncu traffic figure applies only to them."""
+    import hashlib
+
+    from kimi_delta_attention_13_gb300 import build as kbuild
+
+    h = hashlib.sha256()
+    for p in kbuild.sources():
+        if "prefill" in os.path.basename(p) or "internal" in os.path.basename(p):
+            with open(p, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

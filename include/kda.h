@@ -1,0 +1,153 @@
+/*
+ * kda.h -- C ABI of the GB300 Kimi Delta Attention (KDA) library (libkda_gb300.so).
+ *
+ * The operation (page "Kimi K3 im Detail", flozi.net, section "Sequenz-Mixing: KDA-Zustand
+ * und globale MLA"): each KDA head keeps a recurrent matrix S in R^{d_k x d_v}.  For every
+ * token t the old state is attenuated channel-wise by a retention vector, a scalar write gate
+ * beta_t applies a delta-rule correction, and the query reads S_t^T q_t after that update:
+ *
+ *     S'  = diag(exp(clamp(g_t, -5, 0))) S_{t-1}          (decay over the key channels)
+ *     S_t = S' + beta_t k_t (v_t - S'^T k_t)^T            (delta-rule write)
+ *     o_t = S_t^T q_t                                     (read includes the current token)
+ *
+ * The floor -5 on the log-decay is the published bound of the same section; over a 16-token
+ * tile the cumulative log-decay therefore stays >= -80, which keeps every exponential factor
+ * of the chunked prefill inside the fp32/bf16 range.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library allocates no
+ *     memory, keeps no per-call state and never synchronizes the stream.  Every call only
+ *     validates its host-side arguments and enqueues kernels on `stream` (a cudaStream_t;
+ *     NULL = the legacy default stream) of the current device.  Calls are thread-safe.
+ *   - Layouts are row-major with the last index contiguous:
+ *       q, k, g : [T_total, H, d_k]     v, out : [T_total, H, d_v]     beta : [T_total, H]
+ *       states  : [N, H, d_k, d_v] fp32, S[i][j] with i = key channel, j = value channel.
+ *   - `dtype` (kda_dtype) is the element type of q, k, v, g, beta and out; states and
+ *     checkpoints are always fp32, and all accumulation is fp32.
+ *   - Every pointer passed must be 16-byte aligned.
+ *   - Return value: KDA_OK (0) or a kda_status code; nothing is enqueued on error.  Checks that
+ *     need device data (monotone cu_seqlens, finite inputs) are not made.  A bounded device
+ *     wait that expires, or a state index out of range, sets a sticky per-device error word
+ *     that kda_device_status() reads.
+ */
+#ifndef KDA_GB300_H
+#define KDA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad dtype or stride       */
+    KDA_ERR_UNSUPPORTED_SHAPE = 2, /* head dimensions the kernels do not implement            */
+    KDA_ERR_MISALIGNED = 3,        /* a pointer not 16-byte aligned                           */
+    KDA_ERR_CUDA = 4,              /* a CUDA runtime call or kernel launch failed             */
+    KDA_ERR_DEVICE_TIMEOUT = 5,    /* a bounded device-side wait expired (device error word)  */
+    KDA_ERR_INDEX_RANGE = 6        /* kda_state_copy met an index outside its slot range      */
+} kda_status;
+
+typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
+
+/* ABI revision of this header; bumped on any incompatible change. */
+#define KDA_ABI_VERSION 1
+int kda_abi_version(void);
+
+/* Human-readable name of a kda_status value (static storage, never NULL). */
+const char *kda_status_string(int status);
+
+/*
+ * kda_prefill -- varlen chunked prefill.
+ *
+ * Defined by the section cited above: the tokens of a chunk are processed in parallel and the
+ * recurrent state is handed from chunk to chunk (second paragraph); the prefix-reuse paragraph
+ * (fourth paragraph) stores KDA states only at sparse checkpoints.
+ *
+ *   q, k, g, v, beta  inputs, layouts above, `dtype` elements.  May be NULL iff total_tokens==0.
+ *   cu_seqlens        device int32 [n_seqs+1], cu_seqlens[0] = 0, non-decreasing,
+ *                     cu_seqlens[n_seqs] = total_tokens.  Sequence n owns tokens
+ *                     [cu_seqlens[n], cu_seqlens[n+1]); empty sequences are allowed.
+ *                     May be NULL when n_seqs == 1 (one sequence of total_tokens).
+ *   n_seqs, total_tokens, n_heads, d_k, d_v   sizes (n_seqs >= 0, total_tokens >= 0).
+ *   init_state        fp32 [n_seqs, H, d_k, d_v] state before each sequence, or NULL = zeros.
+ *                     May alias final_state (in-place resume).
+ *   out               [total_tokens, H, d_v] outputs o_t, `dtype`.  Must not alias an input.
+ *   final_state       fp32 [n_seqs, H, d_k, d_v] state after each sequence, or NULL.
+ *   ckpt_stride       0 (no checkpoints) or a positive multiple of 64.  Sequence n of length
+ *                     L_n emits floor(L_n / ckpt_stride) checkpoints: the state after its first
+ *                     m*ckpt_stride tokens, m = 1..floor(L_n / ckpt_stride).
+ *   ckpts             fp32 [sum_n floor(L_n / ckpt_stride), H, d_k, d_v]; slots are ordered by
+ *                     sequence, then by position.  Required iff ckpt_stride > 0.
+ *   stream            cudaStream_t to enqueue on.
+ *
+ * Supported head sizes: d_k = d_v = 128 for bf16 (tensor-core chunked kernel); for fp32, and
+ * for bf16 with other sizes, 1 <= d_k <= 128 and d_v a multiple of 32 up to 256 (per-token
+ * CUDA-core kernel).  Errors: KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED_SHAPE,
+ * KDA_ERR_MISALIGNED, KDA_ERR_CUDA.
+ */
+int kda_prefill(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t n_heads,
+                int32_t d_k, int32_t d_v, int32_t dtype, const float *init_state, void *out,
+                float *final_state, int32_t ckpt_stride, float *ckpts, void *stream);
+
+/*
+ * kda_prefill_recurrent -- the same operation and arguments as kda_prefill, always evaluated
+ * token by token on CUDA cores (fp32 state in registers).  It is the path kda_prefill takes
+ * for fp32 inputs; for bf16 it is a slower second evaluation used to cross-check the
+ * tensor-core kernel.  Same errors as kda_prefill.
+ */
+int kda_prefill_recurrent(const void *q, const void *k, const void *v, const void *g,
+                          const void *beta, const int32_t *cu_seqlens, int32_t n_seqs,
+                          int64_t total_tokens, int32_t n_heads, int32_t d_k, int32_t d_v,
+                          int32_t dtype, const float *init_state, void *out, float *final_state,
+                          int32_t ckpt_stride, float *ckpts, void *stream);
+
+/* Which kernel kda_prefill runs for these sizes: 1 = tensor-core chunked, 0 = per-token
+ * CUDA-core, negative = a kda_status (unsupported / invalid). */
+int kda_prefill_path(int32_t d_k, int32_t d_v, int32_t dtype);
+
+/*
+ * kda_decode -- one new token per sequence, state updated in place.
+ *
+ * The recurrence above at T = 1 (same section: the state has a fixed size and replaces a
+ * per-token KV cache, so generating a token is one update of S).
+ *
+ *   q, k, g : [n_seqs, H, d_k]   v : [n_seqs, H, d_v]   beta : [n_seqs, H]   (`dtype`)
+ *   state   : fp32 [n_seqs, H, d_k, d_v], read and overwritten in place with S_t.
+ *   out     : [n_seqs, H, d_v] `dtype`, o_t = S_t^T q_t.
+ * Supported: 1 <= d_k <= 128, d_v a multiple of 4 up to 128.  Errors as kda_prefill.
+ */
+int kda_decode(const void *q, const void *k, const void *v, const void *g, const void *beta,
+               float *state, void *out, int32_t n_seqs, int32_t n_heads, int32_t d_k, int32_t d_v,
+               int32_t dtype, void *stream);
+
+/*
+ * kda_state_copy -- copy whole per-sequence states (H x d_k x d_v fp32 each) between slot
+ * arrays: dst[dst_idx[i]] = src[src_idx[i]] for i in [0, n).  This is the restore step of
+ * prefix reuse (section cited above, fourth paragraph: a reused prefix restarts from a stored
+ * KDA state at the same token boundary).
+ *
+ *   dst, src         fp32 slot arrays [n_dst_slots, H, d_k, d_v] and [n_src_slots, ...];
+ *                    they may be the same array but copied slots must not overlap.
+ *   dst_idx, src_idx device int64 [n] slot indices, or NULL for the identity i.
+ *   An index outside [0, n_*_slots) skips that copy and sets the device error word to
+ *   KDA_ERR_INDEX_RANGE.  Errors: KDA_ERR_INVALID_ARG, KDA_ERR_MISALIGNED, KDA_ERR_CUDA.
+ */
+int kda_state_copy(float *dst, const int64_t *dst_idx, int64_t n_dst_slots, const float *src,
+                   const int64_t *src_idx, int64_t n_src_slots, int64_t n, int32_t n_heads,
+                   int32_t d_k, int32_t d_v, void *stream);
+
+/*
+ * kda_device_status -- synchronize `stream`, then read and clear the current device's sticky
+ * error word (KDA_OK if no device-side error was recorded since the last read).  *status
+ * receives the recorded kda_status.  Returns KDA_OK, or KDA_ERR_CUDA if the read failed.
+ */
+int kda_device_status(int32_t *status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_H */

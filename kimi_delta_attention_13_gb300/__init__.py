@@ -1,0 +1,183 @@
+"""GB300-native Kimi Delta Attention (KDA): thin torch binding over the C ABI of libkda_gb300.
+
+The three calls (and the cross-check path) mirror include/kda.h.  This module only checks
+tensor properties, allocates outputs with torch when the caller does not pass them, and
+hands raw device pointers plus the current CUDA stream to the library; every step of the
+computation runs in the library's CUDA kernels.  There is no CPU fallback: without the
+built library or a CUDA device the calls raise.
+
+Recurrence ("Kimi K3 im Detail", section "Sequenz-Mixing: KDA-Zustand und globale MLA"):
+per head S' = diag(exp(clamp(g_t,-5,0))) S_{t-1}, S_t = S' + beta_t k_t (v_t - S'^T k_t)^T,
+o_t = S_t^T q_t.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import KDAError
+
+__all__ = ["prefill", "prefill_recurrent", "decode", "state_copy", "device_status", "prefill_path",
+           "num_checkpoints", "KDAError", "load"]
+
+_DTYPES = {torch.bfloat16: _lib.KDA_BF16, torch.float32: _lib.KDA_F32}
+
+
+def load():
+    """Load libkda_gb300.so (raises if it is not built)."""
+    return _lib.load()
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _require(t: torch.Tensor, name: str, device, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device}); there is no CPU path")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype} (got {t.dtype})")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def num_checkpoints(lengths: Sequence[int], ckpt_stride: int) -> int:
+    """Checkpoint slots a prefill emits: sum over sequences of floor(len / stride)."""
+    return 0 if ckpt_stride <= 0 else int(sum(int(L) // ckpt_stride for L in lengths))
+
+
+def prefill_path(d_k: int = 128, d_v: int = 128, dtype=torch.bfloat16) -> int:
+    """1 = tensor-core chunked kernel, 0 = per-token CUDA-core kernel, <0 = unsupported."""
+    return int(_lib.load().kda_prefill_path(d_k, d_v, _DTYPES[dtype]))
+
+
+def _prefill(fn_name, q, k, v, g, beta, cu_seqlens, init_state, out, final_state, ckpt_stride,
+             ckpts, lengths, stream):
+    lib = _lib.load()
+    dev = q.device
+    dtype = q.dtype
+    if dtype not in _DTYPES:
+        raise ValueError("q/k/v/g/beta must be bfloat16 or float32")
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, name, shp in ((q, "q", (T, H, dk)), (k, "k", (T, H, dk)), (g, "g", (T, H, dk)),
+                         (v, "v", (T, H, dv)), (beta, "beta", (T, H))):
+        _require(t, name, dev, dtype, shp)
+    if cu_seqlens is None:
+        n = 1
+    else:
+        _require(cu_seqlens, "cu_seqlens", dev, torch.int32)
+        n = cu_seqlens.numel() - 1
+    if init_state is not None:
+        _require(init_state, "init_state", dev, torch.float32, (n, H, dk, dv))
+    if out is None:
+        out = torch.empty((T, H, dv), device=dev, dtype=dtype)
+    else:
+        _require(out, "out", dev, dtype, (T, H, dv))
+    if final_state is True:
+        final_state = torch.empty((n, H, dk, dv), device=dev, dtype=torch.float32)
+    elif final_state is False or final_state is None:
+        final_state = None
+    else:
+        _require(final_state, "final_state", dev, torch.float32, (n, H, dk, dv))
+    if ckpt_stride and ckpts is None:
+        if lengths is None:  # host read of the lengths (synchronizes); pass `lengths` to avoid it
+            lengths = [T] if cu_seqlens is None else torch.diff(cu_seqlens).tolist()
+        slots = num_checkpoints(lengths, ckpt_stride)
+        ckpts = torch.empty((max(slots, 1), H, dk, dv), device=dev, dtype=torch.float32)[:slots]
+    elif ckpts is not None:
+        _require(ckpts, "ckpts", dev, torch.float32)
+    rc = getattr(lib, fn_name)(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), n, T, H, dk, dv,
+        _DTYPES[dtype], _ptr(init_state), _ptr(out), _ptr(final_state), int(ckpt_stride),
+        _ptr(ckpts), _stream(dev, stream))
+    _lib.check(rc, fn_name)
+    return out, final_state, ckpts
+
+
+def prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, *, out=None, final_state=True,
+            ckpt_stride: int = 0, ckpts=None, lengths=None, stream=None):
+    """Varlen chunked KDA prefill (kda_prefill).
+
+    q, k, g: [T, H, d_k]; v: [T, H, d_v]; beta: [T, H] (bf16 or fp32, contiguous, CUDA);
+    cu_seqlens: int32 [N+1] on the device or None for one sequence; init_state: fp32
+    [N, H, d_k, d_v] or None (zeros).  final_state: True to allocate, a tensor to fill, or
+    None/False.  ckpt_stride: 0 or a multiple of 64.  Returns (out, final_state, ckpts).
+    """
+    return _prefill("kda_prefill", q, k, v, g, beta, cu_seqlens, init_state, out, final_state,
+                    ckpt_stride, ckpts, lengths, stream)
+
+
+def prefill_recurrent(q, k, v, g, beta, cu_seqlens=None, init_state=None, *, out=None,
+                      final_state=True, ckpt_stride: int = 0, ckpts=None, lengths=None, stream=None):
+    """Same as prefill, always through the token-by-token CUDA-core kernel."""
+    return _prefill("kda_prefill_recurrent", q, k, v, g, beta, cu_seqlens, init_state, out,
+                    final_state, ckpt_stride, ckpts, lengths, stream)
+
+
+def decode(q, k, v, g, beta, state, *, out=None, stream=None):
+    """One-token KDA update (kda_decode): state [N, H, d_k, d_v] fp32 is updated in place.
+    q, k, g: [N, H, d_k]; v: [N, H, d_v]; beta: [N, H].  Returns out [N, H, d_v]."""
+    lib = _lib.load()
+    dev, dtype = q.device, q.dtype
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, name, shp in ((q, "q", (N, H, dk)), (k, "k", (N, H, dk)), (g, "g", (N, H, dk)),
+                         (v, "v", (N, H, dv)), (beta, "beta", (N, H))):
+        _require(t, name, dev, dtype, shp)
+    _require(state, "state", dev, torch.float32, (N, H, dk, dv))
+    if out is None:
+        out = torch.empty((N, H, dv), device=dev, dtype=dtype)
+    else:
+        _require(out, "out", dev, dtype, (N, H, dv))
+    rc = lib.kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(out),
+                        N, H, dk, dv, _DTYPES[dtype], _stream(dev, stream))
+    _lib.check(rc, "kda_decode")
+    return out
+
+
+def state_copy(dst, src, dst_idx=None, src_idx=None, n: Optional[int] = None, stream=None):
+    """dst[dst_idx[i]] = src[src_idx[i]] over whole states (kda_state_copy).
+    dst, src: fp32 [slots, H, d_k, d_v]; indices: int64 device tensors or None (identity)."""
+    lib = _lib.load()
+    dev = dst.device
+    _require(dst, "dst", dev, torch.float32)
+    _require(src, "src", dev, torch.float32)
+    if dst.shape[1:] != src.shape[1:] or dst.dim() != 4:
+        raise ValueError("dst and src must be [slots, H, d_k, d_v] with the same H, d_k, d_v")
+    for t, name in ((dst_idx, "dst_idx"), (src_idx, "src_idx")):
+        if t is not None:
+            _require(t, name, dev, torch.int64)
+    if n is None:
+        n = (dst_idx.numel() if dst_idx is not None else
+             src_idx.numel() if src_idx is not None else min(dst.shape[0], src.shape[0]))
+    _, H, dk, dv = dst.shape
+    rc = lib.kda_state_copy(_ptr(dst), _ptr(dst_idx), dst.shape[0], _ptr(src), _ptr(src_idx),
+                            src.shape[0], int(n), H, dk, dv, _stream(dev, stream))
+    _lib.check(rc, "kda_state_copy")
+    return dst
+
+
+def device_status(stream=None, device=None) -> int:
+    """Synchronize and read-and-clear the library's sticky device error word (0 = OK)."""
+    import ctypes
+
+    lib = _lib.load()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    st = ctypes.c_int32(0)
+    _lib.check(lib.kda_device_status(ctypes.byref(st), _stream(dev, stream)), "kda_device_status")
+    return int(st.value)

@@ -1,0 +1,146 @@
+// kda_capi.cu -- the C ABI of libkda_gb300: host-side argument validation and kernel dispatch.
+// Declarations, argument meaning, layouts and error behaviour: include/kda.h.
+#include <cstdio>
+
+#include "kda_internal.cuh"
+
+using namespace kda;
+
+namespace {
+
+bool bad_dtype(int32_t dtype) { return dtype != KDA_BF16 && dtype != KDA_F32; }
+
+// Validation shared by both prefill entry points.  Returns KDA_OK when the call may launch.
+int check_prefill(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                  const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t n_heads,
+                  int32_t d_k, int32_t d_v, int32_t dtype, const float *init_state, const void *out,
+                  const float *final_state, int32_t ckpt_stride, const float *ckpts)
+{
+    if (n_seqs < 0 || total_tokens < 0 || n_heads < 1 || d_k < 1 || d_v < 1 || bad_dtype(dtype))
+        return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && n_seqs == 0) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens && n_seqs > 1) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;  // cu_seqlens are int32
+    if (ckpt_stride < 0 || ckpt_stride % 64 != 0) return KDA_ERR_INVALID_ARG;
+    if (ckpt_stride > 0 && !ckpts) return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, g, beta, init_state, out, final_state, ckpts};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return KDA_ERR_MISALIGNED;
+    const int esz = dtype == KDA_BF16 ? 2 : 4;
+    // every row of q/k/g/v/out must start 16-byte aligned for the vector and TMA paths
+    if (((int64_t)d_k * esz) % 16 != 0 || ((int64_t)d_v * esz) % 16 != 0) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (out && (out == q || out == k || out == v || out == g || out == beta))
+        return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
+bool tc_supported(int32_t d_k, int32_t d_v, int32_t dtype)
+{
+    return dtype == KDA_BF16 && d_k == 128 && d_v == 128;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+const char *kda_status_string(int status)
+{
+    switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+    case KDA_ERR_UNSUPPORTED_SHAPE: return "KDA_ERR_UNSUPPORTED_SHAPE: head sizes not implemented";
+    case KDA_ERR_MISALIGNED: return "KDA_ERR_MISALIGNED: pointer not 16-byte aligned";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime call or launch failed";
+    case KDA_ERR_DEVICE_TIMEOUT: return "KDA_ERR_DEVICE_TIMEOUT: bounded device wait expired";
+    case KDA_ERR_INDEX_RANGE: return "KDA_ERR_INDEX_RANGE: state index out of range";
+    default: return "KDA_ERR_UNKNOWN";
+    }
+}
+
+int kda_prefill_path(int32_t d_k, int32_t d_v, int32_t dtype)
+{
+    if (d_k < 1 || d_v < 1 || bad_dtype(dtype)) return -KDA_ERR_INVALID_ARG;
+    if (tc_supported(d_k, d_v, dtype)) return 1;
+    if (d_k <= 128 && d_v % 32 == 0 && d_v <= 256) return 0;
+    return -KDA_ERR_UNSUPPORTED_SHAPE;
+}
+
+int kda_prefill(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t n_heads,
+                int32_t d_k, int32_t d_v, int32_t dtype, const float *init_state, void *out,
+                float *final_state, int32_t ckpt_stride, float *ckpts, void *stream)
+{
+    int rc = check_prefill(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, n_heads, d_k, d_v,
+                           dtype, init_state, out, final_state, ckpt_stride, ckpts);
+    if (rc != KDA_OK) return rc;
+    if (tc_supported(d_k, d_v, dtype))
+        return launch_prefill_tc(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, n_heads,
+                                 init_state, out, final_state, ckpt_stride, ckpts,
+                                 (cudaStream_t)stream);
+    return launch_prefill_recurrent(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, n_heads,
+                                    d_k, d_v, dtype, init_state, out, final_state, ckpt_stride,
+                                    ckpts, (cudaStream_t)stream);
+}
+
+int kda_prefill_recurrent(const void *q, const void *k, const void *v, const void *g,
+                          const void *beta, const int32_t *cu_seqlens, int32_t n_seqs,
+                          int64_t total_tokens, int32_t n_heads, int32_t d_k, int32_t d_v,
+                          int32_t dtype, const float *init_state, void *out, float *final_state,
+                          int32_t ckpt_stride, float *ckpts, void *stream)
+{
+    int rc = check_prefill(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, n_heads, d_k, d_v,
+                           dtype, init_state, out, final_state, ckpt_stride, ckpts);
+    if (rc != KDA_OK) return rc;
+    return launch_prefill_recurrent(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, n_heads,
+                                    d_k, d_v, dtype, init_state, out, final_state, ckpt_stride,
+                                    ckpts, (cudaStream_t)stream);
+}
+
+int kda_decode(const void *q, const void *k, const void *v, const void *g, const void *beta,
+               float *state, void *out, int32_t n_seqs, int32_t n_heads, int32_t d_k, int32_t d_v,
+               int32_t dtype, void *stream)
+{
+    if (n_seqs < 0 || n_heads < 1 || d_k < 1 || d_v < 1 || bad_dtype(dtype)) return KDA_ERR_INVALID_ARG;
+    if (n_seqs > 0 && (!q || !k || !v || !g || !beta || !state || !out)) return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, g, beta, state, out};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+    if (out && (out == q || out == k || out == v || out == g || out == beta || out == state))
+        return KDA_ERR_INVALID_ARG;
+    return launch_decode(q, k, v, g, beta, state, out, n_seqs, n_heads, d_k, d_v, dtype,
+                         (cudaStream_t)stream);
+}
+
+int kda_state_copy(float *dst, const int64_t *dst_idx, int64_t n_dst_slots, const float *src,
+                   const int64_t *src_idx, int64_t n_src_slots, int64_t n, int32_t n_heads,
+                   int32_t d_k, int32_t d_v, void *stream)
+{
+    if (n < 0 || n_dst_slots < 0 || n_src_slots < 0 || n_heads < 1 || d_k < 1 || d_v < 1)
+        return KDA_ERR_INVALID_ARG;
+    if (n > 0 && (!dst || !src)) return KDA_ERR_INVALID_ARG;
+    if ((!dst_idx && n > n_dst_slots) || (!src_idx && n > n_src_slots)) return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {dst, dst_idx, src, src_idx};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+    const int64_t unit = (int64_t)n_heads * d_k * d_v;
+    return launch_state_copy(dst, dst_idx, n_dst_slots, src, src_idx, n_src_slots, n, unit,
+                             (cudaStream_t)stream);
+}
+
+int kda_device_status(int32_t *status, void *stream)
+{
+    if (!status) return KDA_ERR_INVALID_ARG;
+    int32_t a = 0, b = 0;
+    int rc = read_and_clear_status_state_copy((cudaStream_t)stream, &a);
+    if (rc != KDA_OK) return rc;
+    rc = read_and_clear_status_prefill_tc((cudaStream_t)stream, &b);
+    if (rc != KDA_OK) return rc;
+    *status = b != KDA_OK ? b : a;
+    return KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// kda_internal.cuh -- helpers shared by the CUDA translation units of libkda_gb300.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+// Element conversions for the two input/output dtypes.
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void store_as(float *p, float x) { *p = x; }
+__device__ __forceinline__ void store_as(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Retention factor of one token for one key channel: exp of the log-decay clamped to the
+// published range [-5, 0] ("Kimi K3 im Detail", section "Sequenz-Mixing", log-decay floor).
+__device__ __forceinline__ float retention(float g) { return expf(fminf(fmaxf(g, -5.0f), 0.0f)); }
+
+__host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Per-translation-unit readers of the sticky device error words (see kda_device_status).
+int read_and_clear_status_state_copy(cudaStream_t s, int32_t *status);
+int read_and_clear_status_prefill_tc(cudaStream_t s, int32_t *status);
+
+// Kernel launchers (host side, no validation: the C ABI validates first).
+int launch_decode(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                  float *state, void *out, int n_seqs, int n_heads, int d_k, int d_v, int dtype,
+                  cudaStream_t stream);
+int launch_state_copy(float *dst, const int64_t *dst_idx, int64_t n_dst, const float *src,
+                      const int64_t *src_idx, int64_t n_src, int64_t n, int64_t unit_floats,
+                      cudaStream_t stream);
+int launch_prefill_recurrent(const void *q, const void *k, const void *v, const void *g,
+                             const void *beta, const int32_t *cu_seqlens, int n_seqs,
+                             int64_t total_tokens, int n_heads, int d_k, int d_v, int dtype,
+                             const float *init_state, void *out, float *final_state,
+                             int ckpt_stride, float *ckpts, cudaStream_t stream);
+int launch_prefill_tc(const void *q, const void *k, const void *v, const void *g,
+                      const void *beta, const int32_t *cu_seqlens, int n_seqs,
+                      int64_t total_tokens, int n_heads, const float *init_state, void *out,
+                      float *final_state, int ckpt_stride, float *ckpts, cudaStream_t stream);
+
+}  // namespace kda

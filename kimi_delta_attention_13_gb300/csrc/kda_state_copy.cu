@@ -1,0 +1,84 @@
+// kda_state_copy.cu -- indexed copy of whole per-sequence KDA states (checkpoint restore).
+//
+// Prefix reuse ("Kimi K3 im Detail", section "Sequenz-Mixing", prefix-reuse paragraph)
+// restarts a sequence from a stored KDA state at the same token boundary as the global
+// attention cache; this kernel moves such states between slot arrays:
+//     dst[dst_idx[i]] = src[src_idx[i]],  one slot = H * d_k * d_v fp32.
+// Pure HBM copy: 128-bit loads and stores, gridDim.y walks the slots, gridDim.x x blockDim.x
+// threads stride through one slot.  Indices outside their slot range skip the copy and set
+// this unit's sticky error word.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+__device__ int g_state_copy_error;  // sticky device error word of this translation unit
+
+template <typename V>
+__global__ void __launch_bounds__(256)
+state_copy_kernel(V *__restrict__ dst, const int64_t *__restrict__ dst_idx, int64_t n_dst,
+                  const V *__restrict__ src, const int64_t *__restrict__ src_idx, int64_t n_src,
+                  int64_t n, int64_t unit_vecs)
+{
+    for (int64_t i = blockIdx.y; i < n; i += gridDim.y) {
+        const int64_t d = dst_idx ? dst_idx[i] : i;
+        const int64_t s = src_idx ? src_idx[i] : i;
+        if (d < 0 || d >= n_dst || s < 0 || s >= n_src) {
+            if (threadIdx.x == 0 && blockIdx.x == 0) atomicExch(&g_state_copy_error, KDA_ERR_INDEX_RANGE);
+            continue;
+        }
+        V *out = dst + d * unit_vecs;
+        const V *in = src + s * unit_vecs;
+        for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < unit_vecs;
+             e += (int64_t)gridDim.x * blockDim.x)
+            out[e] = __ldcs(in + e);
+    }
+}
+
+}  // namespace
+
+int read_and_clear_status_state_copy(cudaStream_t s, int32_t *status)
+{
+    int host = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&host, g_state_copy_error, sizeof(int), 0,
+                                  cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (cudaMemcpyToSymbolAsync(g_state_copy_error, &zero, sizeof(int), 0,
+                                cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    *status = host;
+    return KDA_OK;
+}
+
+int launch_state_copy(float *dst, const int64_t *dst_idx, int64_t n_dst, const float *src,
+                      const int64_t *src_idx, int64_t n_src, int64_t n, int64_t unit_floats,
+                      cudaStream_t stream)
+{
+    if (n == 0 || unit_floats == 0) return KDA_OK;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const unsigned ys = (unsigned)(n < 65535 ? n : 65535);
+    if (unit_floats % 4 == 0) {
+        const int64_t vecs = unit_floats / 4;
+        // enough blocks per slot that all SMs stream when few slots are copied
+        int64_t bx = (4LL * sms + ys - 1) / ys;
+        const int64_t need = (vecs + 255) / 256;
+        if (bx > need) bx = need;
+        if (bx < 1) bx = 1;
+        state_copy_kernel<float4><<<dim3((unsigned)bx, ys), 256, 0, stream>>>(
+            reinterpret_cast<float4 *>(dst), dst_idx, n_dst, reinterpret_cast<const float4 *>(src),
+            src_idx, n_src, n, vecs);
+    } else {
+        int64_t bx = (4LL * sms + ys - 1) / ys;
+        const int64_t need = (unit_floats + 255) / 256;
+        if (bx > need) bx = need;
+        if (bx < 1) bx = 1;
+        state_copy_kernel<float><<<dim3((unsigned)bx, ys), 256, 0, stream>>>(
+            dst, dst_idx, n_dst, src, src_idx, n_src, n, unit_floats);
+    }
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace kda

@@ -1,0 +1,116 @@
+"""The C ABI library without a GPU: it builds, loads, exports every function include/kda.h
+declares, and its host-side validation rejects bad arguments before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from kimi_delta_attention_13_gb300 import _lib, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for fn in ("kda_prefill", "kda_decode", "kda_state_copy", "kda_status_string"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert names
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in include/kda.h but not exported"
+    assert set(names) == set(_lib.SIGNATURES), "binding signatures out of sync with the header"
+
+
+def test_abi_version_matches_header(lib):
+    m = re.search(r"#define KDA_ABI_VERSION (\d+)", open(HEADER).read())
+    assert lib.kda_abi_version() == int(m.group(1))
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS_NAMES.items():
+        assert lib.kda_status_string(code).decode().startswith(name)
+    assert lib.kda_status_string(99).decode() == "KDA_ERR_UNKNOWN"
+
+
+def test_prefill_path(lib):
+    assert lib.kda_prefill_path(128, 128, 0) == 1      # bf16, d=128: tensor-core kernel
+    assert lib.kda_prefill_path(128, 128, 1) == 0      # fp32: per-token kernel
+    assert lib.kda_prefill_path(64, 32, 0) == 0
+    assert lib.kda_prefill_path(129, 128, 1) == -2
+    assert lib.kda_prefill_path(128, 128, 7) == -1
+
+
+A = 1 << 20  # a fake, 16-byte aligned "device address" that is never dereferenced
+
+
+def _prefill(lib, **over):
+    args = dict(q=A, k=A + 16, v=A + 32, g=A + 48, beta=A + 64, cu=None, n=1, T=16, H=2, dk=128,
+                dv=128, dtype=0, init=None, out=A + 80, fin=None, stride=0, ckpts=None, stream=None)
+    args.update(over)
+    return lib.kda_prefill(args["q"], args["k"], args["v"], args["g"], args["beta"], args["cu"],
+                           args["n"], args["T"], args["H"], args["dk"], args["dv"], args["dtype"],
+                           args["init"], args["out"], args["fin"], args["stride"], args["ckpts"],
+                           args["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(H=0), 1), (dict(n=-1), 1), (dict(T=-5), 1), (dict(dtype=3), 1), (dict(q=None), 1),
+    (dict(n=2), 1),                       # two sequences need cu_seqlens
+    (dict(stride=48), 1),                 # not a multiple of 64
+    (dict(stride=64), 1),                 # checkpoints requested without a buffer
+    (dict(out=A), 1),                     # out aliases q
+    (dict(q=A + 8), 3), (dict(fin=A + 100), 3), (dict(cu=A + 2), 3),
+    (dict(dk=129, dtype=1), 2), (dict(dk=130, dtype=1), 2), (dict(dk=60, dv=64, dtype=0), 2),
+])
+def test_prefill_rejects(lib, over, code):
+    assert _prefill(lib, **over) == code
+
+
+def test_recurrent_rejects_unsupported_dv(lib):
+    # validation passes, the launcher refuses the shape before touching CUDA
+    rc = lib.kda_prefill_recurrent(A, A, A, A, A, None, 1, 16, 2, 128, 48, 1, None, A + 4096, None,
+                                   0, None, None)
+    assert rc == 2
+
+
+def test_decode_rejects(lib):
+    f = lib.kda_decode
+    assert f(A, A, A, A, A, A, A + 16, -1, 2, 128, 128, 0, None) == 1
+    assert f(A, A, A, A, A, None, A + 16, 4, 2, 128, 128, 0, None) == 1
+    assert f(A, A, A, A, A, A + 4, A + 16, 4, 2, 128, 128, 0, None) == 3
+    assert f(A, A, A, A, A, A + 32, A + 16, 4, 2, 200, 128, 0, None) == 2
+    assert f(A, A, A, A, A, A + 32, A + 16, 4, 2, 128, 130, 0, None) == 2
+    assert f(A, A, A, A, A, A + 32, A, 4, 2, 128, 128, 0, None) == 1   # out aliases q
+
+
+def test_state_copy_rejects(lib):
+    f = lib.kda_state_copy
+    assert f(A, None, 2, A + 4096, None, 4, 3, 2, 128, 128, None) == 1   # identity beyond dst slots
+    assert f(None, None, 2, A, None, 2, 1, 2, 128, 128, None) == 1
+    assert f(A + 4, None, 2, A, None, 2, 1, 2, 128, 128, None) == 3
+    assert f(A, None, 2, A, None, 2, 1, 0, 128, 128, None) == 1
+
+
+def test_binding_refuses_cpu_tensors():
+    import kimi_delta_attention_13_gb300 as kda
+
+    x = torch.zeros(4, 2, 128)
+    with pytest.raises(ValueError, match="CUDA"):
+        kda.prefill(x, x, x, x, torch.zeros(4, 2))

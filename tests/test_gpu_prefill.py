@@ -1,0 +1,180 @@
+"""kda_prefill / kda_prefill_recurrent on the GPU against the fp64 oracle, element by element.
+
+Small cases span several 16-token tiles, ragged tails, empty and one-token sequences,
+nonzero start states and checkpoints; the full-size workloads run in the same launch
+configuration the benchmark times and are checked on all heads (T=8192) or on seeded head
+samples (varlen x8, T=262144).
+"""
+import pytest
+import torch
+
+import kimi_delta_attention_13_gb300 as kda
+import oracle
+from kimi_delta_attention_13_gb300 import synth
+from parity import TOL, assert_close, head_slice
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+PATHS = {"prefill": kda.prefill, "recurrent": kda.prefill_recurrent}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    yield
+    torch.cuda.empty_cache()
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.default()
+
+
+def run_and_check(orc, x, path="prefill", ckpt_stride=0, dtype="bf16", heads=None):
+    fn = PATHS[path]
+    out, fin, ck = fn(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], x["state"],
+                      ckpt_stride=ckpt_stride, lengths=x["lengths"])
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    tol = TOL[dtype]
+    if heads is None:
+        ro, rf, rc = orc.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"].cpu(),
+                                 x["state"], ckpt_stride=ckpt_stride)
+        sel = lambda t: t  # noqa: E731
+    else:
+        hs = head_slice(x, heads)
+        init = None if x["state"] is None else x["state"][:, heads]
+        ro, rf, rc = orc.prefill(hs["q"], hs["k"], hs["v"], hs["g"], hs["beta"],
+                                 x["cu_seqlens"].cpu(), init, ckpt_stride=ckpt_stride)
+        idx = torch.as_tensor(heads, device=DEV)
+        sel = lambda t: t.index_select(1, idx)  # noqa: E731
+    errs = {"out": assert_close("out", sel(out), ro, tol["out"]),
+            "final": assert_close("final", sel(fin), rf, tol["state"])}
+    if ckpt_stride:
+        assert ck.shape[0] == (rc.shape[0] if rc is not None else 0)
+        if rc is not None:
+            errs["ckpts"] = assert_close("ckpts", sel(ck), rc, tol["state"])
+    return errs, (out, fin, ck)
+
+
+def test_tiny_f32_workload(orc):
+    w = synth.workloads()[0]
+    x = synth.make_workload_inputs(w, DEV)
+    assert kda.prefill_path(128, 128, torch.float32) == 0
+    run_and_check(orc, x, dtype="f32")
+
+
+@pytest.mark.parametrize("path", ["prefill", "recurrent"])
+@pytest.mark.parametrize("lengths", [[1], [15], [16], [17], [33], [100], [257],
+                                     [5, 64, 0, 130, 1, 200], [128, 128, 128]])
+def test_small_bf16(orc, path, lengths):
+    x = synth.make_inputs(lengths, heads=3, dtype="bf16", seed=sum(lengths) + len(lengths),
+                          device=DEV, init_state=True)
+    run_and_check(orc, x, path=path, ckpt_stride=64)
+
+
+@pytest.mark.parametrize("lengths", [[64], [3, 70, 0, 129]])
+def test_small_f32_with_checkpoints(orc, lengths):
+    x = synth.make_inputs(lengths, heads=2, dtype="f32", seed=7, device=DEV, init_state=True)
+    run_and_check(orc, x, ckpt_stride=64, dtype="f32")
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 32), (1, 32), (128, 256), (72, 96)])
+def test_other_head_sizes_recurrent(orc, dk, dv):
+    x = synth.make_inputs([40, 9], heads=2, d_k=dk, d_v=dv, dtype="f32", seed=dk + dv, device=DEV,
+                          init_state=True)
+    run_and_check(orc, x, path="recurrent", dtype="f32")
+
+
+@pytest.mark.parametrize("path", ["prefill", "recurrent"])
+def test_slow_decay_carries_state(orc, path):
+    """g scaled by 0.01: the state carries over hundreds of tokens, so inter-chunk carry
+    errors cannot hide behind fast forgetting (T=8192, 4 heads)."""
+    x = synth.make_inputs([8192], heads=4, dtype="bf16", seed=21, device=DEV, decay_scale=0.01)
+    run_and_check(orc, x, path=path)
+
+
+def test_extreme_decay_floor(orc):
+    """g at the floor -5 (and below, clamped) on every channel: 16-token tiles reach the -80
+    cumulative bound exactly; nothing may overflow."""
+    x = synth.make_inputs([300], heads=2, dtype="bf16", seed=22, device=DEV, init_state=True)
+    x["g"].fill_(-5.0)
+    x["g"][::7] = -9.0
+    run_and_check(orc, x)
+
+
+def test_zero_gates_keep_state(orc):
+    """beta = 0 and g = 0: the final state equals the initial one and o_t = S_0^T q_t."""
+    x = synth.make_inputs([50, 70], heads=2, dtype="bf16", seed=23, device=DEV, init_state=True)
+    x["beta"].zero_()
+    x["g"].zero_()
+    _, (out, fin, _) = run_and_check(orc, x)
+    assert_close("final==init", fin, x["state"].double().cpu().numpy(), 1e-2)
+
+
+def test_resume_from_split_equals_uninterrupted(orc):
+    """prefill(x[:a]) then prefill(x[a:], init=final) matches one prefill of x (both checked
+    against the oracle's uninterrupted run)."""
+    x = synth.make_inputs([1000], heads=2, dtype="bf16", seed=24, device=DEV, init_state=True)
+    ro, rf, _ = orc.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], None, x["state"])
+    a = 384
+    part = {k: x[k][:a] for k in ("q", "k", "v", "g", "beta")}
+    o1, s1, _ = kda.prefill(**part, init_state=x["state"])
+    rest = {k: x[k][a:].contiguous() for k in ("q", "k", "v", "g", "beta")}
+    o2, s2, _ = kda.prefill(**rest, init_state=s1)
+    torch.cuda.synchronize()
+    assert_close("out", torch.cat([o1, o2]), ro, TOL["bf16"]["out"])
+    assert_close("final", s2, rf, TOL["bf16"]["state"])
+
+
+def test_in_place_resume(orc):
+    """init_state and final_state may be the same buffer."""
+    x = synth.make_inputs([200], heads=2, dtype="bf16", seed=25, device=DEV, init_state=True)
+    ro, rf, _ = orc.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], None, x["state"])
+    S = x["state"].clone()
+    out, fin, _ = kda.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], init_state=S, final_state=S)
+    torch.cuda.synchronize()
+    assert fin is S
+    assert_close("final", S, rf, TOL["bf16"]["state"])
+    assert_close("out", out, ro, TOL["bf16"]["out"])
+
+
+def test_empty_batches():
+    x = synth.make_inputs([0, 0], heads=2, dtype="bf16", seed=26, device=DEV, init_state=True)
+    out, fin, _ = kda.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], x["state"])
+    torch.cuda.synchronize()
+    assert out.shape[0] == 0
+    assert torch.equal(fin, x["state"])
+    out, fin, _ = kda.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(fin) == 0
+
+
+# --- full-size workloads, in the benchmark's launch configuration ---------------------------------
+
+def test_workload_prefill_T8192_all_heads(orc):
+    w = synth.workloads()[1]
+    x = synth.make_workload_inputs(w, DEV)
+    errs, _ = run_and_check(orc, x)
+    print("T8192", errs)
+
+
+def test_workload_varlen8_sampled_heads(orc):
+    w = synth.workloads()[2]
+    x = synth.make_workload_inputs(w, DEV)
+    heads = sorted(torch.randperm(96, generator=torch.Generator().manual_seed(202))[:6].tolist())
+    errs, _ = run_and_check(orc, x, heads=heads)
+    print("varlen8", w.lengths, errs)
+
+
+def test_workload_long_context_checkpoints(orc):
+    w = synth.workloads()[4]
+    x = synth.make_workload_inputs(w, DEV)
+    errs, (out, fin, ck) = run_and_check(orc, x, ckpt_stride=w.ckpt_stride, heads=w.oracle_heads)
+    assert ck.shape[0] == 64
+    # the last checkpoint is the final state (the stride divides the length)
+    assert torch.equal(ck[-1], fin[0])
+    print("T262144", errs)
