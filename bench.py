@@ -35,9 +35,9 @@ H, D = 96, 128
 T1 = 8192                      # prefill workload: one sequence of 8192 tokens
 N_DEC = 256                    # decode workload: 256 sequences
 FLOP_PER_TOKEN_HEAD = 6 * D * D + 8 * 16 * D        # 114,688 (chunk C = 16 accounting)
-BYTES_PER_TOKEN_HEAD = 5 * D * 2 + 2                # q, k, v, g, o bf16 + beta = 1,282
+BYTES_PER_TOKEN_HEAD = 4 * D * 2 + 2 + D * 4        # q, k, v, g bf16 + beta bf16 + o fp32 = 1,538
 STATE_BYTES = D * D * 4                             # 65,536 per (sequence, head)
-DECODE_BYTES_PER_SEQ_HEAD = 2 * STATE_BYTES + 4 * D * 2 + 2 + D * 2   # 132,354
+DECODE_BYTES_PER_SEQ_HEAD = 2 * STATE_BYTES + 4 * D * 2 + 2 + D * 4   # 132,610
 
 
 def load_peaks():
@@ -197,7 +197,7 @@ def run_gb300(args):
 
     # ---- prefill workload (inputs resident in HBM, 1.0 GB: larger than L2) -----------------
     x = synth.make_inputs([T1], heads=H, dtype="bf16", seed=1, device=dev)
-    out = torch.empty(T1, H, D, device=dev, dtype=torch.bfloat16)
+    out = torch.empty(T1, H, D, device=dev, dtype=torch.float32)
     fin = torch.empty(1, H, D, D, device=dev, dtype=torch.float32)
 
     def prefill_step():
@@ -235,7 +235,7 @@ def run_gb300(args):
 
     # ---- end to end through the public API: pinned host inputs -> device -> host outputs -----
     hx = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
-    h_out = torch.empty(T1, H, D, dtype=torch.bfloat16).pin_memory()
+    h_out = torch.empty(T1, H, D, dtype=torch.float32).pin_memory()
     h_fin = torch.empty(1, H, D, D, dtype=torch.float32).pin_memory()
     del x
 
@@ -250,13 +250,13 @@ def run_gb300(args):
     barrier()
     e2e_ms, e2e_per = cuda_time_ms(e2e_step, max(3, args.steps // 2), stream)
     h2d = sum(v.numel() * v.element_size() for v in hx.values())
-    d2h = h_out.numel() * 2 + h_fin.numel() * 4
+    d2h = h_out.numel() * 4 + h_fin.numel() * 4
     del hx, h_out, h_fin
     torch.cuda.empty_cache()
 
     # ---- decode workload: 256 x 96 states (1.6 GB fp32), updated in place -----------------
     d = synth.make_decode_inputs(N_DEC, heads=H, seed=3, device=dev)
-    dout = torch.empty(N_DEC, H, D, device=dev, dtype=torch.bfloat16)
+    dout = torch.empty(N_DEC, H, D, device=dev, dtype=torch.float32)
 
     def decode_step():
         kda.decode(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state"], out=dout, stream=stream)
@@ -303,8 +303,8 @@ def run_gb300(args):
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": per_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"prefill T={T1} H={H} d_k=d_v={D} bf16 in/out, fp32 state, zero "
-                               "initial state, final state written (one sequence)",
+        "config": {"workload": f"prefill T={T1} H={H} d_k=d_v={D}: bf16 q/k/v/g/beta, fp32 out and "
+                               "state, zero initial state, final state written (one sequence)",
                    "global_batch": world, "seq_len": T1, "heads": H, "head_dim": D,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (1.0 GB read per step), no flush needed",

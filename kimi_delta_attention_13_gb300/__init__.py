@@ -66,7 +66,7 @@ def prefill_path(d_k: int = 128, d_v: int = 128, dtype=torch.bfloat16) -> int:
 
 
 def _prefill(fn_name, q, k, v, g, beta, cu_seqlens, init_state, out, final_state, ckpt_stride,
-             ckpts, lengths, stream):
+             ckpts, lengths, stream, out_dtype):
     lib = _lib.load()
     dev = q.device
     dtype = q.dtype
@@ -84,10 +84,12 @@ def _prefill(fn_name, q, k, v, g, beta, cu_seqlens, init_state, out, final_state
         n = cu_seqlens.numel() - 1
     if init_state is not None:
         _require(init_state, "init_state", dev, torch.float32, (n, H, dk, dv))
+    if out_dtype not in _DTYPES:
+        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
     if out is None:
-        out = torch.empty((T, H, dv), device=dev, dtype=dtype)
+        out = torch.empty((T, H, dv), device=dev, dtype=out_dtype)
     else:
-        _require(out, "out", dev, dtype, (T, H, dv))
+        _require(out, "out", dev, out_dtype, (T, H, dv))
     if final_state is True:
         final_state = torch.empty((n, H, dk, dv), device=dev, dtype=torch.float32)
     elif final_state is False or final_state is None:
@@ -103,35 +105,38 @@ def _prefill(fn_name, q, k, v, g, beta, cu_seqlens, init_state, out, final_state
         _require(ckpts, "ckpts", dev, torch.float32)
     rc = getattr(lib, fn_name)(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), n, T, H, dk, dv,
-        _DTYPES[dtype], _ptr(init_state), _ptr(out), _ptr(final_state), int(ckpt_stride),
+        _DTYPES[dtype], _DTYPES[out_dtype], _ptr(init_state), _ptr(out), _ptr(final_state),
+        int(ckpt_stride),
         _ptr(ckpts), _stream(dev, stream))
     _lib.check(rc, fn_name)
     return out, final_state, ckpts
 
 
 def prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, *, out=None, final_state=True,
-            ckpt_stride: int = 0, ckpts=None, lengths=None, stream=None):
+            ckpt_stride: int = 0, ckpts=None, lengths=None, stream=None, out_dtype=torch.float32):
     """Varlen chunked KDA prefill (kda_prefill).
 
     q, k, g: [T, H, d_k]; v: [T, H, d_v]; beta: [T, H] (bf16 or fp32, contiguous, CUDA);
     cu_seqlens: int32 [N+1] on the device or None for one sequence; init_state: fp32
     [N, H, d_k, d_v] or None (zeros).  final_state: True to allocate, a tensor to fill, or
-    None/False.  ckpt_stride: 0 or a multiple of 64.  Returns (out, final_state, ckpts).
+    None/False.  ckpt_stride: 0 or a multiple of 64.  out_dtype: float32 (default, the
+    accumulation precision) or bfloat16.  Returns (out, final_state, ckpts).
     """
     return _prefill("kda_prefill", q, k, v, g, beta, cu_seqlens, init_state, out, final_state,
-                    ckpt_stride, ckpts, lengths, stream)
+                    ckpt_stride, ckpts, lengths, stream, out_dtype)
 
 
 def prefill_recurrent(q, k, v, g, beta, cu_seqlens=None, init_state=None, *, out=None,
-                      final_state=True, ckpt_stride: int = 0, ckpts=None, lengths=None, stream=None):
+                      final_state=True, ckpt_stride: int = 0, ckpts=None, lengths=None, stream=None,
+                      out_dtype=torch.float32):
     """Same as prefill, always through the token-by-token CUDA-core kernel."""
     return _prefill("kda_prefill_recurrent", q, k, v, g, beta, cu_seqlens, init_state, out,
-                    final_state, ckpt_stride, ckpts, lengths, stream)
+                    final_state, ckpt_stride, ckpts, lengths, stream, out_dtype)
 
 
-def decode(q, k, v, g, beta, state, *, out=None, stream=None):
+def decode(q, k, v, g, beta, state, *, out=None, stream=None, out_dtype=torch.float32):
     """One-token KDA update (kda_decode): state [N, H, d_k, d_v] fp32 is updated in place.
-    q, k, g: [N, H, d_k]; v: [N, H, d_v]; beta: [N, H].  Returns out [N, H, d_v]."""
+    q, k, g: [N, H, d_k]; v: [N, H, d_v]; beta: [N, H].  Returns out [N, H, d_v] (out_dtype)."""
     lib = _lib.load()
     dev, dtype = q.device, q.dtype
     N, H, dk = q.shape
@@ -141,11 +146,11 @@ def decode(q, k, v, g, beta, state, *, out=None, stream=None):
         _require(t, name, dev, dtype, shp)
     _require(state, "state", dev, torch.float32, (N, H, dk, dv))
     if out is None:
-        out = torch.empty((N, H, dv), device=dev, dtype=dtype)
+        out = torch.empty((N, H, dv), device=dev, dtype=out_dtype)
     else:
-        _require(out, "out", dev, dtype, (N, H, dv))
+        _require(out, "out", dev, out_dtype, (N, H, dv))
     rc = lib.kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(out),
-                        N, H, dk, dv, _DTYPES[dtype], _stream(dev, stream))
+                        N, H, dk, dv, _DTYPES[dtype], _DTYPES[out.dtype], _stream(dev, stream))
     _lib.check(rc, "kda_decode")
     return out
 

@@ -19,15 +19,16 @@ STATUS_NAMES = {
 
 # name -> (restype, argtypes); every function declared in include/kda.h
 _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
-_PREFILL_ARGS = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
-                 _i32, _vp, _vp]
+_PREFILL_ARGS = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, _i32, _vp, _vp,
+                 _vp, _i32, _vp, _vp]
 SIGNATURES = {
     "kda_abi_version": (ctypes.c_int, []),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kda_prefill": (ctypes.c_int, _PREFILL_ARGS),
     "kda_prefill_recurrent": (ctypes.c_int, _PREFILL_ARGS),
     "kda_prefill_path": (ctypes.c_int, [_i32, _i32, _i32]),
-    "kda_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]),
+    "kda_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                   _vp]),
     "kda_state_copy": (ctypes.c_int, [_vp, _vp, _i64, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp]),
     "kda_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _vp]),
 }

@@ -13,10 +13,12 @@ bool bad_dtype(int32_t dtype) { return dtype != KDA_BF16 && dtype != KDA_F32; }
 // Validation shared by both prefill entry points.  Returns KDA_OK when the call may launch.
 int check_prefill(const void *q, const void *k, const void *v, const void *g, const void *beta,
                   const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t n_heads,
-                  int32_t d_k, int32_t d_v, int32_t dtype, const float *init_state, const void *out,
-                  const float *final_state, int32_t ckpt_stride, const float *ckpts)
+                  int32_t d_k, int32_t d_v, int32_t dtype, int32_t out_dtype,
+                  const float *init_state, const void *out, const float *final_state,
+                  int32_t ckpt_stride, const float *ckpts)
 {
-    if (n_seqs < 0 || total_tokens < 0 || n_heads < 1 || d_k < 1 || d_v < 1 || bad_dtype(dtype))
+    if (n_seqs < 0 || total_tokens < 0 || n_heads < 1 || d_k < 1 || d_v < 1 || bad_dtype(dtype) ||
+        bad_dtype(out_dtype))
         return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0 && n_seqs == 0) return KDA_ERR_INVALID_ARG;
@@ -28,9 +30,11 @@ int check_prefill(const void *q, const void *k, const void *v, const void *g, co
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
     if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return KDA_ERR_MISALIGNED;
-    const int esz = dtype == KDA_BF16 ? 2 : 4;
+    const int esz = dtype == KDA_BF16 ? 2 : 4, osz = out_dtype == KDA_BF16 ? 2 : 4;
     // every row of q/k/g/v/out must start 16-byte aligned for the vector and TMA paths
-    if (((int64_t)d_k * esz) % 16 != 0 || ((int64_t)d_v * esz) % 16 != 0) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (((int64_t)d_k * esz) % 16 != 0 || ((int64_t)d_v * esz) % 16 != 0 ||
+        ((int64_t)d_v * osz) % 16 != 0)
+        return KDA_ERR_UNSUPPORTED_SHAPE;
     if (out && (out == q || out == k || out == v || out == g || out == beta))
         return KDA_ERR_INVALID_ARG;
     return KDA_OK;
@@ -71,47 +75,48 @@ int kda_prefill_path(int32_t d_k, int32_t d_v, int32_t dtype)
 
 int kda_prefill(const void *q, const void *k, const void *v, const void *g, const void *beta,
                 const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t n_heads,
-                int32_t d_k, int32_t d_v, int32_t dtype, const float *init_state, void *out,
-                float *final_state, int32_t ckpt_stride, float *ckpts, void *stream)
+                int32_t d_k, int32_t d_v, int32_t dtype, int32_t out_dtype, const float *init_state,
+                void *out, float *final_state, int32_t ckpt_stride, float *ckpts, void *stream)
 {
     int rc = check_prefill(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, n_heads, d_k, d_v,
-                           dtype, init_state, out, final_state, ckpt_stride, ckpts);
+                           dtype, out_dtype, init_state, out, final_state, ckpt_stride, ckpts);
     if (rc != KDA_OK) return rc;
-    if (tc_supported(d_k, d_v, dtype))
+    if (tc_supported(d_k, d_v, dtype) && total_tokens > 0)
         return launch_prefill_tc(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, n_heads,
-                                 init_state, out, final_state, ckpt_stride, ckpts,
+                                 out_dtype, init_state, out, final_state, ckpt_stride, ckpts,
                                  (cudaStream_t)stream);
     return launch_prefill_recurrent(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, n_heads,
-                                    d_k, d_v, dtype, init_state, out, final_state, ckpt_stride,
-                                    ckpts, (cudaStream_t)stream);
+                                    d_k, d_v, dtype, out_dtype, init_state, out, final_state,
+                                    ckpt_stride, ckpts, (cudaStream_t)stream);
 }
 
 int kda_prefill_recurrent(const void *q, const void *k, const void *v, const void *g,
                           const void *beta, const int32_t *cu_seqlens, int32_t n_seqs,
                           int64_t total_tokens, int32_t n_heads, int32_t d_k, int32_t d_v,
-                          int32_t dtype, const float *init_state, void *out, float *final_state,
-                          int32_t ckpt_stride, float *ckpts, void *stream)
+                          int32_t dtype, int32_t out_dtype, const float *init_state, void *out,
+                          float *final_state, int32_t ckpt_stride, float *ckpts, void *stream)
 {
     int rc = check_prefill(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, n_heads, d_k, d_v,
-                           dtype, init_state, out, final_state, ckpt_stride, ckpts);
+                           dtype, out_dtype, init_state, out, final_state, ckpt_stride, ckpts);
     if (rc != KDA_OK) return rc;
     return launch_prefill_recurrent(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, n_heads,
-                                    d_k, d_v, dtype, init_state, out, final_state, ckpt_stride,
-                                    ckpts, (cudaStream_t)stream);
+                                    d_k, d_v, dtype, out_dtype, init_state, out, final_state,
+                                    ckpt_stride, ckpts, (cudaStream_t)stream);
 }
 
 int kda_decode(const void *q, const void *k, const void *v, const void *g, const void *beta,
                float *state, void *out, int32_t n_seqs, int32_t n_heads, int32_t d_k, int32_t d_v,
-               int32_t dtype, void *stream)
+               int32_t dtype, int32_t out_dtype, void *stream)
 {
-    if (n_seqs < 0 || n_heads < 1 || d_k < 1 || d_v < 1 || bad_dtype(dtype)) return KDA_ERR_INVALID_ARG;
+    if (n_seqs < 0 || n_heads < 1 || d_k < 1 || d_v < 1 || bad_dtype(dtype) || bad_dtype(out_dtype))
+        return KDA_ERR_INVALID_ARG;
     if (n_seqs > 0 && (!q || !k || !v || !g || !beta || !state || !out)) return KDA_ERR_INVALID_ARG;
     const void *ptrs[] = {q, k, v, g, beta, state, out};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
     if (out && (out == q || out == k || out == v || out == g || out == beta || out == state))
         return KDA_ERR_INVALID_ARG;
-    return launch_decode(q, k, v, g, beta, state, out, n_seqs, n_heads, d_k, d_v, dtype,
+    return launch_decode(q, k, v, g, beta, state, out, n_seqs, n_heads, d_k, d_v, dtype, out_dtype,
                          (cudaStream_t)stream);
 }
 

@@ -24,11 +24,11 @@ constexpr int kMaxDk = 128;
 constexpr int kMaxDv = 128;
 constexpr int kRowsPerWarp = kMaxDk / kWarps;  // 16
 
-template <typename T>
+template <typename T, typename TO>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const T *__restrict__ g, const T *__restrict__ beta, float *__restrict__ state,
-              T *__restrict__ out, int dk, int dv)
+              TO *__restrict__ out, int dk, int dv)
 {
     const int64_t nh = blockIdx.x;  // sequence * H + head
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -106,7 +106,7 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 
     if (warp == 0) {
         const float kq = s_kq;
-        T *o = out + nh * dv + 4 * lane;
+        TO *o = out + nh * dv + 4 * lane;
 #pragma unroll
         for (int c = 0; c < 4; ++c) store_as(o + c, s_r[1][4 * lane + c] + kq * u[c]);
     }
@@ -128,22 +128,24 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 
 int launch_decode(const void *q, const void *k, const void *v, const void *g, const void *beta,
                   float *state, void *out, int n_seqs, int n_heads, int d_k, int d_v, int dtype,
-                  cudaStream_t stream)
+                  int out_dtype, cudaStream_t stream)
 {
     if (d_k < 1 || d_k > kMaxDk || d_v < 4 || d_v > kMaxDv || d_v % 4 != 0)
         return KDA_ERR_UNSUPPORTED_SHAPE;
     const int64_t blocks = (int64_t)n_seqs * n_heads;
     if (blocks == 0) return KDA_OK;
     if (blocks > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
-    if (dtype == KDA_BF16) {
-        using T = __nv_bfloat16;
-        decode_kernel<T><<<(unsigned)blocks, kThreads, 0, stream>>>(
+    auto go = [&](auto in_tag, auto out_tag) {
+        using T = decltype(in_tag);
+        using TO = decltype(out_tag);
+        decode_kernel<T, TO><<<(unsigned)blocks, kThreads, 0, stream>>>(
             (const T *)q, (const T *)k, (const T *)v, (const T *)g, (const T *)beta, state,
-            (T *)out, d_k, d_v);
+            (TO *)out, d_k, d_v);
+    };
+    if (dtype == KDA_BF16) {
+        if (out_dtype == KDA_BF16) go(__nv_bfloat16{}, __nv_bfloat16{}); else go(__nv_bfloat16{}, float{});
     } else {
-        decode_kernel<float><<<(unsigned)blocks, kThreads, 0, stream>>>(
-            (const float *)q, (const float *)k, (const float *)v, (const float *)g,
-            (const float *)beta, state, (float *)out, d_k, d_v);
+        if (out_dtype == KDA_BF16) go(float{}, __nv_bfloat16{}); else go(float{}, float{});
     }
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -30,18 +30,19 @@ int read_and_clear_status_prefill_tc(cudaStream_t s, int32_t *status);
 // Kernel launchers (host side, no validation: the C ABI validates first).
 int launch_decode(const void *q, const void *k, const void *v, const void *g, const void *beta,
                   float *state, void *out, int n_seqs, int n_heads, int d_k, int d_v, int dtype,
-                  cudaStream_t stream);
+                  int out_dtype, cudaStream_t stream);
 int launch_state_copy(float *dst, const int64_t *dst_idx, int64_t n_dst, const float *src,
                       const int64_t *src_idx, int64_t n_src, int64_t n, int64_t unit_floats,
                       cudaStream_t stream);
 int launch_prefill_recurrent(const void *q, const void *k, const void *v, const void *g,
                              const void *beta, const int32_t *cu_seqlens, int n_seqs,
                              int64_t total_tokens, int n_heads, int d_k, int d_v, int dtype,
-                             const float *init_state, void *out, float *final_state,
+                             int out_dtype, const float *init_state, void *out, float *final_state,
                              int ckpt_stride, float *ckpts, cudaStream_t stream);
 int launch_prefill_tc(const void *q, const void *k, const void *v, const void *g,
                       const void *beta, const int32_t *cu_seqlens, int n_seqs,
-                      int64_t total_tokens, int n_heads, const float *init_state, void *out,
-                      float *final_state, int ckpt_stride, float *ckpts, cudaStream_t stream);
+                      int64_t total_tokens, int n_heads, int out_dtype, const float *init_state,
+                      void *out, float *final_state, int ckpt_stride, float *ckpts,
+                      cudaStream_t stream);
 
 }  // namespace kda

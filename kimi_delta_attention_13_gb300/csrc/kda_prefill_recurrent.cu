@@ -21,12 +21,12 @@ constexpr int kMaxDk = 128;
 constexpr int kRows = kMaxDk / 4;  // key rows per thread
 constexpr int kStage = 16;         // tokens staged per shared-memory fill
 
-template <typename T>
+template <typename T, typename TO>
 __global__ void __launch_bounds__(kThreads)
 prefill_recurrent_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                          const T *__restrict__ g, const T *__restrict__ beta,
                          const int32_t *__restrict__ cu_seqlens, int64_t total_tokens, int H,
-                         int dk, int dv, const float *__restrict__ init, T *__restrict__ out,
+                         int dk, int dv, const float *__restrict__ init, TO *__restrict__ out,
                          float *__restrict__ final_state, int ckpt_stride, float *__restrict__ ckpts)
 {
     const int n_slices = dv / kSlice;
@@ -131,7 +131,7 @@ prefill_recurrent_kernel(const T *__restrict__ q, const T *__restrict__ k, const
 int launch_prefill_recurrent(const void *q, const void *k, const void *v, const void *g,
                              const void *beta, const int32_t *cu_seqlens, int n_seqs,
                              int64_t total_tokens, int n_heads, int d_k, int d_v, int dtype,
-                             const float *init_state, void *out, float *final_state,
+                             int out_dtype, const float *init_state, void *out, float *final_state,
                              int ckpt_stride, float *ckpts, cudaStream_t stream)
 {
     if (d_k < 1 || d_k > kMaxDk || d_v < kSlice || d_v > 256 || d_v % kSlice != 0)
@@ -139,16 +139,17 @@ int launch_prefill_recurrent(const void *q, const void *k, const void *v, const 
     const int64_t blocks = (int64_t)n_seqs * n_heads * (d_v / kSlice);
     if (blocks == 0) return KDA_OK;
     if (blocks > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
-    if (dtype == KDA_BF16) {
-        using T = __nv_bfloat16;
-        prefill_recurrent_kernel<T><<<(unsigned)blocks, kThreads, 0, stream>>>(
+    auto go = [&](auto in_tag, auto out_tag) {
+        using T = decltype(in_tag);
+        using TO = decltype(out_tag);
+        prefill_recurrent_kernel<T, TO><<<(unsigned)blocks, kThreads, 0, stream>>>(
             (const T *)q, (const T *)k, (const T *)v, (const T *)g, (const T *)beta, cu_seqlens,
-            total_tokens, n_heads, d_k, d_v, init_state, (T *)out, final_state, ckpt_stride, ckpts);
+            total_tokens, n_heads, d_k, d_v, init_state, (TO *)out, final_state, ckpt_stride, ckpts);
+    };
+    if (dtype == KDA_BF16) {
+        if (out_dtype == KDA_BF16) go(__nv_bfloat16{}, __nv_bfloat16{}); else go(__nv_bfloat16{}, float{});
     } else {
-        prefill_recurrent_kernel<float><<<(unsigned)blocks, kThreads, 0, stream>>>(
-            (const float *)q, (const float *)k, (const float *)v, (const float *)g,
-            (const float *)beta, cu_seqlens, total_tokens, n_heads, d_k, d_v, init_state,
-            (float *)out, final_state, ckpt_stride, ckpts);
+        if (out_dtype == KDA_BF16) go(float{}, __nv_bfloat16{}); else go(float{}, float{});
     }
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

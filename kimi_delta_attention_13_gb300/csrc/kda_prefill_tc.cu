@@ -22,12 +22,13 @@ int read_and_clear_status_prefill_tc(cudaStream_t s, int32_t *status)
 
 int launch_prefill_tc(const void *q, const void *k, const void *v, const void *g,
                       const void *beta, const int32_t *cu_seqlens, int n_seqs,
-                      int64_t total_tokens, int n_heads, const float *init_state, void *out,
-                      float *final_state, int ckpt_stride, float *ckpts, cudaStream_t stream)
+                      int64_t total_tokens, int n_heads, int out_dtype, const float *init_state,
+                      void *out, float *final_state, int ckpt_stride, float *ckpts,
+                      cudaStream_t stream)
 {
     return launch_prefill_recurrent(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, n_heads,
-                                    128, 128, KDA_BF16, init_state, out, final_state, ckpt_stride,
-                                    ckpts, stream);
+                                    128, 128, KDA_BF16, out_dtype, init_state, out, final_state,
+                                    ckpt_stride, ckpts, stream);
 }
 
 }  // namespace kda

@@ -62,16 +62,18 @@ A = 1 << 20  # a fake, 16-byte aligned "device address" that is never dereferenc
 
 def _prefill(lib, **over):
     args = dict(q=A, k=A + 16, v=A + 32, g=A + 48, beta=A + 64, cu=None, n=1, T=16, H=2, dk=128,
-                dv=128, dtype=0, init=None, out=A + 80, fin=None, stride=0, ckpts=None, stream=None)
+                dv=128, dtype=0, odt=1, init=None, out=A + 80, fin=None, stride=0, ckpts=None,
+                stream=None)
     args.update(over)
     return lib.kda_prefill(args["q"], args["k"], args["v"], args["g"], args["beta"], args["cu"],
                            args["n"], args["T"], args["H"], args["dk"], args["dv"], args["dtype"],
-                           args["init"], args["out"], args["fin"], args["stride"], args["ckpts"],
-                           args["stream"])
+                           args["odt"], args["init"], args["out"], args["fin"], args["stride"],
+                           args["ckpts"], args["stream"])
 
 
 @pytest.mark.parametrize("over,code", [
     (dict(H=0), 1), (dict(n=-1), 1), (dict(T=-5), 1), (dict(dtype=3), 1), (dict(q=None), 1),
+    (dict(odt=2), 1),
     (dict(n=2), 1),                       # two sequences need cu_seqlens
     (dict(stride=48), 1),                 # not a multiple of 64
     (dict(stride=64), 1),                 # checkpoints requested without a buffer
@@ -85,19 +87,20 @@ def test_prefill_rejects(lib, over, code):
 
 def test_recurrent_rejects_unsupported_dv(lib):
     # validation passes, the launcher refuses the shape before touching CUDA
-    rc = lib.kda_prefill_recurrent(A, A, A, A, A, None, 1, 16, 2, 128, 48, 1, None, A + 4096, None,
-                                   0, None, None)
+    rc = lib.kda_prefill_recurrent(A, A, A, A, A, None, 1, 16, 2, 128, 48, 1, 1, None, A + 4096,
+                                   None, 0, None, None)
     assert rc == 2
 
 
 def test_decode_rejects(lib):
     f = lib.kda_decode
-    assert f(A, A, A, A, A, A, A + 16, -1, 2, 128, 128, 0, None) == 1
-    assert f(A, A, A, A, A, None, A + 16, 4, 2, 128, 128, 0, None) == 1
-    assert f(A, A, A, A, A, A + 4, A + 16, 4, 2, 128, 128, 0, None) == 3
-    assert f(A, A, A, A, A, A + 32, A + 16, 4, 2, 200, 128, 0, None) == 2
-    assert f(A, A, A, A, A, A + 32, A + 16, 4, 2, 128, 130, 0, None) == 2
-    assert f(A, A, A, A, A, A + 32, A, 4, 2, 128, 128, 0, None) == 1   # out aliases q
+    assert f(A, A, A, A, A, A, A + 16, -1, 2, 128, 128, 0, 1, None) == 1
+    assert f(A, A, A, A, A, None, A + 16, 4, 2, 128, 128, 0, 1, None) == 1
+    assert f(A, A, A, A, A, A + 4, A + 16, 4, 2, 128, 128, 0, 1, None) == 3
+    assert f(A, A, A, A, A, A + 32, A + 16, 4, 2, 200, 128, 0, 1, None) == 2
+    assert f(A, A, A, A, A, A + 32, A + 16, 4, 2, 128, 130, 0, 1, None) == 2
+    assert f(A, A, A, A, A, A + 32, A, 4, 2, 128, 128, 0, 1, None) == 1   # out aliases q
+    assert f(A, A, A, A, A, A + 32, A + 16, 4, 2, 128, 128, 0, 5, None) == 1  # bad out dtype
 
 
 def test_state_copy_rejects(lib):

@@ -48,11 +48,25 @@ def test_decode_other_head_sizes(orc, dk, dv):
     check_decode(orc, d, "f32")
 
 
+def test_decode_bf16_outputs(orc):
+    d = synth.make_inputs([1] * 9, heads=3, dtype="bf16", seed=35, device=DEV, init_state=True)
+    S0 = d["state"].clone()
+    out = kda.decode(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state"], out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    ro, rs = orc.decode(d["q"], d["k"], d["v"], d["g"], d["beta"], S0)
+    import numpy as np
+
+    g = out.double().cpu().numpy()
+    rms = float(np.sqrt(np.mean(ro ** 2)))
+    assert out.dtype == torch.bfloat16
+    assert np.all(np.abs(g - ro) <= 2e-2 * rms + 2.0 ** -8 * np.abs(ro))
+
+
 def test_decode_zero_sequences():
     d = synth.make_inputs([], heads=2, dtype="bf16", seed=1, device=DEV, init_state=True)
     out = kda.decode(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state"])
     torch.cuda.synchronize()
-    assert out.shape == (0, 2, 128)
+    assert out.shape == (0, 2, 128) and out.dtype == torch.float32
 
 
 def test_decode_continues_prefill(orc):

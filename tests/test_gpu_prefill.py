@@ -178,3 +178,21 @@ def test_workload_long_context_checkpoints(orc):
     # the last checkpoint is the final state (the stride divides the length)
     assert torch.equal(ck[-1], fin[0])
     print("T262144", errs)
+
+
+@pytest.mark.parametrize("path", ["prefill", "recurrent"])
+def test_bf16_outputs(orc, path):
+    """bf16 outputs: the error beyond the 2e-2 * RMS bound is at most the bf16 rounding of each
+    value (half an ulp, 2^-9 relative)."""
+    x = synth.make_inputs([300, 47], heads=2, dtype="bf16", seed=27, device=DEV, init_state=True)
+    out, fin, _ = PATHS[path](x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], x["state"],
+                              out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert out.dtype == torch.bfloat16
+    ro, rf, _ = orc.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"].cpu(), x["state"])
+    import numpy as np
+
+    g = out.double().cpu().numpy()
+    rms = float(np.sqrt(np.mean(ro ** 2)))
+    assert np.all(np.abs(g - ro) <= 2e-2 * rms + 2.0 ** -8 * np.abs(ro))
+    assert_close("final", fin, rf, TOL["bf16"]["state"])
