@@ -100,9 +100,11 @@ def _prefill(fn_name, q, k, v, g, beta, cu_seqlens, init_state, out, final_state
         if lengths is None:  # host read of the lengths (synchronizes); pass `lengths` to avoid it
             lengths = [T] if cu_seqlens is None else torch.diff(cu_seqlens).tolist()
         slots = num_checkpoints(lengths, ckpt_stride)
-        ckpts = torch.empty((max(slots, 1), H, dk, dv), device=dev, dtype=torch.float32)[:slots]
+        ckpts = torch.empty((slots, H, dk, dv), device=dev, dtype=torch.float32)
     elif ckpts is not None:
         _require(ckpts, "ckpts", dev, torch.float32)
+    if ckpts is not None and ckpts.numel() == 0:
+        ckpt_stride = 0   # no sequence reaches a checkpoint: nothing to emit
     rc = getattr(lib, fn_name)(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), n, T, H, dk, dv,
         _DTYPES[dtype], _DTYPES[out_dtype], _ptr(init_state), _ptr(out), _ptr(final_state),

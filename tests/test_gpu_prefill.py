@@ -82,7 +82,7 @@ def test_small_f32_with_checkpoints(orc, lengths):
     run_and_check(orc, x, ckpt_stride=64, dtype="f32")
 
 
-@pytest.mark.parametrize("dk,dv", [(64, 32), (1, 32), (128, 256), (72, 96)])
+@pytest.mark.parametrize("dk,dv", [(64, 32), (4, 32), (128, 256), (72, 96)])
 def test_other_head_sizes_recurrent(orc, dk, dv):
     x = synth.make_inputs([40, 9], heads=2, d_k=dk, d_v=dv, dtype="f32", seed=dk + dv, device=DEV,
                           init_state=True)
