@@ -19,13 +19,18 @@
 // factor lies in [e^-80, e^80] (Gram blocks: left operand relative to its own tile start, right
 // operand relative to the row tile's start).
 //
-// Work split: one CTA per (sequence, head), 384 threads:
-//   warp 0       TMA producer: q, k, g, v tiles (32 tokens x 128, 128-byte swizzle) + beta
-//   warp 1       TMEM owner and the single MMA-issuing thread (tcgen05.mma, kind::f16)
-//   warps 4..7   chain: thread j <-> TMEM lane j <-> value channel j; fp32 state S^T in TMEM,
-//                its bf16 copy in TMEM as the A operand of the state products; outputs
-//   warps 8..11  prep: state-independent work of the next step (decay cumprods, scaled bf16
-//                operands, Gram post-processing, the 32x32 unit-triangular solve, W and U)
+// Work split: one CTA per (sequence, head), 512 threads; each group issues its own MMAs:
+//   warp 0        TMA producer: q, k, g, v tiles (32 tokens x 128, 128-byte swizzle) + beta
+//   warp 1        TMEM allocation
+//   warps 4..7    chain: thread j <-> TMEM lane j <-> value channel j.  fp32 state S^T in TMEM
+//                 (pre-multiplied by the step's decay), its fp16 copy in TMEM as the A operand
+//                 of the state reads; issues MMA1 (state reads), MMA2 (outputs), MMA3 (state
+//                 update); writes outputs, checkpoints and the final state
+//   warps 8..15   prep (state-independent, software-pipelined one step ahead of the chain):
+//                 per iteration, for step s: Gram -> A and Aqk, the 32x32 unit-triangular
+//                 solve, W and U; for step s+1: decay cumprods, every scaled operand, its Gram;
+//                 then W^T of step s into the MMA1 operand.  The MMA latencies hide behind the
+//                 next phase's work.
 // Accumulators and A operands live in TMEM (512 columns); B operands in shared memory.
 //
 // Precision: the max-error bound (2e-2 x RMS on outputs, 1e-2 on states) needs ~1e-3 relative
@@ -47,11 +52,11 @@ using namespace ptx;
 
 constexpr int D = 128;        // d_k = d_v
 constexpr int C = 32;         // tokens per chain step
-constexpr int kThreads = 384;
-constexpr uint64_t kTimeoutNs = 2000000000ull;   // bounded waits: 2 s
+constexpr int kThreads = 512;
+constexpr long long kTimeout = 4000000000ll;     // bounded waits: 4e9 SM cycles (~2 s)
 
 // shared memory map (bytes from a 1024-aligned base)
-constexpr int kQStages = 2;                                // q, k, g ring (read by the prep step)
+constexpr int kQStages = 2;                                // q, k, g ring (read by prep A)
 constexpr int kVStages = 3;                                // v ring (read by the U product)
 constexpr uint32_t TILE_BYTES = 2 * C * 128;               // 64 channels x 32 rows x 2 halves
 constexpr uint32_t QSTAGE_BYTES = 3 * TILE_BYTES;          // q, k, g
@@ -67,25 +72,23 @@ constexpr uint32_t GA_REGION = 64 * 128, GB_REGION = 48 * 128;
 constexpr uint32_t OFF_GA = OFF_AB + 2 * 8192;                       // Gram A: 4 x 8 KB
 constexpr uint32_t OFF_GB = OFF_GA + 4 * GA_REGION;                  // Gram B: 4 x 6 KB (N = 48)
 constexpr uint32_t OFF_BC = OFF_GB + 4 * GB_REGION;                  // step decay b_C, x2
-constexpr uint32_t OFF_BETA = OFF_BC + 2 * D * 4;                    // beta per v stage
+constexpr uint32_t OFF_SA = OFF_BC + 2 * D * 4;                      // A (fp32) 32 x 36
+constexpr uint32_t OFF_ST = OFF_SA + C * 36 * 4;                     // T (fp32) 32 x 33
+constexpr uint32_t OFF_SX = OFF_ST + C * 33 * 4;                     // A10 T00, 16 x 17
+constexpr uint32_t OFF_TOT = OFF_SX + 16 * 17 * 4;                   // per-quarter decay totals
+constexpr uint32_t OFF_BETA = OFF_TOT + 4 * 64 * 8;                  // beta per v stage
 constexpr uint32_t OFF_BARS = OFF_BETA + kVStages * C * 4;
-constexpr uint32_t NUM_BARS = 24;
+constexpr uint32_t NUM_BARS = 32;
 constexpr uint32_t OFF_MISC = OFF_BARS + NUM_BARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;                   // alignment slack
-// fp32 scratch of the triangular solve, placed in the Gram B buffer, which is dead between the
-// completion of the Gram product and the next step's operand writes
-constexpr uint32_t OFF_SA = OFF_GB;                                  // A (fp32) 32 x 33
-constexpr uint32_t OFF_ST = OFF_SA + C * 33 * 4;                     // T (fp32) 32 x 33
-constexpr uint32_t OFF_SX = OFF_ST + C * 33 * 4;                     // A10 T00, 16 x 17
-static_assert(OFF_SX + 16 * 17 * 4 <= OFF_GB + 4 * GB_REGION, "solve scratch fits in the Gram B buffer");
 static_assert(SMEM_ALLOC <= 232448, "shared memory per block");
 
 // TMEM column map
 constexpr uint32_t TM_S32 = 0;      // fp32 state S^T (lane j, column = key channel)
-constexpr uint32_t TM_SBF = 128;    // bf16 copy, A operand (64 columns)
+constexpr uint32_t TM_SBF = 128;    // fp16 copy, A operand (64 columns)
 constexpr uint32_t TM_D1 = 192;     // 2 x 64: [U^T -> V_new^T | Y^T -> O^T]
-constexpr uint32_t TM_VBF = 320;    // bf16 V_new^T, A operand (16 columns)
+constexpr uint32_t TM_VBF = 320;    // fp16 V_new^T, A operand (16 columns)
 constexpr uint32_t TM_DG = 352;     // Gram (48 columns)
 constexpr uint32_t TM_DW = 416;     // W^T (32 columns)
 constexpr uint32_t TM_COLS = 512;
@@ -98,13 +101,23 @@ constexpr uint32_t I_MMA1 = idesc_f32acc(128, 64, FMT_F16, 0, 1);
 constexpr uint32_t I_MMA2 = idesc_f32acc(128, 32, FMT_F16, 0, 0);
 constexpr uint32_t I_MMA3 = idesc_f32acc(128, 128, FMT_F16, 0, 0);
 
+// mbarriers.  Every cross-group handoff that a group can run ahead of is double-buffered by
+// step parity, so that no waiter can ever be two phases behind the barrier it polls.
 enum Bar {
-    B_QFULL = 0,         // + q stage (2)
-    B_QEMPTY = 2,        // + q stage (2)
-    B_VFULL = 4,         // + v stage (3)
-    B_VEMPTY = 7,        // + v stage (3)
-    B_GRAM_OPS = 10, B_GRAM_DONE, B_WU_OPS, B_WU_DONE, B_MMA1_OPS, B_MMA1_DONE, B_VNEW, B_MMA3_DONE,
-    B_STATE, B_D1FREE = 19 /* +buf (2) */, B_CHAIN_SYNC = 21, B_PREP_SYNC = 22, B_COUNT = 23
+    B_QFULL = 0,                 // + q stage (2): TMA landed q, k, g
+    B_QEMPTY = 2,                // + q stage (2): prep A read them
+    B_VFULL = 4,                 // + v stage (3): TMA landed v (+ beta stored)
+    B_VEMPTY = 7,                // + v stage (3): the U product read v
+    B_GRAM_DONE = 10,            // Gram product complete
+    B_WU_DONE = 12,              // W / U products complete
+    B_MMA1_OPS = 13,             // + step parity (2): MMA1 operands and U of the step ready
+    B_MMA1_DONE = 15,            // MMA1 complete
+    B_MMA3_DONE = 16,            // MMA2 + MMA3 complete
+    B_BC_READY = 17,             // + step parity (2): the step's decay b_C published
+    B_OPS_FREE = 19,             // + step parity (2): the chain's products of a step completed
+    B_D1_FREE = 21,              // + step parity (2): the chain read a step's outputs from TMEM
+    B_DRAIN = 23,                // + issuing group (2): end-of-kernel drain of in-flight MMAs
+    B_COUNT = 25
 };
 static_assert(B_COUNT <= (int)NUM_BARS, "barrier slots");
 
@@ -137,55 +150,46 @@ __device__ __forceinline__ void fail(Misc *misc)
     misc->abort = 1;
 }
 
+// Bounded wait; on failure the CTA's abort flag is raised and the caller carries on to its
+// group's next vote, where the whole group leaves together.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Misc *misc)
 {
-    if (mbar_wait(bar, parity, &misc->abort, kTimeoutNs)) return true;
+    if (mbar_wait(bar, parity, &misc->abort, kTimeout)) return true;
     fail(misc);
     return false;
 }
 
-// Barrier among the 128 threads of one group, built on an mbarrier so that a member that gave
-// up (timeout or abort) cannot leave the others blocked: every wait here is bounded too.
+// Barrier among the `n` threads of one group (hardware barrier `id`).  It also votes on the
+// CTA's abort flag, so the whole group takes the same decision to leave its loop: a member that
+// gave up on a bounded wait never leaves the others blocked at a later barrier.
 struct GroupSync {
-    uint64_t *bar;
-    uint32_t phase;
-    __device__ __forceinline__ bool sync(Misc *misc)
-    {
-        mbar_arrive(bar);
-        const bool ok = wait_bar(bar, phase, misc);
-        phase ^= 1u;
-        return ok;
-    }
+    uint32_t id, n;
+    __device__ __forceinline__ bool sync(Misc *misc) { return bar_and(id, n, misc->abort == 0); }
 };
 
-__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+// Before the CTA exits (normally or after an abort), the thread that issued MMAs waits until
+// they have all completed, so that no MMA still writes TMEM when it is released.
+__device__ __forceinline__ void drain_mmas(uint64_t *bar, Misc *misc)
 {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
+    mma_commit(bar);
+    mbar_wait(bar, 0, &misc->abort, kTimeout);
 }
 
-// 8 consecutive bf16 values (one 16-byte chunk) from fp32
-__device__ __forceinline__ void store_chunk(uint32_t addr, const float *v)
+__device__ __forceinline__ void st_shared_v4(uint8_t *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    *reinterpret_cast<uint4 *>(p) = make_uint4(a, b, c, d);
+}
+
+// 8 consecutive bf16 / fp16 values (one 16-byte chunk) from fp32
+__device__ __forceinline__ void store_chunk(uint8_t *addr, const float *v)
 {
     st_shared_v4(addr, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                  pack_bf16x2(v[6], v[7]));
 }
-
-__device__ __forceinline__ void store_chunk_f16(uint32_t addr, const float *v)
+__device__ __forceinline__ void store_chunk_f16(uint8_t *addr, const float *v)
 {
     st_shared_v4(addr, pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]), pack_f16x2(v[4], v[5]),
                  pack_f16x2(v[6], v[7]));
-}
-
-// one fp32 value rounded to the nearest tf32 (10-bit mantissa), so the tf32 product sees a
-// round-to-nearest operand whatever it does with the low mantissa bits
-__device__ __forceinline__ void store_tf32(uint32_t addr, float x)
-{
-    uint32_t t;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(t) : "f"(x));
-    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(t) : "memory");
 }
 
 template <typename TO>
@@ -227,6 +231,55 @@ __device__ void select_item(const Params &p, Misc *misc)
 }
 
 // ------------------------------------------------------------------------------------------------
+// MMA issue (each called by one thread of the owning group)
+
+// state reads of a step: V_new^T = U^T - S^T W^T (onto U^T), Y^T = S^T Q~^T (onto zeros)
+__device__ __forceinline__ void issue_mma1(uint32_t tm, uint32_t sb, int buf, uint64_t *done)
+{
+    for (int k = 0; k < 8; ++k)
+        mma_ts(tm + TM_D1 + 64 * buf, tm + TM_SBF + 8 * k,
+               smem_desc(sb + OFF_MMA1B + buf * 16384 + 2048 * k, 16384, 1024), I_MMA1, 1);
+    mma_commit(done);
+}
+
+// outputs O^T += V_new^T Aqk^T and the state update S^T += V_new^T Kbar
+__device__ __forceinline__ void issue_mma23(uint32_t tm, uint32_t sb, int buf, uint64_t *done)
+{
+    for (int k = 0; k < 2; ++k)
+        mma_ts(tm + TM_D1 + 64 * buf + 32, tm + TM_VBF + 8 * k,
+               smem_desc(sb + OFF_AB + buf * 8192 + 32 * k, 0, 1024), I_MMA2, 1);
+    for (int k = 0; k < 2; ++k)
+        mma_ts(tm + TM_S32, tm + TM_VBF + 8 * k,
+               smem_desc(sb + OFF_KK + buf * 16384 + 32 * k, 0, 1024), I_MMA3, 1);
+    mma_commit(done);
+}
+
+// Gram of a step (tf32: K = 8 channels, 32 bytes, per instruction)
+__device__ __forceinline__ void issue_gram(uint32_t tm, uint32_t sb, uint64_t *done)
+{
+    for (int k = 0; k < 16; ++k)
+        mma_ss_tf32(tm + TM_DG,
+                    smem_desc(sb + OFF_GA + (k >> 2) * GA_REGION + (k & 3) * 32, 0, 1024),
+                    smem_desc(sb + OFF_GB + (k >> 2) * GB_REGION + (k & 3) * 32, 0, 1024),
+                    I_GRAM, k > 0);
+    mma_commit(done);
+}
+
+// W^T = K~^T (beta T)^T and [U^T | 0] = V^T [beta T | 0]^T
+__device__ __forceinline__ void issue_wu(uint32_t tm, uint32_t sb, int buf, int vs, uint64_t *done)
+{
+    const uint32_t ab = sb + OFF_AB + buf * 8192 + 64;
+    for (int k = 0; k < 2; ++k)
+        mma_ss(tm + TM_DW, smem_desc(sb + OFF_KK + buf * 16384 + 64 + 32 * k, 0, 1024),
+               smem_desc(ab + 32 * k, 0, 1024), I_W, k > 0);
+    const uint32_t vt = sb + OFF_VRING + vs * TILE_BYTES;
+    for (int k = 0; k < 2; ++k)
+        mma_ss(tm + TM_D1 + 64 * buf, smem_desc(vt + 2048 * k, 4096, 1024),
+               smem_desc(ab + 32 * k, 0, 1024), I_U, k > 0);
+    mma_commit(done);
+}
+
+// ------------------------------------------------------------------------------------------------
 // chain group: thread j owns TMEM lane j = value channel j
 
 template <typename TO>
@@ -235,51 +288,55 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
 {
     const int j = threadIdx.x - 128;
     const int wq = j >> 5;  // TMEM sub-partition of this warp
-    // TMEM A operands: fp16 state copy (TM_SBF) and fp16 V_new^T (TM_VBF)
-    const uint32_t tb = misc->tmem_base + ((uint32_t)(32 * wq) << 16);
+    const uint32_t tm = misc->tmem_base;
+    const uint32_t tb = tm + ((uint32_t)(32 * wq) << 16);
+    const uint32_t sb = smem_u32(smem);
     const int n = misc->seq;
     const long long start = misc->start, end = misc->end;
     const long long sbase = ((long long)n * p.H + h) * D * D;
     const float *bc_all = reinterpret_cast<const float *>(smem + OFF_BC);
-    GroupSync gs{&bars[B_CHAIN_SYNC], 0};
+    GroupSync gs{1, 128};
 
-    // initial state: S^T[j][c] = S[c][j]
+    // initial state S^T[j][c] = S[c][j]: fp16 copy and fp32 state (scaled by step 0's b_C later)
     for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t r[32];
+        uint32_t r[32], rb[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            r[i] = __float_as_uint(p.init ? p.init[sbase + (long long)(c0 + i) * D + j] : 0.f);
-        tmem_st32(tb + TM_S32 + c0, r);
-        uint32_t rb[16];
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(p.init ? p.init[sbase + (long long)(c0 + i) * D + j] : 0.f);
 #pragma unroll
         for (int i = 0; i < 16; ++i) rb[i] = pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
         tmem_st16(tb + TM_SBF + c0 / 2, rb);
+        tmem_st32(tb + TM_S32 + c0, r);
     }
     tmem_wait_st();
     tc_fence_before();
     if (!gs.sync(misc)) return;
-    if (j == 0) mbar_arrive(&bars[B_STATE]);
+    if (j == 0) {
+        wait_bar(&bars[B_MMA1_OPS + 0], 0, misc);
+        tc_fence_after();
+        issue_mma1(tm, sb, 0, &bars[B_MMA1_DONE]);
+    }
 
     TO *out = reinterpret_cast<TO *>(p.out);
-    for (int s = 0; s < nsteps && !misc->abort; ++s) {
+    for (int s = 0; s < nsteps; ++s) {
         const int buf = s & 1;
         const uint32_t ph = s & 1;
         const long long t0 = start + (long long)s * C;
         const int valid = (int)((end - t0) < C ? (end - t0) : C);
-        const float *bc = bc_all + buf * D;
+        const bool last = (s == nsteps - 1);
 
-        // decay the fp32 state by the step's b_C while MMA1 runs on the bf16 copy
-        if (!wait_bar(&bars[B_MMA1_OPS], ph, misc)) break;
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(tb + TM_S32 + c0, r);
-            tmem_wait_ld();
+        if (s == 0) {   // the fp32 state takes step 0's decay before MMA3 accumulates onto it
+            wait_bar(&bars[B_BC_READY + 0], 0, misc);
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tb + TM_S32 + c0, r);
+                tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * bc[c0 + i]);
-            tmem_st32(tb + TM_S32 + c0, r);
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * bc_all[c0 + i]);
+                tmem_st32(tb + TM_S32 + c0, r);
+            }
         }
         // V_new^T (fp32, from MMA1) -> fp16 A operand of the output and state products
-        if (!wait_bar(&bars[B_MMA1_DONE], ph, misc)) break;
+        wait_bar(&bars[B_MMA1_DONE], ph, misc);
         tc_fence_after();
         {
             uint32_t r[32], rb[16];
@@ -292,37 +349,56 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
         tmem_wait_st();
         tc_fence_before();
         if (!gs.sync(misc)) break;
-        if (j == 0) mbar_arrive(&bars[B_VNEW]);
+        if (j == 0) {
+            tc_fence_after();
+            issue_mma23(tm, sb, buf, &bars[B_MMA3_DONE]);
+        }
 
-        // updated state: checkpoints / final state, bf16 copy for the next step
-        if (!wait_bar(&bars[B_MMA3_DONE], ph, misc)) break;
+        // updated state S_{s+1}: checkpoint / final state, fp16 copy for the next state read,
+        // and the fp32 state pre-multiplied by the next step's decay
+        wait_bar(&bars[B_MMA3_DONE], ph, misc);
         tc_fence_after();
+        if (j == 0) mbar_arrive(&bars[B_OPS_FREE + buf]);   // this step's operand buffers are free
+        if (!last) wait_bar(&bars[B_BC_READY + (buf ^ 1)], ((s + 1) >> 1) & 1, misc);   // b_C(s+1)
         const long long done = (long long)(s + 1) * C;
-        const bool last = (s == nsteps - 1);
         const bool ckpt = p.ckpt_stride > 0 && done <= end - start && (done % p.ckpt_stride) == 0;
         float *ck = nullptr;
         if (ckpt)
             ck = p.ckpts + ((misc->first_ckpt + done / p.ckpt_stride - 1) * p.H + h) * (long long)D * D;
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t r[32], rb[16];
-            tmem_ld32(tb + TM_S32 + c0, r);
+        const float *bcn = bc_all + (buf ^ 1) * D;
+        for (int c0 = 0; c0 < D; c0 += 64) {
+            uint32_t r[64], rb[32];
+            tmem_ld32(tb + TM_S32 + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+            tmem_ld32(tb + TM_S32 + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
             tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rb[i] = pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            tmem_st16(tb + TM_SBF + c0 / 2, *reinterpret_cast<uint32_t(*)[16]>(&rb[0]));
+            tmem_st16(tb + TM_SBF + c0 / 2 + 16, *reinterpret_cast<uint32_t(*)[16]>(&rb[16]));
             if (ck) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) ck[(long long)(c0 + i) * D + j] = __uint_as_float(r[i]);
+                for (int i = 0; i < 64; ++i) ck[(long long)(c0 + i) * D + j] = __uint_as_float(r[i]);
             }
-            if (last && p.final_state) {
+            if (last) {
+                if (p.final_state) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) p.final_state[sbase + (long long)(c0 + i) * D + j] = __uint_as_float(r[i]);
+                    for (int i = 0; i < 64; ++i) p.final_state[sbase + (long long)(c0 + i) * D + j] = __uint_as_float(r[i]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * bcn[c0 + i]);
+                tmem_st32(tb + TM_S32 + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                tmem_st32(tb + TM_S32 + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
             }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) rb[i] = pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-            tmem_st16(tb + TM_SBF + c0 / 2, rb);
         }
         tmem_wait_st();
         tc_fence_before();
         if (!gs.sync(misc)) break;
-        if (j == 0) mbar_arrive(&bars[B_STATE]);
+        if (!last && j == 0) {   // next step's state reads overlap this step's output epilogue
+            wait_bar(&bars[B_MMA1_OPS + (buf ^ 1)], ((s + 1) >> 1) & 1, misc);
+            tc_fence_after();
+            issue_mma1(tm, sb, buf ^ 1, &bars[B_MMA1_DONE]);
+        }
 
         // outputs of this step: O^T[j][r]
         {
@@ -336,287 +412,279 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
         }
         tc_fence_before();
         if (!gs.sync(misc)) break;
-        if (j == 0) mbar_arrive(&bars[B_D1FREE + buf]);
+        if (j == 0) mbar_arrive(&bars[B_D1_FREE + buf]);   // outputs read: D1 reusable
     }
+    if (j == 0) drain_mmas(&bars[B_DRAIN + 0], misc);
 }
 
 // ------------------------------------------------------------------------------------------------
-// prep group: thread p = key channel c for the elementwise work
+// prep group (256 threads)
 
-__device__ void prep_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
+__device__ __forceinline__ float2 bf2x2(uint32_t w)
 {
-    const int c = threadIdx.x - 256;           // key channel in the elementwise phase
-    const int warp = c >> 5, lane = c & 31;    // warp 8 + warp; TMEM sub-partition = warp
-    const uint32_t sbase = smem_u32(smem);
-    const uint32_t tb = misc->tmem_base + ((uint32_t)(32 * warp) << 16);
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// two fp32 values rounded to the nearest tf32 (10-bit mantissa), so the tf32 product sees
+// round-to-nearest operands whatever it does with the low mantissa bits
+__device__ __forceinline__ void store_tf32x2(uint8_t *addr, float x, float y)
+{
+    uint32_t a, b;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(a) : "f"(x));
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(b) : "f"(y));
+    *reinterpret_cast<uint2 *>(addr) = make_uint2(a, b);
+}
+
+// Decay factors and every scaled operand of step s.  Thread p owns the channel pair (2cp, 2cp+1)
+// and the 8 tokens of quarter qr (tokens 8qr .. 8qr+7; tile = qr / 2).
+//   F = cumulative retention from the own tile's start through the token,
+//   G = retention after the token through the own tile's end,
+//   E = from the step's start through the token,  X = after the token through the step's end.
+__device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg, int p, int buf,
+                                              int valid, Misc *misc, GroupSync &gs, bool &ok)
+{
+    constexpr float LOG2E = 1.4426950408889634f;
+    const int cp = p & 63, qr = p >> 6, tile = qr >> 1;
+    const int c0 = 2 * cp;
+    const uint32_t tile_off = (c0 >> 6) * 4096, cbyte = (c0 & 63) * 2;
+    float2 *tot = reinterpret_cast<float2 *>(smem + OFF_TOT);
+    float2 f[8], gl[8], kv[8], qv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 8 * qr + i;
+        const uint32_t off = tile_off + sw128(r, cbyte);
+        const bool in = r < valid;
+        float2 g = in ? bf2x2(*reinterpret_cast<const uint32_t *>(qkg + 2 * TILE_BYTES + off)) : make_float2(0.f, 0.f);
+        kv[i] = in ? bf2x2(*reinterpret_cast<const uint32_t *>(qkg + TILE_BYTES + off)) : make_float2(0.f, 0.f);
+        qv[i] = in ? bf2x2(*reinterpret_cast<const uint32_t *>(qkg + off)) : make_float2(0.f, 0.f);
+        f[i].x = exp2f(fminf(fmaxf(g.x, -5.0f), 0.0f) * LOG2E);
+        f[i].y = exp2f(fminf(fmaxf(g.y, -5.0f), 0.0f) * LOG2E);
+    }
+    // quarter-local products: gl = after the token to the quarter end, f = through the token
+    {
+        float2 acc = make_float2(1.f, 1.f);
+#pragma unroll
+        for (int i = 7; i >= 0; --i) { gl[i] = acc; acc.x *= f[i].x; acc.y *= f[i].y; }
+#pragma unroll
+        for (int i = 1; i < 8; ++i) { f[i].x *= f[i - 1].x; f[i].y *= f[i - 1].y; }
+    }
+    tot[qr * 64 + cp] = f[7];
+    ok = gs.sync(misc) && ok;
+    const float2 P0 = tot[cp], P1 = tot[64 + cp], P2 = tot[128 + cp], P3 = tot[192 + cp];
+    const float2 B0 = make_float2(P0.x * P1.x, P0.y * P1.y), B1 = make_float2(P2.x * P3.x, P2.y * P3.y);
+    const float2 pre = (qr & 1) ? (qr == 1 ? P0 : P2) : make_float2(1.f, 1.f);
+    const float2 suf = (qr & 1) ? make_float2(1.f, 1.f) : (qr == 0 ? P1 : P3);
+    if (qr == 0) {
+        float *bc = reinterpret_cast<float *>(smem + OFF_BC) + buf * D;
+        bc[c0] = B0.x * B1.x;
+        bc[c0 + 1] = B0.y * B1.y;
+    }
+    float2 F[8], G[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        F[i] = make_float2(f[i].x * pre.x, f[i].y * pre.y);
+        G[i] = make_float2(gl[i].x * suf.x, gl[i].y * suf.y);
+    }
+    // operands of the state products (double-buffered), 8 tokens = one 16-byte chunk per row
+    uint8_t *mma1b = smem + OFF_MMA1B + buf * 16384;
+    uint8_t *kk = smem + OFF_KK + buf * 16384;
+    {
+        float qt0[8], qt1[8], kt0[8], kt1[8], kb0[8], kb1[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float ex = tile ? F[i].x * B0.x : F[i].x, ey = tile ? F[i].y * B0.y : F[i].y;
+            const float xx = tile ? G[i].x : G[i].x * B1.x, xy = tile ? G[i].y : G[i].y * B1.y;
+            qt0[i] = qv[i].x * ex; qt1[i] = qv[i].y * ey;
+            kt0[i] = kv[i].x * ex; kt1[i] = kv[i].y * ey;
+            kb0[i] = kv[i].x * xx; kb1[i] = kv[i].y * xy;
+        }
+        store_chunk_f16(mma1b + sw128(c0, (4 + qr) * 16), qt0);          // Q~   (MMA1 B, N=32+r)
+        store_chunk_f16(mma1b + sw128(c0 + 1, (4 + qr) * 16), qt1);
+        store_chunk(kk + sw128(c0, (4 + qr) * 16), kt0);                 // K~   (W A, bf16, k=s)
+        store_chunk(kk + sw128(c0 + 1, (4 + qr) * 16), kt1);
+        store_chunk_f16(kk + sw128(c0, qr * 16), kb0);                   // Kbar (MMA3 B, k=r)
+        store_chunk_f16(kk + sw128(c0 + 1, qr * 16), kb1);
+    }
+    // Gram operands, fp32 K-major (tf32 product): row = token (A: k rows 0..31, q rows 32..63;
+    // B: k/F rows 0..31, tile-0 k*G rows 32..47), column = channel
+    uint8_t *ga_c = smem + OFF_GA + (c0 >> 5) * GA_REGION;
+    uint8_t *gb_c = smem + OFF_GB + (c0 >> 5) * GB_REGION;
+    const uint32_t cb = (c0 & 31) * 4;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 8 * qr + i;
+        store_tf32x2(ga_c + sw128(r, cb), kv[i].x * F[i].x, kv[i].y * F[i].y);            // K_L
+        store_tf32x2(ga_c + sw128(32 + r, cb), qv[i].x * F[i].x, qv[i].y * F[i].y);       // Q_L
+        store_tf32x2(gb_c + sw128(r, cb), kv[i].x * __fdividef(1.f, F[i].x),
+                     kv[i].y * __fdividef(1.f, F[i].y));                                  // k / F
+        if (tile == 0) store_tf32x2(gb_c + sw128(32 + r, cb), kv[i].x * G[i].x, kv[i].y * G[i].y);
+    }
+}
+
+__device__ void prep_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
+{
+    const int p = threadIdx.x - 256;
+    const int pw = p >> 5, lane = p & 31;
+    const int sub = pw & 3;                    // TMEM sub-partition of this warp
+    const uint32_t tm = misc->tmem_base;
+    const uint32_t tb = tm + ((uint32_t)(32 * sub) << 16);
+    const uint32_t sb = smem_u32(smem);
     float *sA = reinterpret_cast<float *>(smem + OFF_SA);
     float *sT = reinterpret_cast<float *>(smem + OFF_ST);
     float *sX = reinterpret_cast<float *>(smem + OFF_SX);
     const float *sbeta_all = reinterpret_cast<const float *>(smem + OFF_BETA);
-    float *bc_all = reinterpret_cast<float *>(smem + OFF_BC);
     const long long start = misc->start, end = misc->end;
-    constexpr float LOG2E = 1.4426950408889634f;
-    GroupSync gs{&bars[B_PREP_SYNC], 0};
+    GroupSync gs256{2, 256};
 
-    for (int s = 0; s < nsteps && !misc->abort; ++s) {
-        const int qs = s % kQStages, vs = s % kVStages, buf = s & 1;
-        const uint32_t ph = s & 1;
-        const long long t0 = start + (long long)s * C;
-        const int valid = (int)((end - t0) < C ? (end - t0) : C);
-        const uint8_t *qkg = smem + OFF_QRING + qs * QSTAGE_BYTES;   // q, k, g tiles
-        const float *sbeta = sbeta_all + vs * C;
-        if (!wait_bar(&bars[B_QFULL + qs], (s / kQStages) & 1, misc)) break;
-
-        // ---- P1: decay factors of channel c and the scaled operands --------------------------
-        const uint32_t tile_off = (c >> 6) * 4096;
-        float F[C], G[C];
-        {
-            float a[C];
+    for (int it = 0; it <= nsteps; ++it) {
+        bool ok = true;
+        // ---- step s = it - 1, part 1: Gram -> A / Aqk, T, Bt, issue W and U ------------------
+        if (it >= 1) {
+            const int s = it - 1, vs = s % kVStages, buf = s & 1;
+            const float *sbeta = sbeta_all + vs * C;
+            wait_bar(&bars[B_VFULL + vs], (s / kVStages) & 1, misc);   // beta (and v)
+            wait_bar(&bars[B_GRAM_DONE], s & 1, misc);
+            tc_fence_after();
+            if (pw < 2) {
+                uint32_t r0[32], r1[16];
+                tmem_ld32(tb + TM_DG, r0);
+                tmem_ld16(tb + TM_DG + 32, r1);
+                tmem_wait_ld();
+                const int r = lane;   // token row
+                // Gram(r, i): row tile 0 -> column i; row tile 1 -> column 32 + i for i in
+                // tile 0 (right operand relative to the end of tile 0), column i for i in tile 1
+                auto gram = [&](int i) -> float {
+                    return __uint_as_float((r >= 16 && i < 16) ? r1[i & 15] : r0[i & 31]);
+                };
+                if (pw == 0) {
+                    const float br = sbeta[r];
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                const uint16_t gb = *reinterpret_cast<const uint16_t *>(qkg + 2 * TILE_BYTES + tile_off + sw128(r, (c & 63) * 2));
-                float g = r < valid ? bf2f(gb) : 0.f;
-                g = fminf(fmaxf(g, -5.0f), 0.0f);
-                a[r] = exp2f(g * LOG2E);
+                    for (int m = 0; m < 8; ++m) {
+                        float4 v;
+                        v.x = (4 * m + 0 < r) ? br * gram(4 * m + 0) : 0.f;
+                        v.y = (4 * m + 1 < r) ? br * gram(4 * m + 1) : 0.f;
+                        v.z = (4 * m + 2 < r) ? br * gram(4 * m + 2) : 0.f;
+                        v.w = (4 * m + 3 < r) ? br * gram(4 * m + 3) : 0.f;
+                        *reinterpret_cast<float4 *>(sA + r * 36 + 4 * m) = v;
+                    }
+                } else {
+                    uint8_t *ab = smem + OFF_AB + buf * 8192;
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        float t[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) t[i] = (8 * m + i <= r) ? gram(8 * m + i) : 0.f;
+                        store_chunk_f16(ab + sw128(r, m * 16), t);          // Aqk row r (MMA2 B)
+                    }
+                }
             }
+            tc_fence_before();
+            ok = gs256.sync(misc) && ok;
+            // T = (I + A)^-1 by 16x16 blocks: diagonal blocks by forward substitution
+            if (pw == 0) {
+                const int blk = lane >> 4, col = lane & 15, o = 16 * blk;
+                float x[16];
 #pragma unroll
-            for (int tile = 0; tile < 2; ++tile) {
-                float f = 1.f;
+                for (int r = 0; r < 16; ++r) {
+                    float acc[4] = {(r == col) ? 1.f : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int r = 0; r < 16; ++r) { f *= a[16 * tile + r]; F[16 * tile + r] = f; }
-                float gacc = 1.f;
+                    for (int q = 0; q < r; ++q) acc[q & 3] -= sA[(o + r) * 36 + o + q] * x[q];
+                    x[r] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                }
 #pragma unroll
-                for (int r = 15; r >= 0; --r) { G[16 * tile + r] = gacc; gacc *= a[16 * tile + r]; }
+                for (int r = 0; r < 16; ++r) sT[(o + r) * 33 + o + col] = x[r];
             }
-        }
-        const float B0 = F[15], B1 = F[31];
-        bc_all[buf * D + c] = B0 * B1;
-        const uint32_t mma1b = sbase + OFF_MMA1B + buf * 16384;
-        const uint32_t kk = sbase + OFF_KK + buf * 16384;
-        const uint32_t ga_c = sbase + OFF_GA + (c >> 5) * GA_REGION;
-        const uint32_t gb_c = sbase + OFF_GB + (c >> 5) * GB_REGION;
-        const uint32_t cb = (c & 31) * 4;
+            ok = gs256.sync(misc) && ok;
+            {   // X = A10 T00
+                const int r = p >> 4, cc = p & 15;
+                float acc[2] = {0.f, 0.f};
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {  // 8-token groups
-            float kv[8], qv[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = 8 * m + i;
-                const uint32_t off = tile_off + sw128(r, (c & 63) * 2);
-                const bool ok = r < valid;
-                qv[i] = ok ? bf2f(*reinterpret_cast<const uint16_t *>(qkg + off)) : 0.f;
-                kv[i] = ok ? bf2f(*reinterpret_cast<const uint16_t *>(qkg + TILE_BYTES + off)) : 0.f;
+                for (int q = 0; q < 16; ++q)
+                    if (q >= cc) acc[q & 1] += sA[(16 + r) * 36 + q] * sT[q * 33 + cc];
+                sX[r * 17 + cc] = acc[0] + acc[1];
             }
-            float t[8];
-            // E_r: decay from the step start through r (tile 1 adds tile 0's full decay)
+            ok = gs256.sync(misc) && ok;
+            {   // T10 = -T11 X
+                const int r = p >> 4, cc = p & 15;
+                float acc[2] = {0.f, 0.f};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) t[i] = qv[i] * (m < 2 ? F[8 * m + i] : F[8 * m + i] * B0);
-            store_chunk_f16(mma1b + sw128(c, (4 + m) * 16), t);             // Q~   (MMA1 B, N=32+r)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) t[i] = kv[i] * (m < 2 ? F[8 * m + i] : F[8 * m + i] * B0);
-            store_chunk(kk + sw128(c, (4 + m) * 16), t);                    // K~   (W A, bf16, k=s)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) t[i] = kv[i] * (m < 2 ? G[8 * m + i] * B1 : G[8 * m + i]);
-            store_chunk_f16(kk + sw128(c, m * 16), t);                      // Kbar (MMA3 B, k=r)
-            // Gram operands, fp32 K-major (tf32 product): row = token (A: k rows 0..31, q rows
-            // 32..63; B: k/F rows 0..31, tile-0 k*G rows 32..47), column = channel
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = 8 * m + i;
-                store_tf32(ga_c + sw128(r, cb), kv[i] * F[r]);                      // K_L
-                store_tf32(ga_c + sw128(32 + r, cb), qv[i] * F[r]);                 // Q_L
-                store_tf32(gb_c + sw128(r, cb), kv[i] * __fdividef(1.f, F[r]));     // k / F
-                if (m < 2) store_tf32(gb_c + sw128(32 + r, cb), kv[i] * G[r]);      // tile 0 rel. end
+                for (int q = 0; q < 16; ++q)
+                    if (q <= r) acc[q & 1] += sT[(16 + r) * 33 + 16 + q] * sX[q * 17 + cc];
+                sT[(16 + r) * 33 + cc] = -(acc[0] + acc[1]);
             }
-        }
-        fence_proxy_async_smem();
-        if (!gs.sync(misc)) break;
-        if (c == 0) {
-            mbar_arrive(&bars[B_GRAM_OPS]);
-            mbar_arrive(&bars[B_QEMPTY + qs]);   // q, k, g of this step fully read
-        }
-
-        // ---- P3: Gram -> A (fp32, beta folded) and Aqk (fp16 B operand) ----------------------
-        if (!wait_bar(&bars[B_VFULL + vs], (s / kVStages) & 1, misc)) break;   // beta
-        if (!wait_bar(&bars[B_GRAM_DONE], ph, misc)) break;
-        tc_fence_after();
-        if (warp < 2) {
-            uint32_t r0[32], r1[16];
-            tmem_ld32(tb + TM_DG, r0);
-            tmem_ld16(tb + TM_DG + 32, r1);
-            tmem_wait_ld();
-            const int r = lane;   // token row
-            // Gram(r, i): row tile 0 -> column i; row tile 1 -> column 32 + i for i in tile 0
-            // (right operand relative to the end of tile 0), column i for i in tile 1.
-            auto gram = [&](int i) -> float {
-                return __uint_as_float((r >= 16 && i < 16) ? r1[i & 15] : r0[i & 31]);
-            };
-            if (warp == 0) {
-                const float br = sbeta[r];
-#pragma unroll
-                for (int i = 0; i < C; ++i) sA[r * 33 + i] = (i < r) ? br * gram(i) : 0.f;
-            } else {
-                const uint32_t ab = sbase + OFF_AB + buf * 8192;
+            ok = gs256.sync(misc) && ok;
+            if (pw == 0) {   // Bt[r][s] = beta_s T[r][s] (B operand of the W and U products, bf16)
+                const int r = lane;
+                uint8_t *ab = smem + OFF_AB + buf * 8192;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     float t[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) t[i] = (8 * m + i <= r) ? gram(8 * m + i) : 0.f;
-                    store_chunk_f16(ab + sw128(r, m * 16), t);              // Aqk row r (MMA2 B)
+                    for (int i = 0; i < 8; ++i) {
+                        const int q = 8 * m + i;
+                        t[i] = (q <= r) ? sbeta[q] * sT[r * 33 + q] : 0.f;
+                    }
+                    store_chunk(ab + sw128(r, (4 + m) * 16), t);
                 }
             }
-        }
-        if (!gs.sync(misc)) break;
-
-        // ---- P4: T = (I + A)^-1, blocked by 16x16 tiles ---------------------------------------
-        if (warp == 0) {
-            const int blk = lane >> 4, col = lane & 15, o = 16 * blk;
-            float x[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float acc = (r == col) ? 1.f : 0.f;
-#pragma unroll
-                for (int q = 0; q < r; ++q) acc -= sA[(o + r) * 33 + o + q] * x[q];
-                x[r] = acc;
+            fence_proxy_async_smem();
+            ok = gs256.sync(misc) && ok;
+            if (!ok) break;
+            if (p == 0) {
+                if (s >= 2) wait_bar(&bars[B_D1_FREE + buf], ((s >> 1) - 1) & 1, misc);   // D1 outputs read
+                tc_fence_after();
+                issue_wu(tm, sb, buf, vs, &bars[B_WU_DONE]);
             }
-#pragma unroll
-            for (int r = 0; r < 16; ++r) sT[(o + r) * 33 + o + col] = x[r];
         }
-        if (!gs.sync(misc)) break;
-        for (int e = c; e < 256; e += 128) {    // X = A10 T00
-            const int r = e >> 4, cc = e & 15;
-            float acc = 0.f;
-            for (int q = cc; q < 16; ++q) acc += sA[(16 + r) * 33 + q] * sT[q * 33 + cc];
-            sX[r * 17 + cc] = acc;
+        // ---- step it: decay factors, scaled operands, Gram ----------------------------------
+        if (it < nsteps) {
+            const int s = it, qs = s % kQStages, buf = s & 1;
+            const long long t0 = start + (long long)s * C;
+            const int valid = (int)((end - t0) < C ? (end - t0) : C);
+            if (s >= 2) wait_bar(&bars[B_OPS_FREE + buf], ((s >> 1) - 1) & 1, misc);
+            wait_bar(&bars[B_QFULL + qs], (s / kQStages) & 1, misc);
+            prep_operands(smem, smem + OFF_QRING + qs * QSTAGE_BYTES, p, buf, valid, misc, gs256, ok);
+            fence_proxy_async_smem();
+            ok = gs256.sync(misc) && ok;
+            if (!ok) break;
+            if (p == 0) {
+                mbar_arrive(&bars[B_QEMPTY + qs]);        // q, k, g of this step fully read
+                mbar_arrive(&bars[B_BC_READY + buf]);     // the chain scales its state early
+                tc_fence_after();
+                issue_gram(tm, sb, &bars[B_GRAM_DONE]);
+            }
         }
-        if (!gs.sync(misc)) break;
-        for (int e = c; e < 256; e += 128) {    // T10 = -T11 X
-            const int r = e >> 4, cc = e & 15;
-            float acc = 0.f;
-            for (int q = 0; q <= r; ++q) acc += sT[(16 + r) * 33 + 16 + q] * sX[q * 17 + cc];
-            sT[(16 + r) * 33 + cc] = -acc;
-            sT[cc * 33 + 16 + r] = 0.f;          // upper block
-        }
-        if (!gs.sync(misc)) break;
-        if (warp == 0) {   // Bt[r][s] = beta_s T[r][s] (B operand of the W and U products, bf16)
-            const int r = lane;
-            const uint32_t ab = sbase + OFF_AB + buf * 8192;
+        // ---- step s = it - 1, part 2: -W (from W^T in TMEM) into the MMA1 B operand ---------
+        if (it >= 1) {
+            const int s = it - 1, vs = s % kVStages, buf = s & 1;
+            wait_bar(&bars[B_WU_DONE], s & 1, misc);
+            tc_fence_after();
+            {
+                const int half = pw >> 2;            // columns 16*half .. 16*half+15 of W^T
+                uint32_t r[16];
+                tmem_ld16(tb + TM_DW + 16 * half, r);
+                tmem_wait_ld();
+                uint8_t *mma1b = smem + OFF_MMA1B + buf * 16384;
+                const int row = 32 * sub + lane;     // key channel
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                float t[8];
+                for (int m = 0; m < 2; ++m) {
+                    float t[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int q = 8 * m + i;
-                    t[i] = (q <= r) ? sbeta[q] * sT[r * 33 + q] : 0.f;
+                    for (int i = 0; i < 8; ++i) t[i] = -__uint_as_float(r[8 * m + i]);
+                    store_chunk_f16(mma1b + sw128(row, (2 * half + m) * 16), t);
                 }
-                store_chunk(ab + sw128(r, (4 + m) * 16), t);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            ok = gs256.sync(misc) && ok;
+            if (!ok) break;
+            if (p == 0) {
+                mbar_arrive(&bars[B_MMA1_OPS + buf]);
+                mbar_arrive(&bars[B_VEMPTY + vs]);
             }
         }
-        fence_proxy_async_smem();
-        if (!gs.sync(misc)) break;
-        if (c == 0) mbar_arrive(&bars[B_WU_OPS]);
-
-        // ---- P6: -W (from W^T in TMEM) into the MMA1 B operand; release the v stage ------------
-        if (!wait_bar(&bars[B_WU_DONE], ph, misc)) break;
-        tc_fence_after();
-        {
-            uint32_t r[32];
-            tmem_ld32(tb + TM_DW, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                float t[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) t[i] = -__uint_as_float(r[8 * m + i]);
-                store_chunk_f16(mma1b + sw128(c, m * 16), t);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (!gs.sync(misc)) break;
-        if (c == 0) {
-            mbar_arrive(&bars[B_MMA1_OPS]);
-            mbar_arrive(&bars[B_VEMPTY + vs]);
-        }
     }
-}
-
-// ------------------------------------------------------------------------------------------------
-// MMA issuer (one thread)
-
-__device__ void mma_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
-{
-    const uint32_t sb = smem_u32(smem);
-    const uint32_t tm = misc->tmem_base;
-    int g = 0, w = 0, m1 = 0, m3 = 0;
-    uint64_t last_progress = globaltimer_ns();
-    while (m3 < nsteps) {
-        if (misc->abort) break;
-        bool progressed = false;
-        // state products of step m3: MMA2 (outputs) and MMA3 (state)
-        if (m3 < m1 && mbar_try_wait(&bars[B_VNEW], m3 & 1)) {
-            tc_fence_after();
-            const int buf = m3 & 1;
-            for (int k = 0; k < 2; ++k)
-                mma_ts(tm + TM_D1 + 64 * buf + 32, tm + TM_VBF + 8 * k,
-                       smem_desc(sb + OFF_AB + buf * 8192 + 32 * k, 0, 1024), I_MMA2, 1);
-            for (int k = 0; k < 2; ++k)
-                mma_ts(tm + TM_S32, tm + TM_VBF + 8 * k,
-                       smem_desc(sb + OFF_KK + buf * 16384 + 32 * k, 0, 1024), I_MMA3, 1);
-            mma_commit(&bars[B_MMA3_DONE]);
-            ++m3;
-            progressed = true;
-        }
-        // state reads of step m1: V_new^T = U^T - S^T W^T, Y^T = S^T Q~^T
-        if (m1 < w && m1 == m3 && mbar_try_wait(&bars[B_MMA1_OPS], m1 & 1) &&
-            mbar_try_wait(&bars[B_STATE], m1 & 1)) {
-            tc_fence_after();
-            const int buf = m1 & 1;
-            for (int k = 0; k < 8; ++k)
-                mma_ts(tm + TM_D1 + 64 * buf, tm + TM_SBF + 8 * k,
-                       smem_desc(sb + OFF_MMA1B + buf * 16384 + 2048 * k, 16384, 1024), I_MMA1, 1);
-            mma_commit(&bars[B_MMA1_DONE]);
-            ++m1;
-            progressed = true;
-        }
-        // W and U of step w (needs the chain to have consumed step w-1's products and read
-        // the outputs of step w-2 from this D1 buffer)
-        if (w < g && w <= m3 && mbar_try_wait(&bars[B_WU_OPS], w & 1) &&
-            (w < 2 || mbar_try_wait(&bars[B_D1FREE + (w & 1)], ((w >> 1) - 1) & 1)) &&
-            mbar_try_wait(&bars[B_VFULL + w % kVStages], (w / kVStages) & 1)) {
-            tc_fence_after();
-            const int buf = w & 1, stage = w % kVStages;
-            const uint32_t ab = sb + OFF_AB + buf * 8192 + 64;
-            for (int k = 0; k < 2; ++k)
-                mma_ss(tm + TM_DW, smem_desc(sb + OFF_KK + buf * 16384 + 64 + 32 * k, 0, 1024),
-                       smem_desc(ab + 32 * k, 0, 1024), I_W, k > 0);
-            const uint32_t vt = sb + OFF_VRING + stage * TILE_BYTES;
-            for (int k = 0; k < 2; ++k)
-                mma_ss(tm + TM_D1 + 64 * buf, smem_desc(vt + 2048 * k, 4096, 1024),
-                       smem_desc(ab + 32 * k, 0, 1024), I_U, k > 0);
-            mma_commit(&bars[B_WU_DONE]);
-            ++w;
-            progressed = true;
-        }
-        // Gram of step g
-        if (g < nsteps && g <= w && mbar_try_wait(&bars[B_GRAM_OPS], g & 1)) {
-            tc_fence_after();
-            for (int k = 0; k < 16; ++k)   // tf32: K = 8 channels (32 bytes) per instruction
-                mma_ss_tf32(tm + TM_DG,
-                            smem_desc(sb + OFF_GA + (k >> 2) * GA_REGION + (k & 3) * 32, 0, 1024),
-                            smem_desc(sb + OFF_GB + (k >> 2) * GB_REGION + (k & 3) * 32, 0, 1024),
-                            I_GRAM, k > 0);
-            mma_commit(&bars[B_GRAM_DONE]);
-            ++g;
-            progressed = true;
-        }
-        if (progressed) {
-            last_progress = globaltimer_ns();
-        } else if (globaltimer_ns() - last_progress > kTimeoutNs) {
-            fail(misc);
-            break;
-        }
-    }
+    if (p == 0) drain_mmas(&bars[B_DRAIN + 1], misc);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -659,9 +727,9 @@ __device__ void producer_role(const Params &p, const CUtensorMap *mq, const CUte
     }
     // never leave the CTA with copies in flight
     for (int s = (issued > kQStages ? issued - kQStages : 0); s < issued; ++s)
-        mbar_wait(&bars[B_QFULL + s % kQStages], (s / kQStages) & 1, &misc->abort, kTimeoutNs);
+        mbar_wait(&bars[B_QFULL + s % kQStages], (s / kQStages) & 1, &misc->abort, kTimeout);
     for (int s = (issued > kVStages ? issued - kVStages : 0); s < issued; ++s)
-        mbar_wait(&bars[B_VFULL + s % kVStages], (s / kVStages) & 1, &misc->abort, kTimeoutNs);
+        mbar_wait(&bars[B_VFULL + s % kVStages], (s / kVStages) & 1, &misc->abort, kTimeout);
 }
 
 template <typename TO>
@@ -670,8 +738,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                   const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUtensorMap mv,
                   const Params p)
 {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    // 1024-byte aligned base by pointer arithmetic on the shared array, so that the compiler keeps
+    // every access through `smem` in the shared state space (an integer round trip would turn
+    // them into generic loads and stores)
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BARS);
     Misc *misc = reinterpret_cast<Misc *>(smem + OFF_MISC);
     const int warp = threadIdx.x >> 5;
@@ -687,9 +758,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             mbar_init(&bars[B_VFULL + s], 1 + 32);   // expect_tx arrival + one per lane (beta)
             mbar_init(&bars[B_VEMPTY + s], 1);
         }
-        for (int b = B_GRAM_OPS; b < B_CHAIN_SYNC; ++b) mbar_init(&bars[b], 1);
-        mbar_init(&bars[B_CHAIN_SYNC], 128);
-        mbar_init(&bars[B_PREP_SYNC], 128);
+        for (int b = B_GRAM_DONE; b < B_COUNT; ++b) mbar_init(&bars[b], 1);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -720,13 +789,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         }
     } else if (warp == 0) {
         producer_role(p, &mq, &mk, &mg, &mv, smem, bars, misc, h, nsteps);
-    } else if (warp == 1) {
-        if ((threadIdx.x & 31) == 0) mma_role(smem, bars, misc, nsteps);
-        __syncwarp();
     } else if (warp >= 4 && warp < 8) {
         chain_role<TO>(p, smem, bars, misc, h, nsteps);
     } else if (warp >= 8) {
-        prep_role(p, smem, bars, misc, nsteps);
+        prep_role(smem, bars, misc, nsteps);
     }
     tc_fence_before();
     __syncthreads();

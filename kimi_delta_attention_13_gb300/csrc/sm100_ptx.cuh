@@ -56,17 +56,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, giving up after `timeout_ns` or when
-// *abort becomes nonzero.  Returns true if the phase completed.
+// Non-blocking probe of the same condition (never suspends the thread): for polling loops.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// try_wait with an explicit suspend-time hint: the thread sleeps in hardware until the phase
+// completes or about `hint_ns` pass, instead of spinning on issue slots its SM sub-partition
+// neighbours need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, giving up after `timeout_cycles` SM
+// clock cycles (the SM-local counter; the global timer is far slower to read) or when *abort
+// becomes nonzero.  Returns true if the phase completed.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          uint64_t timeout_ns)
+                                          long long timeout_cycles)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const long long t0 = clock64();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > timeout_ns) return false;
+        if (clock64() - t0 > timeout_cycles) return false;
     }
 }
 
@@ -258,6 +283,17 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Barrier over `n` threads (hardware barrier `id`) that also returns the AND of every
+// participant's `v`: all participants get the same answer, so a group can leave a loop together.
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t n, bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+                 "bar.red.and.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+                 : "=r"(r) : "r"((uint32_t)v), "r"(id), "r"(n) : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
