@@ -21,16 +21,16 @@
 //
 // Work split: one CTA per (sequence, head), 512 threads; each group issues its own MMAs:
 //   warp 0        TMA producer: q, k, g, v tiles (32 tokens x 128, 128-byte swizzle) + beta
-//   warp 1        TMEM allocation
+//   warp 1        TMEM allocation; the solver: T = (I + A)^-1 by column forward substitution
+//                 (lane = column), the beta-scaled T as the B operand of W and U; issues W and U
 //   warps 4..7    chain: thread j <-> TMEM lane j <-> value channel j.  fp32 state S^T in TMEM
 //                 (pre-multiplied by the step's decay), its fp16 copy in TMEM as the A operand
 //                 of the state reads; issues MMA1 (state reads), MMA2 (outputs), MMA3 (state
 //                 update); writes outputs, checkpoints and the final state
 //   warps 8..15   prep (state-independent, software-pipelined one step ahead of the chain):
-//                 per iteration, for step s: Gram -> A and Aqk, the 32x32 unit-triangular
-//                 solve, W and U; for step s+1: decay cumprods, every scaled operand, its Gram;
-//                 then W^T of step s into the MMA1 operand.  The MMA latencies hide behind the
-//                 next phase's work.
+//                 per iteration, for step s: Gram -> A and Aqk; for step s+1: decay cumprods,
+//                 every scaled operand, its Gram; then W^T of step s into the MMA1 operand.
+//                 The MMA latencies and the solver's work hide behind the next phase.
 // Accumulators and A operands live in TMEM (512 columns); B operands in shared memory.
 //
 // Precision: the max-error bound (2e-2 x RMS on outputs, 1e-2 on states) needs ~1e-3 relative
@@ -73,9 +73,7 @@ constexpr uint32_t OFF_GA = OFF_AB + 2 * 8192;                       // Gram A: 
 constexpr uint32_t OFF_GB = OFF_GA + 4 * GA_REGION;                  // Gram B: 4 x 6 KB (N = 48)
 constexpr uint32_t OFF_BC = OFF_GB + 4 * GB_REGION;                  // step decay b_C, x2
 constexpr uint32_t OFF_SA = OFF_BC + 2 * D * 4;                      // A (fp32) 32 x 36
-constexpr uint32_t OFF_ST = OFF_SA + C * 36 * 4;                     // T (fp32) 32 x 33
-constexpr uint32_t OFF_SX = OFF_ST + C * 33 * 4;                     // A10 T00, 16 x 17
-constexpr uint32_t OFF_TOT = OFF_SX + 16 * 17 * 4;                   // per-quarter decay totals
+constexpr uint32_t OFF_TOT = OFF_SA + C * 36 * 4;                    // per-quarter decay totals
 constexpr uint32_t OFF_BETA = OFF_TOT + 4 * 64 * 8;                  // beta per v stage
 constexpr uint32_t OFF_BARS = OFF_BETA + kVStages * C * 4;
 constexpr uint32_t NUM_BARS = 32;
@@ -116,8 +114,9 @@ enum Bar {
     B_BC_READY = 17,             // + step parity (2): the step's decay b_C published
     B_OPS_FREE = 19,             // + step parity (2): the chain's products of a step completed
     B_D1_FREE = 21,              // + step parity (2): the chain read a step's outputs from TMEM
-    B_DRAIN = 23,                // + issuing group (2): end-of-kernel drain of in-flight MMAs
-    B_COUNT = 25
+    B_DRAIN = 23,                // + issuing group (3): end-of-kernel drain of in-flight MMAs
+    B_A_READY = 26,              // the step's A matrix is in shared memory (prep -> solver)
+    B_COUNT = 27
 };
 static_assert(B_COUNT <= (int)NUM_BARS, "barrier slots");
 
@@ -228,6 +227,28 @@ __device__ void select_item(const Params &p, Misc *misc)
         misc->first_ckpt = first;
         misc->abort = 0;
     }
+}
+
+// ------------------------------------------------------------------------------------------------
+// packed fp32 pairs (two lanes of work per instruction)
+
+__device__ __forceinline__ unsigned long long pk(float2 v)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+    return r;
+}
+__device__ __forceinline__ float2 upk(unsigned long long r)
+{
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b)
+{
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)));
+    return upk(r);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -386,7 +407,13 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
                 }
             } else {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * bcn[c0 + i]);
+                for (int i = 0; i < 64; i += 4) {
+                    const float4 b4 = *reinterpret_cast<const float4 *>(bcn + c0 + i);
+                    const float2 lo = mul2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), make_float2(b4.x, b4.y));
+                    const float2 hi = mul2(make_float2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])), make_float2(b4.z, b4.w));
+                    r[i] = __float_as_uint(lo.x); r[i + 1] = __float_as_uint(lo.y);
+                    r[i + 2] = __float_as_uint(hi.x); r[i + 3] = __float_as_uint(hi.y);
+                }
                 tmem_st32(tb + TM_S32 + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
                 tmem_st32(tb + TM_S32 + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
             }
@@ -425,18 +452,16 @@ __device__ __forceinline__ float2 bf2x2(uint32_t w)
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-// two fp32 values rounded to the nearest tf32 (10-bit mantissa), so the tf32 product sees
-// round-to-nearest operands whatever it does with the low mantissa bits
-__device__ __forceinline__ void store_tf32x2(uint8_t *addr, float x, float y)
+// Two fp32 values rounded half away from zero to tf32 (10-bit mantissa) by one 64-bit add of
+// half a tf32 ulp to each bit pattern (no carry crosses the halves for finite values; the tf32
+// product ignores the low 13 bits), so the Gram sees round-to-nearest operands.
+__device__ __forceinline__ void store_tf32x2(uint8_t *addr, float2 v)
 {
-    uint32_t a, b;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(a) : "f"(x));
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(b) : "f"(y));
-    *reinterpret_cast<uint2 *>(addr) = make_uint2(a, b);
+    *reinterpret_cast<unsigned long long *>(addr) = pk(v) + 0x0000100000001000ull;
 }
 
 // Decay factors and every scaled operand of step s.  Thread p owns the channel pair (2cp, 2cp+1)
-// and the 8 tokens of quarter qr (tokens 8qr .. 8qr+7; tile = qr / 2).
+// (x and y of every float2 below) and the 8 tokens of quarter qr (8qr .. 8qr+7; tile = qr / 2).
 //   F = cumulative retention from the own tile's start through the token,
 //   G = retention after the token through the own tile's end,
 //   E = from the step's start through the token,  X = after the token through the step's end.
@@ -454,71 +479,58 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
         const int r = 8 * qr + i;
         const uint32_t off = tile_off + sw128(r, cbyte);
         const bool in = r < valid;
-        float2 g = in ? bf2x2(*reinterpret_cast<const uint32_t *>(qkg + 2 * TILE_BYTES + off)) : make_float2(0.f, 0.f);
+        const float2 g = in ? bf2x2(*reinterpret_cast<const uint32_t *>(qkg + 2 * TILE_BYTES + off)) : make_float2(0.f, 0.f);
         kv[i] = in ? bf2x2(*reinterpret_cast<const uint32_t *>(qkg + TILE_BYTES + off)) : make_float2(0.f, 0.f);
         qv[i] = in ? bf2x2(*reinterpret_cast<const uint32_t *>(qkg + off)) : make_float2(0.f, 0.f);
-        f[i].x = exp2f(fminf(fmaxf(g.x, -5.0f), 0.0f) * LOG2E);
-        f[i].y = exp2f(fminf(fmaxf(g.y, -5.0f), 0.0f) * LOG2E);
+        const float2 gc = mul2(make_float2(fminf(fmaxf(g.x, -5.0f), 0.0f), fminf(fmaxf(g.y, -5.0f), 0.0f)),
+                               make_float2(LOG2E, LOG2E));
+        f[i] = make_float2(exp2f(gc.x), exp2f(gc.y));
     }
     // quarter-local products: gl = after the token to the quarter end, f = through the token
     {
         float2 acc = make_float2(1.f, 1.f);
 #pragma unroll
-        for (int i = 7; i >= 0; --i) { gl[i] = acc; acc.x *= f[i].x; acc.y *= f[i].y; }
+        for (int i = 7; i >= 0; --i) { gl[i] = acc; acc = mul2(acc, f[i]); }
 #pragma unroll
-        for (int i = 1; i < 8; ++i) { f[i].x *= f[i - 1].x; f[i].y *= f[i - 1].y; }
+        for (int i = 1; i < 8; ++i) f[i] = mul2(f[i], f[i - 1]);
     }
     tot[qr * 64 + cp] = f[7];
     ok = gs.sync(misc) && ok;
     const float2 P0 = tot[cp], P1 = tot[64 + cp], P2 = tot[128 + cp], P3 = tot[192 + cp];
-    const float2 B0 = make_float2(P0.x * P1.x, P0.y * P1.y), B1 = make_float2(P2.x * P3.x, P2.y * P3.y);
-    const float2 pre = (qr & 1) ? (qr == 1 ? P0 : P2) : make_float2(1.f, 1.f);
-    const float2 suf = (qr & 1) ? make_float2(1.f, 1.f) : (qr == 0 ? P1 : P3);
-    if (qr == 0) {
-        float *bc = reinterpret_cast<float *>(smem + OFF_BC) + buf * D;
-        bc[c0] = B0.x * B1.x;
-        bc[c0 + 1] = B0.y * B1.y;
-    }
-    float2 F[8], G[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        F[i] = make_float2(f[i].x * pre.x, f[i].y * pre.y);
-        G[i] = make_float2(gl[i].x * suf.x, gl[i].y * suf.y);
-    }
-    // operands of the state products (double-buffered), 8 tokens = one 16-byte chunk per row
+    const float2 B0 = mul2(P0, P1), B1 = mul2(P2, P3);
+    const float2 one = make_float2(1.f, 1.f);
+    const float2 pre = (qr & 1) ? (qr == 1 ? P0 : P2) : one;
+    const float2 suf = (qr & 1) ? one : (qr == 0 ? P1 : P3);
+    if (qr == 0) reinterpret_cast<float2 *>(smem + OFF_BC + buf * D * 4)[cp] = mul2(B0, B1);
+    const float2 emul = tile ? mul2(pre, B0) : pre;      // E = f * emul
+    const float2 xmul = tile ? suf : mul2(suf, B1);      // X = gl * xmul
     uint8_t *mma1b = smem + OFF_MMA1B + buf * 16384;
     uint8_t *kk = smem + OFF_KK + buf * 16384;
-    {
-        float qt0[8], qt1[8], kt0[8], kt1[8], kb0[8], kb1[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float ex = tile ? F[i].x * B0.x : F[i].x, ey = tile ? F[i].y * B0.y : F[i].y;
-            const float xx = tile ? G[i].x : G[i].x * B1.x, xy = tile ? G[i].y : G[i].y * B1.y;
-            qt0[i] = qv[i].x * ex; qt1[i] = qv[i].y * ey;
-            kt0[i] = kv[i].x * ex; kt1[i] = kv[i].y * ey;
-            kb0[i] = kv[i].x * xx; kb1[i] = kv[i].y * xy;
-        }
-        store_chunk_f16(mma1b + sw128(c0, (4 + qr) * 16), qt0);          // Q~   (MMA1 B, N=32+r)
-        store_chunk_f16(mma1b + sw128(c0 + 1, (4 + qr) * 16), qt1);
-        store_chunk(kk + sw128(c0, (4 + qr) * 16), kt0);                 // K~   (W A, bf16, k=s)
-        store_chunk(kk + sw128(c0 + 1, (4 + qr) * 16), kt1);
-        store_chunk_f16(kk + sw128(c0, qr * 16), kb0);                   // Kbar (MMA3 B, k=r)
-        store_chunk_f16(kk + sw128(c0 + 1, qr * 16), kb1);
-    }
-    // Gram operands, fp32 K-major (tf32 product): row = token (A: k rows 0..31, q rows 32..63;
-    // B: k/F rows 0..31, tile-0 k*G rows 32..47), column = channel
     uint8_t *ga_c = smem + OFF_GA + (c0 >> 5) * GA_REGION;
     uint8_t *gb_c = smem + OFF_GB + (c0 >> 5) * GB_REGION;
     const uint32_t cb = (c0 & 31) * 4;
+    float qt0[8], qt1[8], kt0[8], kt1[8], kb0[8], kb1[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int r = 8 * qr + i;
-        store_tf32x2(ga_c + sw128(r, cb), kv[i].x * F[i].x, kv[i].y * F[i].y);            // K_L
-        store_tf32x2(ga_c + sw128(32 + r, cb), qv[i].x * F[i].x, qv[i].y * F[i].y);       // Q_L
-        store_tf32x2(gb_c + sw128(r, cb), kv[i].x * __fdividef(1.f, F[i].x),
-                     kv[i].y * __fdividef(1.f, F[i].y));                                  // k / F
-        if (tile == 0) store_tf32x2(gb_c + sw128(32 + r, cb), kv[i].x * G[i].x, kv[i].y * G[i].y);
+        const float2 F = mul2(f[i], pre), G = mul2(gl[i], suf);
+        const float2 E = mul2(f[i], emul), X = mul2(gl[i], xmul);
+        const float2 qt = mul2(qv[i], E), kt = mul2(kv[i], E), kb = mul2(kv[i], X);
+        qt0[i] = qt.x; qt1[i] = qt.y; kt0[i] = kt.x; kt1[i] = kt.y; kb0[i] = kb.x; kb1[i] = kb.y;
+        // Gram operands, fp32 K-major (tf32 product): row = token (A: k rows 0..31, q rows
+        // 32..63; B: k/F rows 0..31, tile-0 k*G rows 32..47), column = channel
+        store_tf32x2(ga_c + sw128(r, cb), mul2(kv[i], F));                                  // K_L
+        store_tf32x2(ga_c + sw128(32 + r, cb), mul2(qv[i], F));                             // Q_L
+        store_tf32x2(gb_c + sw128(r, cb), mul2(kv[i], make_float2(__fdividef(1.f, F.x), __fdividef(1.f, F.y))));
+        if (tile == 0) store_tf32x2(gb_c + sw128(32 + r, cb), mul2(kv[i], G));              // k*G
     }
+    // operands of the state products (double-buffered), 8 tokens = one 16-byte chunk per row
+    store_chunk_f16(mma1b + sw128(c0, (4 + qr) * 16), qt0);          // Q~   (MMA1 B, N=32+r)
+    store_chunk_f16(mma1b + sw128(c0 + 1, (4 + qr) * 16), qt1);
+    store_chunk(kk + sw128(c0, (4 + qr) * 16), kt0);                 // K~   (W A, bf16, k=s)
+    store_chunk(kk + sw128(c0 + 1, (4 + qr) * 16), kt1);
+    store_chunk_f16(kk + sw128(c0, qr * 16), kb0);                   // Kbar (MMA3 B, k=r)
+    store_chunk_f16(kk + sw128(c0 + 1, qr * 16), kb1);
 }
 
 __device__ void prep_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
@@ -530,15 +542,13 @@ __device__ void prep_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
     const uint32_t tb = tm + ((uint32_t)(32 * sub) << 16);
     const uint32_t sb = smem_u32(smem);
     float *sA = reinterpret_cast<float *>(smem + OFF_SA);
-    float *sT = reinterpret_cast<float *>(smem + OFF_ST);
-    float *sX = reinterpret_cast<float *>(smem + OFF_SX);
     const float *sbeta_all = reinterpret_cast<const float *>(smem + OFF_BETA);
     const long long start = misc->start, end = misc->end;
-    GroupSync gs256{2, 256};
+    GroupSync gs{2, 256};
 
     for (int it = 0; it <= nsteps; ++it) {
         bool ok = true;
-        // ---- step s = it - 1, part 1: Gram -> A / Aqk, T, Bt, issue W and U ------------------
+        // ---- step s = it - 1, part 1: Gram -> A (for the solver) and Aqk (MMA2 operand) -----
         if (it >= 1) {
             const int s = it - 1, vs = s % kVStages, buf = s & 1;
             const float *sbeta = sbeta_all + vs * C;
@@ -567,6 +577,8 @@ __device__ void prep_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
                         v.w = (4 * m + 3 < r) ? br * gram(4 * m + 3) : 0.f;
                         *reinterpret_cast<float4 *>(sA + r * 36 + 4 * m) = v;
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[B_A_READY]);   // the solver may start
                 } else {
                     uint8_t *ab = smem + OFF_AB + buf * 8192;
 #pragma unroll
@@ -576,64 +588,9 @@ __device__ void prep_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
                         for (int i = 0; i < 8; ++i) t[i] = (8 * m + i <= r) ? gram(8 * m + i) : 0.f;
                         store_chunk_f16(ab + sw128(r, m * 16), t);          // Aqk row r (MMA2 B)
                     }
+                    fence_proxy_async_smem();
                 }
-            }
-            tc_fence_before();
-            ok = gs256.sync(misc) && ok;
-            // T = (I + A)^-1 by 16x16 blocks: diagonal blocks by forward substitution
-            if (pw == 0) {
-                const int blk = lane >> 4, col = lane & 15, o = 16 * blk;
-                float x[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    float acc[4] = {(r == col) ? 1.f : 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int q = 0; q < r; ++q) acc[q & 3] -= sA[(o + r) * 36 + o + q] * x[q];
-                    x[r] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-                }
-#pragma unroll
-                for (int r = 0; r < 16; ++r) sT[(o + r) * 33 + o + col] = x[r];
-            }
-            ok = gs256.sync(misc) && ok;
-            {   // X = A10 T00
-                const int r = p >> 4, cc = p & 15;
-                float acc[2] = {0.f, 0.f};
-#pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    if (q >= cc) acc[q & 1] += sA[(16 + r) * 36 + q] * sT[q * 33 + cc];
-                sX[r * 17 + cc] = acc[0] + acc[1];
-            }
-            ok = gs256.sync(misc) && ok;
-            {   // T10 = -T11 X
-                const int r = p >> 4, cc = p & 15;
-                float acc[2] = {0.f, 0.f};
-#pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    if (q <= r) acc[q & 1] += sT[(16 + r) * 33 + 16 + q] * sX[q * 17 + cc];
-                sT[(16 + r) * 33 + cc] = -(acc[0] + acc[1]);
-            }
-            ok = gs256.sync(misc) && ok;
-            if (pw == 0) {   // Bt[r][s] = beta_s T[r][s] (B operand of the W and U products, bf16)
-                const int r = lane;
-                uint8_t *ab = smem + OFF_AB + buf * 8192;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    float t[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int q = 8 * m + i;
-                        t[i] = (q <= r) ? sbeta[q] * sT[r * 33 + q] : 0.f;
-                    }
-                    store_chunk(ab + sw128(r, (4 + m) * 16), t);
-                }
-            }
-            fence_proxy_async_smem();
-            ok = gs256.sync(misc) && ok;
-            if (!ok) break;
-            if (p == 0) {
-                if (s >= 2) wait_bar(&bars[B_D1_FREE + buf], ((s >> 1) - 1) & 1, misc);   // D1 outputs read
-                tc_fence_after();
-                issue_wu(tm, sb, buf, vs, &bars[B_WU_DONE]);
+                tc_fence_before();
             }
         }
         // ---- step it: decay factors, scaled operands, Gram ----------------------------------
@@ -643,9 +600,9 @@ __device__ void prep_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
             const int valid = (int)((end - t0) < C ? (end - t0) : C);
             if (s >= 2) wait_bar(&bars[B_OPS_FREE + buf], ((s >> 1) - 1) & 1, misc);
             wait_bar(&bars[B_QFULL + qs], (s / kQStages) & 1, misc);
-            prep_operands(smem, smem + OFF_QRING + qs * QSTAGE_BYTES, p, buf, valid, misc, gs256, ok);
+            prep_operands(smem, smem + OFF_QRING + qs * QSTAGE_BYTES, p, buf, valid, misc, gs, ok);
             fence_proxy_async_smem();
-            ok = gs256.sync(misc) && ok;
+            ok = gs.sync(misc) && ok;
             if (!ok) break;
             if (p == 0) {
                 mbar_arrive(&bars[B_QEMPTY + qs]);        // q, k, g of this step fully read
@@ -676,7 +633,7 @@ __device__ void prep_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            ok = gs256.sync(misc) && ok;
+            ok = gs.sync(misc) && ok;
             if (!ok) break;
             if (p == 0) {
                 mbar_arrive(&bars[B_MMA1_OPS + buf]);
@@ -685,6 +642,54 @@ __device__ void prep_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
         }
     }
     if (p == 0) drain_mmas(&bars[B_DRAIN + 1], misc);
+}
+
+// ------------------------------------------------------------------------------------------------
+// solver (warp 1): T = (I + A)^-1 for the 32x32 strictly lower A, one column per lane, by forward
+// substitution x_r = delta_rc - sum_{q<r} A[r][q] x_q; then Bt[r][c] = beta_c T[r][c] (bf16, the B
+// operand of W and U); then W and U are issued.
+
+__device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t tm = misc->tmem_base;
+    const uint32_t sb = smem_u32(smem);
+    const float *sA = reinterpret_cast<const float *>(smem + OFF_SA);
+    const float *sbeta_all = reinterpret_cast<const float *>(smem + OFF_BETA);
+    for (int s = 0; s < nsteps; ++s) {
+        const int vs = s % kVStages, buf = s & 1;
+        if (!wait_bar(&bars[B_A_READY], s & 1, misc)) break;
+        float x[C];
+#pragma unroll
+        for (int r = 0; r < C; ++r) {
+            float acc[4] = {(r == lane) ? 1.f : 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int m = 0; m < (r + 3) / 4; ++m) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(sA + r * 36 + 4 * m);
+                if (4 * m + 0 < r) acc[0] -= a4.x * x[4 * m + 0];
+                if (4 * m + 1 < r) acc[1] -= a4.y * x[4 * m + 1];
+                if (4 * m + 2 < r) acc[2] -= a4.z * x[4 * m + 2];
+                if (4 * m + 3 < r) acc[3] -= a4.w * x[4 * m + 3];
+            }
+            x[r] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        }
+        const float bc = sbeta_all[vs * C + lane];
+        uint8_t *ab = smem + OFF_AB + buf * 8192;
+#pragma unroll
+        for (int r = 0; r < C; ++r)
+            *reinterpret_cast<__nv_bfloat16 *>(ab + sw128(r, 64 + 2 * lane)) =
+                __float2bfloat16_rn(r >= lane ? bc * x[r] : 0.f);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            if (s >= 2) wait_bar(&bars[B_D1_FREE + buf], ((s >> 1) - 1) & 1, misc);   // D1 outputs read
+            tc_fence_after();
+            issue_wu(tm, sb, buf, vs, &bars[B_WU_DONE]);
+        }
+        __syncwarp();
+        if (misc->abort) break;
+    }
+    if (lane == 0) drain_mmas(&bars[B_DRAIN + 2], misc);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -789,6 +794,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         }
     } else if (warp == 0) {
         producer_role(p, &mq, &mk, &mg, &mv, smem, bars, misc, h, nsteps);
+    } else if (warp == 1) {
+        solver_role(smem, bars, misc, nsteps);
     } else if (warp >= 4 && warp < 8) {
         chain_role<TO>(p, smem, bars, misc, h, nsteps);
     } else if (warp >= 8) {
