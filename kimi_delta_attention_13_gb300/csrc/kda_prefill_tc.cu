@@ -11,33 +11,36 @@
 // Chunk algebra for one step (S0 = state at the step start, G_r = cumulative clamped log-decay
 // from the step start through token r, b_r = exp(G_r), per key channel):
 //   u_r = beta_r (v_r - S0^T (k_r b_r) - sum_{s<r} ((k_r b_r).(k_s / b_s)) u_s)
-//     =>  U = T diag(beta) (V - K~ S0),  T = (I + A)^-1,  A[r][s] = beta_r (k_r b_r).(k_s / b_s), s<r
+//     =>  U_new = T diag(beta) (V - K~ S0),  T = (I + A)^-1,  A[r][s] = beta_r (k_r b_r).(k_s / b_s), s<r
 //   o_r = S0^T (q_r b_r) + sum_{s<=r} ((q_r b_r).(k_s / b_s)) u_s      (mask includes the diagonal)
 //   S_C = diag(b_C) S0 + sum_s (k_s b_C / b_s) u_s^T
-// With Wm = T diag(beta) K~ and Um = T diag(beta) V:  V_new = Um - Wm S0,  O = Q~ S0 + Aqk V_new.
-// Every exponential is formed inside one 16-token tile or relative to a tile boundary, so each
-// factor lies in [e^-80, e^80] (Gram blocks: left operand relative to its own tile start, right
-// operand relative to the row tile's start).
+// With Dl = V - K~ S0 and Bt = T diag(beta), every product that involves the state is
+//   Dl = V - K~ S0,   O = Q~ S0 + P Dl  (P = Aqk Bt),   S_C = diag(b_C) S0 + R^T Dl  (R = Bt^T Kbar),
+// so the state reads need only the scaled q and k of the step, and P and R, which do not depend on
+// the state, are formed beside the chain.  Every exponential that can exceed 1 is formed inside
+// one 16-token tile or relative to a tile boundary, so each such factor lies within e^80 (Gram
+// blocks: left operand relative to its own tile start, right operand relative to the row tile's
+// start); factors <= 1 may underflow, which only drops terms below fp32 resolution.
 //
 // Work split: one CTA per (sequence, head), 512 threads; each group issues its own MMAs:
 //   warp 0        TMA producer: q, k, g, v tiles (32 tokens x 128, 128-byte swizzle) + beta
 //   warp 1        TMEM allocation; the solver: T = (I + A)^-1 by column forward substitution
-//                 (lane = column), the beta-scaled T as the B operand of W and U; issues W and U
+//                 (lane = column), Bt = T diag(beta) as MMA operand; issues P and R^T = Kbar^T Bt
+//   warps 2..3    Gram: issue the step's Gram product, read A (warp 2) and Aqk (warp 3) out of it
 //   warps 4..7    chain: thread j <-> TMEM lane j <-> value channel j.  fp32 state S^T in TMEM
 //                 (pre-multiplied by the step's decay), its fp16 copy in TMEM as the A operand
-//                 of the state reads; issues MMA1 (state reads), MMA2 (outputs), MMA3 (state
-//                 update); writes outputs, checkpoints and the final state
-//   warps 8..15   prep (state-independent, software-pipelined one step ahead of the chain):
-//                 per iteration, for step s: Gram -> A and Aqk; for step s+1: decay cumprods,
-//                 every scaled operand, its Gram; then W^T of step s into the MMA1 operand.
-//                 The MMA latencies and the solver's work hide behind the next phase.
+//                 of the state reads; issues V (identity product), the state reads, the output
+//                 and state-update products; copies P and R into their operand buffers while the
+//                 state reads run; writes outputs, checkpoints and the final state
+//   warps 8..15   prep: decay cumprods and every scaled operand of a step, up to two steps ahead
+//                 of the chain.
 // Accumulators and A operands live in TMEM (512 columns); B operands in shared memory.
 //
 // Precision: the max-error bound (2e-2 x RMS on outputs, 1e-2 on states) needs ~1e-3 relative
 // accuracy on the largest elements.  The Gram products (q.k with e^+-80 scalings, where the dot
-// product cancels) therefore run as kind::tf32 on fp32 operands, the state products as fp16
-// (10-bit mantissa; all their operands are O(1) after the tile scalings), and only the W / U
-// products, whose dominant terms are exact, as bf16.
+// product cancels) therefore run as kind::tf32 on fp32 operands, and every other product as fp16
+// (10-bit mantissa; all their operands are O(1) after the tile scalings); V enters exactly
+// (bf16 times an identity).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -56,18 +59,24 @@ constexpr int kThreads = 512;
 constexpr long long kTimeout = 4000000000ll;     // bounded waits: 4e9 SM cycles (~2 s)
 
 // shared memory map (bytes from a 1024-aligned base)
-constexpr int kQStages = 2;                                // q, k, g ring (read by prep A)
-constexpr int kVStages = 3;                                // v ring (read by the U product)
+constexpr int kQStages = 2;                                // q, k, g ring (read by prep)
+constexpr int kVStages = 3;                                // v ring (read by the V product)
 constexpr uint32_t TILE_BYTES = 2 * C * 128;               // 64 channels x 32 rows x 2 halves
 constexpr uint32_t QSTAGE_BYTES = 3 * TILE_BYTES;          // q, k, g
 constexpr uint32_t OFF_QRING = 0;
 constexpr uint32_t OFF_VRING = OFF_QRING + kQStages * QSTAGE_BYTES;
-constexpr uint32_t OFF_MMA1B = OFF_VRING + kVStages * TILE_BYTES;  // [-W^T | Q~^T] fp16, x2
-constexpr uint32_t OFF_KK = OFF_MMA1B + 2 * 16384;                   // [Kbar fp16 | K~ bf16], x2
-constexpr uint32_t OFF_AB = OFF_KK + 2 * 16384;                      // [Aqk fp16 | Bt bf16] 64 rows, x2
+// per step parity: MMA1 B operand [-K~ | Q~] fp16, rows = key channel, 64 tokens (MN-major)
+constexpr uint32_t OFF_MMA1B = OFF_VRING + kVStages * TILE_BYTES;
+// per step parity, rows = key channel: bytes 0..63 Kbar fp16 (A of the R product), then R fp16
+// (B of the state update); bytes 64..127 of rows 0..63: the constant [I | 0] (B of the V product)
+constexpr uint32_t OFF_KK = OFF_MMA1B + 2 * 16384;
+// per step parity, rows = token: bytes 0..63 Aqk fp16 (A of the P product), then P fp16 (B of
+// the output product); bytes 64..127 Bt^T fp16 (B of the P and R products)
+constexpr uint32_t OFF_AB = OFF_KK + 2 * 16384;
 // Gram operands, fp32 K-major (tf32 product), 4 regions of 32 channels each.  A has M = 128 rows
-// of which 64 are real (32 k-rows, 32 q-rows): its regions are spaced 64 rows apart, so the 64
-// unused rows of one region read the next region (or Gram B), and their results are ignored.
+// of which 64 are real (32 k-rows, 32 q-rows): each region's descriptor starts 64 rows before
+// it, so the real rows land in TMEM lanes 64..127 (read by warps 2 and 3) and the 64 leading rows
+// read the previous region (or the AB buffers), whose results are ignored.
 constexpr uint32_t GA_REGION = 64 * 128, GB_REGION = 48 * 128;
 constexpr uint32_t OFF_GA = OFF_AB + 2 * 8192;                       // Gram A: 4 x 8 KB
 constexpr uint32_t OFF_GB = OFF_GA + 4 * GA_REGION;                  // Gram B: 4 x 6 KB (N = 48)
@@ -81,42 +90,44 @@ constexpr uint32_t OFF_MISC = OFF_BARS + NUM_BARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;                   // alignment slack
 static_assert(SMEM_ALLOC <= 232448, "shared memory per block");
+static_assert(OFF_GA >= GA_REGION, "the first Gram region's leading rows stay inside the buffer");
 
 // TMEM column map
 constexpr uint32_t TM_S32 = 0;      // fp32 state S^T (lane j, column = key channel)
 constexpr uint32_t TM_SBF = 128;    // fp16 copy, A operand (64 columns)
-constexpr uint32_t TM_D1 = 192;     // 2 x 64: [U^T -> V_new^T | Y^T -> O^T]
-constexpr uint32_t TM_VBF = 320;    // fp16 V_new^T, A operand (16 columns)
+constexpr uint32_t TM_D1 = 192;     // 2 x 64: [V^T -> Dl^T | Y^T -> O^T]
+constexpr uint32_t TM_VBF = 320;    // fp16 Dl^T, A operand (16 columns)
 constexpr uint32_t TM_DG = 352;     // Gram (48 columns)
-constexpr uint32_t TM_DW = 416;     // W^T (32 columns)
+constexpr uint32_t TM_DP = 416;     // P (lanes 0..31, 32 columns)
+constexpr uint32_t TM_DR = 448;     // R^T (lane = key channel, 32 columns)
 constexpr uint32_t TM_COLS = 512;
 
 // instruction descriptors (M = 128 everywhere)
 constexpr uint32_t I_GRAM = idesc_f32acc(128, 48, FMT_TF32, 0, 0);
-constexpr uint32_t I_W = idesc_f32acc(128, 32, FMT_BF16, 0, 0);
-constexpr uint32_t I_U = idesc_f32acc(128, 64, FMT_BF16, 1, 0);
+constexpr uint32_t I_VI = idesc_f32acc(128, 64, FMT_BF16, 1, 0);
+constexpr uint32_t I_PR = idesc_f32acc(128, 32, FMT_F16, 0, 0);
 constexpr uint32_t I_MMA1 = idesc_f32acc(128, 64, FMT_F16, 0, 1);
 constexpr uint32_t I_MMA2 = idesc_f32acc(128, 32, FMT_F16, 0, 0);
 constexpr uint32_t I_MMA3 = idesc_f32acc(128, 128, FMT_F16, 0, 0);
 
-// mbarriers.  Every cross-group handoff that a group can run ahead of is double-buffered by
-// step parity, so that no waiter can ever be two phases behind the barrier it polls.
+// mbarriers.  A handoff that a group can run two steps ahead of is double-buffered by step
+// parity, so that no waiter can ever be two phases behind the barrier it polls.
 enum Bar {
     B_QFULL = 0,                 // + q stage (2): TMA landed q, k, g
-    B_QEMPTY = 2,                // + q stage (2): prep A read them
+    B_QEMPTY = 2,                // + q stage (2): prep read them
     B_VFULL = 4,                 // + v stage (3): TMA landed v (+ beta stored)
-    B_VEMPTY = 7,                // + v stage (3): the U product read v
-    B_GRAM_DONE = 10,            // Gram product complete
-    B_WU_DONE = 12,              // W / U products complete
-    B_MMA1_OPS = 13,             // + step parity (2): MMA1 operands and U of the step ready
-    B_MMA1_DONE = 15,            // MMA1 complete
-    B_MMA3_DONE = 16,            // MMA2 + MMA3 complete
-    B_BC_READY = 17,             // + step parity (2): the step's decay b_C published
-    B_OPS_FREE = 19,             // + step parity (2): the chain's products of a step completed
-    B_D1_FREE = 21,              // + step parity (2): the chain read a step's outputs from TMEM
-    B_DRAIN = 23,                // + issuing group (3): end-of-kernel drain of in-flight MMAs
-    B_A_READY = 26,              // the step's A matrix is in shared memory (prep -> solver)
-    B_COUNT = 27
+    B_VEMPTY = 7,                // + v stage (3): the V product and the solver are done with it
+    B_OPS_READY = 10,            // + step parity (2): prep wrote the step's operands and b_C
+    B_GRAM_DONE = 12,            // Gram product complete
+    B_A_READY = 13,              // A and Aqk of the step are in shared memory
+    B_SA_FREE = 14,              // the solver read A
+    B_PR_DONE = 15,              // P and R^T products complete
+    B_PR_FREE = 16,              // the chain read P and R^T out of TMEM
+    B_MMA1_DONE = 17,            // state reads complete
+    B_MMA3_DONE = 18,            // output and state-update products complete
+    B_OPS_FREE = 19,             // + step parity (2): every product of the step completed
+    B_DRAIN = 21,                // + issuing group (3): end-of-kernel drain of in-flight MMAs
+    B_COUNT = 24
 };
 static_assert(B_COUNT <= (int)NUM_BARS, "barrier slots");
 
@@ -124,11 +135,24 @@ struct Misc {
     uint32_t tmem_base;
     int abort;
     int seq;
-    int pad;
+    int zero;          // always 0: the abort flag of waits that must not give up early
     long long start, end, first_ckpt;
 };
 
 __device__ int g_prefill_tc_error;  // sticky device error word of this translation unit
+
+// Per-step timeline of the first CTA (SM clock stamps), compiled in only with -DKDA_TRACE.
+#ifdef KDA_TRACE
+__device__ long long g_kda_trace[32 * 64];
+#define KDA_TRACE_EVENT(ev, s)                                                        \
+    do {                                                                              \
+        if (blockIdx.x == 0 && (s) < 64) g_kda_trace[(ev) * 64 + (s)] = clock64();    \
+    } while (0)
+#else
+#define KDA_TRACE_EVENT(ev, s) \
+    do {                       \
+    } while (0)
+#endif
 
 struct Params {
     const __nv_bfloat16 *beta;
@@ -171,7 +195,7 @@ struct GroupSync {
 __device__ __forceinline__ void drain_mmas(uint64_t *bar, Misc *misc)
 {
     mma_commit(bar);
-    mbar_wait(bar, 0, &misc->abort, kTimeout);
+    mbar_wait(bar, 0, &misc->zero, kTimeout);   // even after an abort: bounded by the timeout only
 }
 
 __device__ __forceinline__ void st_shared_v4(uint8_t *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
@@ -179,12 +203,7 @@ __device__ __forceinline__ void st_shared_v4(uint8_t *p, uint32_t a, uint32_t b,
     *reinterpret_cast<uint4 *>(p) = make_uint4(a, b, c, d);
 }
 
-// 8 consecutive bf16 / fp16 values (one 16-byte chunk) from fp32
-__device__ __forceinline__ void store_chunk(uint8_t *addr, const float *v)
-{
-    st_shared_v4(addr, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                 pack_bf16x2(v[6], v[7]));
-}
+// 8 consecutive fp16 values (one 16-byte chunk) from fp32
 __device__ __forceinline__ void store_chunk_f16(uint8_t *addr, const float *v)
 {
     st_shared_v4(addr, pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]), pack_f16x2(v[4], v[5]),
@@ -226,6 +245,7 @@ __device__ void select_item(const Params &p, Misc *misc)
             for (int m = 0; m < n; ++m) first += (p.cu_seqlens[m + 1] - p.cu_seqlens[m]) / p.ckpt_stride;
         misc->first_ckpt = first;
         misc->abort = 0;
+        misc->zero = 0;
     }
 }
 
@@ -250,53 +270,77 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b)
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)));
     return upk(r);
 }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)), "l"(pk(c)));
+    return upk(r);
+}
 
 // ------------------------------------------------------------------------------------------------
 // MMA issue (each called by one thread of the owning group)
 
-// state reads of a step: V_new^T = U^T - S^T W^T (onto U^T), Y^T = S^T Q~^T (onto zeros)
+// A shared-memory descriptor advanced by `bytes` (the start address is its low field, in 16-byte
+// units; every operand here lies below 256 KB, so the field never carries)
+__device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
+// D1 of a step: [V^T | 0] = V^T [I | 0] (v tile as an MN-major A operand, exact in fp32)
+__device__ __forceinline__ void issue_vi(uint32_t tm, uint32_t sb, int buf, int vs)
+{
+    const uint64_t a = smem_desc(sb + OFF_VRING + vs * TILE_BYTES, 4096, 1024);
+    const uint64_t b = smem_desc(sb + OFF_KK + buf * 16384 + 64, 0, 1024);
+    const uint32_t d = tm + TM_D1 + 64 * buf;
+    mma_ss(d, a, b, I_VI, 0);
+    mma_ss(d, desc_at(a, 2048), desc_at(b, 32), I_VI, 1);
+}
+
+// state reads of a step: Dl^T = V^T - S^T K~^T (onto V^T), Y^T = S^T Q~^T (onto zeros)
 __device__ __forceinline__ void issue_mma1(uint32_t tm, uint32_t sb, int buf, uint64_t *done)
 {
-    for (int k = 0; k < 8; ++k)
-        mma_ts(tm + TM_D1 + 64 * buf, tm + TM_SBF + 8 * k,
-               smem_desc(sb + OFF_MMA1B + buf * 16384 + 2048 * k, 16384, 1024), I_MMA1, 1);
+    const uint64_t b = smem_desc(sb + OFF_MMA1B + buf * 16384, 16384, 1024);
+    const uint32_t d = tm + TM_D1 + 64 * buf, a = tm + TM_SBF;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mma_ts(d, a + 8 * k, desc_at(b, 2048 * k), I_MMA1, 1);
     mma_commit(done);
 }
 
-// outputs O^T += V_new^T Aqk^T and the state update S^T += V_new^T Kbar
+// outputs O^T += Dl^T P^T and the state update S^T += Dl^T R
 __device__ __forceinline__ void issue_mma23(uint32_t tm, uint32_t sb, int buf, uint64_t *done)
 {
-    for (int k = 0; k < 2; ++k)
-        mma_ts(tm + TM_D1 + 64 * buf + 32, tm + TM_VBF + 8 * k,
-               smem_desc(sb + OFF_AB + buf * 8192 + 32 * k, 0, 1024), I_MMA2, 1);
-    for (int k = 0; k < 2; ++k)
-        mma_ts(tm + TM_S32, tm + TM_VBF + 8 * k,
-               smem_desc(sb + OFF_KK + buf * 16384 + 32 * k, 0, 1024), I_MMA3, 1);
+    const uint64_t bp = smem_desc(sb + OFF_AB + buf * 8192, 0, 1024);
+    const uint64_t br = smem_desc(sb + OFF_KK + buf * 16384, 0, 1024);
+    const uint32_t a = tm + TM_VBF;
+    mma_ts(tm + TM_D1 + 64 * buf + 32, a, bp, I_MMA2, 1);
+    mma_ts(tm + TM_D1 + 64 * buf + 32, a + 8, desc_at(bp, 32), I_MMA2, 1);
+    mma_ts(tm + TM_S32, a, br, I_MMA3, 1);
+    mma_ts(tm + TM_S32, a + 8, desc_at(br, 32), I_MMA3, 1);
     mma_commit(done);
 }
 
-// Gram of a step (tf32: K = 8 channels, 32 bytes, per instruction)
+// Gram of a step (tf32: K = 8 channels, 32 bytes, per instruction); k-rows land in TMEM lanes
+// 64..95, q-rows in lanes 96..127
 __device__ __forceinline__ void issue_gram(uint32_t tm, uint32_t sb, uint64_t *done)
 {
+    const uint64_t a = smem_desc(sb + OFF_GA - GA_REGION, 0, 1024);
+    const uint64_t b = smem_desc(sb + OFF_GB, 0, 1024);
+#pragma unroll
     for (int k = 0; k < 16; ++k)
-        mma_ss_tf32(tm + TM_DG,
-                    smem_desc(sb + OFF_GA + (k >> 2) * GA_REGION + (k & 3) * 32, 0, 1024),
-                    smem_desc(sb + OFF_GB + (k >> 2) * GB_REGION + (k & 3) * 32, 0, 1024),
-                    I_GRAM, k > 0);
+        mma_ss_tf32(tm + TM_DG, desc_at(a, (k >> 2) * GA_REGION + (k & 3) * 32),
+                    desc_at(b, (k >> 2) * GB_REGION + (k & 3) * 32), I_GRAM, k > 0);
     mma_commit(done);
 }
 
-// W^T = K~^T (beta T)^T and [U^T | 0] = V^T [beta T | 0]^T
-__device__ __forceinline__ void issue_wu(uint32_t tm, uint32_t sb, int buf, int vs, uint64_t *done)
+// P = Aqk Bt (rows 0..31 of the A operand are Aqk: lanes 0..31) and R^T = Kbar^T Bt (lane = key
+// channel); both with B = Bt^T rows
+__device__ __forceinline__ void issue_pr(uint32_t tm, uint32_t sb, int buf, uint64_t *done)
 {
-    const uint32_t ab = sb + OFF_AB + buf * 8192 + 64;
-    for (int k = 0; k < 2; ++k)
-        mma_ss(tm + TM_DW, smem_desc(sb + OFF_KK + buf * 16384 + 64 + 32 * k, 0, 1024),
-               smem_desc(ab + 32 * k, 0, 1024), I_W, k > 0);
-    const uint32_t vt = sb + OFF_VRING + vs * TILE_BYTES;
-    for (int k = 0; k < 2; ++k)
-        mma_ss(tm + TM_D1 + 64 * buf, smem_desc(vt + 2048 * k, 4096, 1024),
-               smem_desc(ab + 32 * k, 0, 1024), I_U, k > 0);
+    const uint64_t ab = smem_desc(sb + OFF_AB + buf * 8192, 0, 1024);
+    const uint64_t kk = smem_desc(sb + OFF_KK + buf * 16384, 0, 1024);
+    const uint64_t bt = desc_at(ab, 64);
+    mma_ss(tm + TM_DP, ab, bt, I_PR, 0);
+    mma_ss(tm + TM_DP, desc_at(ab, 32), desc_at(bt, 32), I_PR, 1);
+    mma_ss(tm + TM_DR, kk, bt, I_PR, 0);
+    mma_ss(tm + TM_DR, desc_at(kk, 32), desc_at(bt, 32), I_PR, 1);
     mma_commit(done);
 }
 
@@ -318,7 +362,16 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
     const float *bc_all = reinterpret_cast<const float *>(smem + OFF_BC);
     GroupSync gs{1, 128};
 
-    // initial state S^T[j][c] = S[c][j]: fp16 copy and fp32 state (scaled by step 0's b_C later)
+    // the V products of steps 0 and 1 go first: every later one is issued two steps ahead
+    if (j == 0) {
+        for (int s = 0; s < 2 && s < nsteps; ++s) {
+            wait_bar(&bars[B_VFULL + s], 0, misc);
+            tc_fence_after();
+            issue_vi(tm, sb, s, s);
+        }
+    }
+    // initial state S^T[j][c] = S[c][j]: fp16 copy, and the fp32 state times step 0's decay
+    wait_bar(&bars[B_OPS_READY + 0], 0, misc);
     for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t r[32], rb[16];
 #pragma unroll
@@ -326,38 +379,62 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
 #pragma unroll
         for (int i = 0; i < 16; ++i) rb[i] = pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
         tmem_st16(tb + TM_SBF + c0 / 2, rb);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * bc_all[c0 + i]);
         tmem_st32(tb + TM_S32 + c0, r);
     }
     tmem_wait_st();
     tc_fence_before();
-    if (!gs.sync(misc)) return;
+    if (!gs.sync(misc)) {
+        if (j == 0) drain_mmas(&bars[B_DRAIN + 0], misc);
+        return;
+    }
     if (j == 0) {
-        wait_bar(&bars[B_MMA1_OPS + 0], 0, misc);
         tc_fence_after();
         issue_mma1(tm, sb, 0, &bars[B_MMA1_DONE]);
     }
 
     TO *out = reinterpret_cast<TO *>(p.out);
     for (int s = 0; s < nsteps; ++s) {
-        const int buf = s & 1;
+        const int buf = s & 1, vs = s % kVStages;
         const uint32_t ph = s & 1;
         const long long t0 = start + (long long)s * C;
         const int valid = (int)((end - t0) < C ? (end - t0) : C);
         const bool last = (s == nsteps - 1);
 
-        if (s == 0) {   // the fp32 state takes step 0's decay before MMA3 accumulates onto it
-            wait_bar(&bars[B_BC_READY + 0], 0, misc);
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tb + TM_S32 + c0, r);
-                tmem_wait_ld();
+        // while the state reads run: R (all lanes) and P (lanes 0..31) into their operand buffers
+        wait_bar(&bars[B_PR_DONE], ph, misc);
+        if (j == 0) KDA_TRACE_EVENT(9, s);
+        tc_fence_after();
+        {
+            uint32_t r[32];
+            float t[8];
+            tmem_ld32(tb + TM_DR, r);
+            tmem_wait_ld();
+            uint8_t *kk = smem + OFF_KK + buf * 16384;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * bc_all[c0 + i]);
-                tmem_st32(tb + TM_S32 + c0, r);
+            for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) t[i] = __uint_as_float(r[8 * m + i]);
+                store_chunk_f16(kk + sw128(j, 16 * m), t);            // R row = key channel j
             }
+            if (wq == 0) {
+                tmem_ld32(tb + TM_DP, r);
+                tmem_wait_ld();
+                uint8_t *ab = smem + OFF_AB + buf * 8192;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) t[i] = __uint_as_float(r[8 * m + i]);
+                    store_chunk_f16(ab + sw128(j, 16 * m), t);        // P row = token j
+                }
+            }
+            fence_proxy_async_smem();
+            if (j == 0) KDA_TRACE_EVENT(10, s);
         }
-        // V_new^T (fp32, from MMA1) -> fp16 A operand of the output and state products
+        // Dl^T (fp32, from the state reads) -> fp16 A operand of the output and state products
         wait_bar(&bars[B_MMA1_DONE], ph, misc);
+        if (j == 0) KDA_TRACE_EVENT(11, s);
         tc_fence_after();
         {
             uint32_t r[32], rb[16];
@@ -371,16 +448,21 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
         tc_fence_before();
         if (!gs.sync(misc)) break;
         if (j == 0) {
+            mbar_arrive(&bars[B_PR_FREE]);         // P and R^T read: the solver may issue again
+            mbar_arrive(&bars[B_VEMPTY + vs]);     // the V product of this step has completed
             tc_fence_after();
             issue_mma23(tm, sb, buf, &bars[B_MMA3_DONE]);
+            KDA_TRACE_EVENT(12, s);
         }
 
         // updated state S_{s+1}: checkpoint / final state, fp16 copy for the next state read,
         // and the fp32 state pre-multiplied by the next step's decay
         wait_bar(&bars[B_MMA3_DONE], ph, misc);
+        if (j == 0) KDA_TRACE_EVENT(13, s);
         tc_fence_after();
         if (j == 0) mbar_arrive(&bars[B_OPS_FREE + buf]);   // this step's operand buffers are free
-        if (!last) wait_bar(&bars[B_BC_READY + (buf ^ 1)], ((s + 1) >> 1) & 1, misc);   // b_C(s+1)
+        if (!last) wait_bar(&bars[B_OPS_READY + (buf ^ 1)], ((s + 1) >> 1) & 1, misc);   // b_C(s+1)
+        if (j == 0) KDA_TRACE_EVENT(14, s);
         const long long done = (long long)(s + 1) * C;
         const bool ckpt = p.ckpt_stride > 0 && done <= end - start && (done % p.ckpt_stride) == 0;
         float *ck = nullptr;
@@ -421,10 +503,11 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
         tmem_wait_st();
         tc_fence_before();
         if (!gs.sync(misc)) break;
+        if (j == 0) KDA_TRACE_EVENT(15, s);
         if (!last && j == 0) {   // next step's state reads overlap this step's output epilogue
-            wait_bar(&bars[B_MMA1_OPS + (buf ^ 1)], ((s + 1) >> 1) & 1, misc);
             tc_fence_after();
             issue_mma1(tm, sb, buf ^ 1, &bars[B_MMA1_DONE]);
+            KDA_TRACE_EVENT(16, s);
         }
 
         // outputs of this step: O^T[j][r]
@@ -439,13 +522,27 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
         }
         tc_fence_before();
         if (!gs.sync(misc)) break;
-        if (j == 0) mbar_arrive(&bars[B_D1_FREE + buf]);   // outputs read: D1 reusable
+        if (j == 0) KDA_TRACE_EVENT(17, s);
+        if (j == 0 && s + 2 < nsteps) {   // D1 of this parity is free: V product two steps ahead
+            wait_bar(&bars[B_VFULL + (s + 2) % kVStages], ((s + 2) / kVStages) & 1, misc);
+            tc_fence_after();
+            issue_vi(tm, sb, buf, (s + 2) % kVStages);
+        }
     }
     if (j == 0) drain_mmas(&bars[B_DRAIN + 0], misc);
 }
 
 // ------------------------------------------------------------------------------------------------
 // prep group (256 threads)
+
+// 2^x for x in [-7.3, 0] (no denormal results): the hardware approximation, relative error
+// below 2^-22
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __device__ __forceinline__ float2 bf2x2(uint32_t w)
 {
@@ -466,7 +563,8 @@ __device__ __forceinline__ void store_tf32x2(uint8_t *addr, float2 v)
 //   G = retention after the token through the own tile's end,
 //   E = from the step's start through the token,  X = after the token through the step's end.
 __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg, int p, int buf,
-                                              int valid, Misc *misc, GroupSync &gs, bool &ok)
+                                              int valid, Misc *misc, GroupSync &gs, bool &ok,
+                                              uint64_t *gram_done, int s)
 {
     constexpr float LOG2E = 1.4426950408889634f;
     const int cp = p & 63, qr = p >> 6, tile = qr >> 1;
@@ -484,7 +582,7 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
         qv[i] = in ? bf2x2(*reinterpret_cast<const uint32_t *>(qkg + off)) : make_float2(0.f, 0.f);
         const float2 gc = mul2(make_float2(fminf(fmaxf(g.x, -5.0f), 0.0f), fminf(fmaxf(g.y, -5.0f), 0.0f)),
                                make_float2(LOG2E, LOG2E));
-        f[i] = make_float2(exp2f(gc.x), exp2f(gc.y));
+        f[i] = make_float2(ex2_approx(gc.x), ex2_approx(gc.y));
     }
     // quarter-local products: gl = after the token to the quarter end, f = through the token
     {
@@ -496,6 +594,8 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
     }
     tot[qr * 64 + cp] = f[7];
     ok = gs.sync(misc) && ok;
+    if (s >= 1) wait_bar(gram_done, (s - 1) & 1, misc);   // the previous Gram read its operands
+    if (p == 0) KDA_TRACE_EVENT(1, s);
     const float2 P0 = tot[cp], P1 = tot[64 + cp], P2 = tot[128 + cp], P3 = tot[192 + cp];
     const float2 B0 = mul2(P0, P1), B1 = mul2(P2, P3);
     const float2 one = make_float2(1.f, 1.f);
@@ -504,6 +604,10 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
     if (qr == 0) reinterpret_cast<float2 *>(smem + OFF_BC + buf * D * 4)[cp] = mul2(B0, B1);
     const float2 emul = tile ? mul2(pre, B0) : pre;      // E = f * emul
     const float2 xmul = tile ? suf : mul2(suf, B1);      // X = gl * xmul
+    // 1/F = G / (tile total): F G is the tile's total retention for every token of the tile, so
+    // one reciprocal per channel replaces one per token (the total is >= e^-80, a normal float)
+    const float2 Bt = tile ? B1 : B0;
+    const float2 ginv = mul2(suf, make_float2(__fdividef(1.f, Bt.x), __fdividef(1.f, Bt.y)));
     uint8_t *mma1b = smem + OFF_MMA1B + buf * 16384;
     uint8_t *kk = smem + OFF_KK + buf * 16384;
     uint8_t *ga_c = smem + OFF_GA + (c0 >> 5) * GA_REGION;
@@ -521,133 +625,129 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
         // 32..63; B: k/F rows 0..31, tile-0 k*G rows 32..47), column = channel
         store_tf32x2(ga_c + sw128(r, cb), mul2(kv[i], F));                                  // K_L
         store_tf32x2(ga_c + sw128(32 + r, cb), mul2(qv[i], F));                             // Q_L
-        store_tf32x2(gb_c + sw128(r, cb), mul2(kv[i], make_float2(__fdividef(1.f, F.x), __fdividef(1.f, F.y))));
+        store_tf32x2(gb_c + sw128(r, cb), mul2(kv[i], mul2(gl[i], ginv)));                // k/F
         if (tile == 0) store_tf32x2(gb_c + sw128(32 + r, cb), mul2(kv[i], G));              // k*G
     }
     // operands of the state products (double-buffered), 8 tokens = one 16-byte chunk per row
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { kt0[i] = -kt0[i]; kt1[i] = -kt1[i]; }
+    store_chunk_f16(mma1b + sw128(c0, qr * 16), kt0);                // -K~  (MMA1 B, N=r)
+    store_chunk_f16(mma1b + sw128(c0 + 1, qr * 16), kt1);
     store_chunk_f16(mma1b + sw128(c0, (4 + qr) * 16), qt0);          // Q~   (MMA1 B, N=32+r)
     store_chunk_f16(mma1b + sw128(c0 + 1, (4 + qr) * 16), qt1);
-    store_chunk(kk + sw128(c0, (4 + qr) * 16), kt0);                 // K~   (W A, bf16, k=s)
-    store_chunk(kk + sw128(c0 + 1, (4 + qr) * 16), kt1);
-    store_chunk_f16(kk + sw128(c0, qr * 16), kb0);                   // Kbar (MMA3 B, k=r)
+    store_chunk_f16(kk + sw128(c0, qr * 16), kb0);                   // Kbar (R product A, k=r)
     store_chunk_f16(kk + sw128(c0 + 1, qr * 16), kb1);
 }
 
 __device__ void prep_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
 {
     const int p = threadIdx.x - 256;
-    const int pw = p >> 5, lane = p & 31;
-    const int sub = pw & 3;                    // TMEM sub-partition of this warp
-    const uint32_t tm = misc->tmem_base;
-    const uint32_t tb = tm + ((uint32_t)(32 * sub) << 16);
-    const uint32_t sb = smem_u32(smem);
-    float *sA = reinterpret_cast<float *>(smem + OFF_SA);
-    const float *sbeta_all = reinterpret_cast<const float *>(smem + OFF_BETA);
     const long long start = misc->start, end = misc->end;
     GroupSync gs{2, 256};
 
-    for (int it = 0; it <= nsteps; ++it) {
+    for (int s = 0; s < nsteps; ++s) {
         bool ok = true;
-        // ---- step s = it - 1, part 1: Gram -> A (for the solver) and Aqk (MMA2 operand) -----
-        if (it >= 1) {
-            const int s = it - 1, vs = s % kVStages, buf = s & 1;
-            const float *sbeta = sbeta_all + vs * C;
-            wait_bar(&bars[B_VFULL + vs], (s / kVStages) & 1, misc);   // beta (and v)
-            wait_bar(&bars[B_GRAM_DONE], s & 1, misc);
-            tc_fence_after();
-            if (pw < 2) {
-                uint32_t r0[32], r1[16];
-                tmem_ld32(tb + TM_DG, r0);
-                tmem_ld16(tb + TM_DG + 32, r1);
-                tmem_wait_ld();
-                const int r = lane;   // token row
-                // Gram(r, i): row tile 0 -> column i; row tile 1 -> column 32 + i for i in
-                // tile 0 (right operand relative to the end of tile 0), column i for i in tile 1
-                auto gram = [&](int i) -> float {
-                    return __uint_as_float((r >= 16 && i < 16) ? r1[i & 15] : r0[i & 31]);
-                };
-                if (pw == 0) {
-                    const float br = sbeta[r];
-#pragma unroll
-                    for (int m = 0; m < 8; ++m) {
-                        float4 v;
-                        v.x = (4 * m + 0 < r) ? br * gram(4 * m + 0) : 0.f;
-                        v.y = (4 * m + 1 < r) ? br * gram(4 * m + 1) : 0.f;
-                        v.z = (4 * m + 2 < r) ? br * gram(4 * m + 2) : 0.f;
-                        v.w = (4 * m + 3 < r) ? br * gram(4 * m + 3) : 0.f;
-                        *reinterpret_cast<float4 *>(sA + r * 36 + 4 * m) = v;
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars[B_A_READY]);   // the solver may start
-                } else {
-                    uint8_t *ab = smem + OFF_AB + buf * 8192;
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        float t[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) t[i] = (8 * m + i <= r) ? gram(8 * m + i) : 0.f;
-                        store_chunk_f16(ab + sw128(r, m * 16), t);          // Aqk row r (MMA2 B)
-                    }
-                    fence_proxy_async_smem();
-                }
-                tc_fence_before();
-            }
+        const int qs = s % kQStages, buf = s & 1;
+        const long long t0 = start + (long long)s * C;
+        const int valid = (int)((end - t0) < C ? (end - t0) : C);
+        if (s >= 2) wait_bar(&bars[B_OPS_FREE + buf], ((s >> 1) - 1) & 1, misc);
+        wait_bar(&bars[B_QFULL + qs], (s / kQStages) & 1, misc);
+        if (p == 0) KDA_TRACE_EVENT(0, s);
+        prep_operands(smem, smem + OFF_QRING + qs * QSTAGE_BYTES, p, buf, valid, misc, gs, ok,
+                      &bars[B_GRAM_DONE], s);
+        fence_proxy_async_smem();
+        ok = gs.sync(misc) && ok;
+        if (!ok) break;
+        if (p == 0) {
+            mbar_arrive(&bars[B_QEMPTY + qs]);        // q, k, g of this step fully read
+            mbar_arrive(&bars[B_OPS_READY + buf]);    // Gram operands, MMA1 B, Kbar, b_C written
+            KDA_TRACE_EVENT(2, s);
         }
-        // ---- step it: decay factors, scaled operands, Gram ----------------------------------
-        if (it < nsteps) {
-            const int s = it, qs = s % kQStages, buf = s & 1;
-            const long long t0 = start + (long long)s * C;
-            const int valid = (int)((end - t0) < C ? (end - t0) : C);
-            if (s >= 2) wait_bar(&bars[B_OPS_FREE + buf], ((s >> 1) - 1) & 1, misc);
-            wait_bar(&bars[B_QFULL + qs], (s / kQStages) & 1, misc);
-            prep_operands(smem, smem + OFF_QRING + qs * QSTAGE_BYTES, p, buf, valid, misc, gs, ok);
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Gram group (warps 2 and 3): warp 2's lane 0 issues each step's Gram product; warp 2 then reads
+// A = strict_lower(beta_r Gram_kk) (TMEM lanes 64..95) for the solver and warp 3 reads
+// Aqk = lower_incl_diag(Gram_qk) (lanes 96..127) as the A operand of the P product.
+
+__device__ void gram_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
+{
+    const int w = (threadIdx.x >> 5) - 2;      // 0: A, 1: Aqk
+    const int lane = threadIdx.x & 31;
+    const uint32_t tm = misc->tmem_base;
+    const uint32_t tb = tm + ((uint32_t)(32 * (2 + w)) << 16);
+    const uint32_t sb = smem_u32(smem);
+    float *sA = reinterpret_cast<float *>(smem + OFF_SA);
+    const float *sbeta_all = reinterpret_cast<const float *>(smem + OFF_BETA);
+    const bool issuer = (w == 0 && lane == 0);
+    GroupSync gs{3, 64};
+
+    if (issuer) {
+        wait_bar(&bars[B_OPS_READY + 0], 0, misc);
+        tc_fence_after();
+        issue_gram(tm, sb, &bars[B_GRAM_DONE]);
+    }
+    for (int s = 0; s < nsteps; ++s) {
+        const int vs = s % kVStages, buf = s & 1;
+        const float *sbeta = sbeta_all + vs * C;
+        wait_bar(&bars[B_VFULL + vs], (s / kVStages) & 1, misc);   // beta
+        wait_bar(&bars[B_GRAM_DONE], s & 1, misc);
+        if (w == 0 && s >= 1) wait_bar(&bars[B_SA_FREE], (s - 1) & 1, misc);
+        if (issuer) KDA_TRACE_EVENT(4, s);
+        tc_fence_after();
+        uint32_t r0[32], r1[16];
+        tmem_ld32(tb + TM_DG, r0);
+        tmem_ld16(tb + TM_DG + 32, r1);
+        tmem_wait_ld();
+        const int r = lane;   // token row
+        // Gram(r, i): row tile 0 -> column i; row tile 1 -> column 32 + i for i in tile 0 (right
+        // operand relative to the end of tile 0), column i for i in tile 1
+        auto gram = [&](int i) -> float {
+            return __uint_as_float((r >= 16 && i < 16) ? r1[i & 15] : r0[i & 31]);
+        };
+        if (w == 0) {
+            const float nbr = -sbeta[r];   // sA holds -A
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                float4 v;
+                v.x = (4 * m + 0 < r) ? nbr * gram(4 * m + 0) : 0.f;
+                v.y = (4 * m + 1 < r) ? nbr * gram(4 * m + 1) : 0.f;
+                v.z = (4 * m + 2 < r) ? nbr * gram(4 * m + 2) : 0.f;
+                v.w = (4 * m + 3 < r) ? nbr * gram(4 * m + 3) : 0.f;
+                *reinterpret_cast<float4 *>(sA + r * 36 + 4 * m) = v;
+            }
+        } else {
+            uint8_t *ab = smem + OFF_AB + buf * 8192;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                float t[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) t[i] = (8 * m + i <= r) ? gram(8 * m + i) : 0.f;
+                store_chunk_f16(ab + sw128(r, m * 16), t);          // Aqk row r
+            }
             fence_proxy_async_smem();
-            ok = gs.sync(misc) && ok;
-            if (!ok) break;
-            if (p == 0) {
-                mbar_arrive(&bars[B_QEMPTY + qs]);        // q, k, g of this step fully read
-                mbar_arrive(&bars[B_BC_READY + buf]);     // the chain scales its state early
+        }
+        tc_fence_before();
+        if (!gs.sync(misc)) break;              // both warps have read the Gram accumulator
+        if (issuer) {
+            mbar_arrive(&bars[B_A_READY]);
+            KDA_TRACE_EVENT(5, s);
+            if (s + 1 < nsteps) {
+                wait_bar(&bars[B_OPS_READY + (buf ^ 1)], ((s + 1) >> 1) & 1, misc);
                 tc_fence_after();
                 issue_gram(tm, sb, &bars[B_GRAM_DONE]);
-            }
-        }
-        // ---- step s = it - 1, part 2: -W (from W^T in TMEM) into the MMA1 B operand ---------
-        if (it >= 1) {
-            const int s = it - 1, vs = s % kVStages, buf = s & 1;
-            wait_bar(&bars[B_WU_DONE], s & 1, misc);
-            tc_fence_after();
-            {
-                const int half = pw >> 2;            // columns 16*half .. 16*half+15 of W^T
-                uint32_t r[16];
-                tmem_ld16(tb + TM_DW + 16 * half, r);
-                tmem_wait_ld();
-                uint8_t *mma1b = smem + OFF_MMA1B + buf * 16384;
-                const int row = 32 * sub + lane;     // key channel
-#pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    float t[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) t[i] = -__uint_as_float(r[8 * m + i]);
-                    store_chunk_f16(mma1b + sw128(row, (2 * half + m) * 16), t);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            ok = gs.sync(misc) && ok;
-            if (!ok) break;
-            if (p == 0) {
-                mbar_arrive(&bars[B_MMA1_OPS + buf]);
-                mbar_arrive(&bars[B_VEMPTY + vs]);
+                KDA_TRACE_EVENT(3, s + 1);
             }
         }
     }
-    if (p == 0) drain_mmas(&bars[B_DRAIN + 1], misc);
+    if (issuer) drain_mmas(&bars[B_DRAIN + 1], misc);
 }
 
 // ------------------------------------------------------------------------------------------------
 // solver (warp 1): T = (I + A)^-1 for the 32x32 strictly lower A, one column per lane, by forward
-// substitution x_r = delta_rc - sum_{q<r} A[r][q] x_q; then Bt[r][c] = beta_c T[r][c] (bf16, the B
-// operand of W and U); then W and U are issued.
+// substitution x_r = delta_rc - sum_{q<r} A[r][q] x_q (shared memory holds -A); row c of Bt^T = beta_c T[:, c] (fp16, the B
+// operand of the P and R products); then P and R^T are issued.
 
 __device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
 {
@@ -658,36 +758,54 @@ __device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nstep
     const float *sbeta_all = reinterpret_cast<const float *>(smem + OFF_BETA);
     for (int s = 0; s < nsteps; ++s) {
         const int vs = s % kVStages, buf = s & 1;
-        if (!wait_bar(&bars[B_A_READY], s & 1, misc)) break;
-        float x[C];
+        const bool ok = wait_bar(&bars[B_A_READY], s & 1, misc);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        if (lane == 0) KDA_TRACE_EVENT(6, s);
+        // x_r = delta_{r,lane} + sum_{q<r} (-A[r][q]) x_q, two packed accumulators per row
+        float2 x2[C / 2];
 #pragma unroll
         for (int r = 0; r < C; ++r) {
-            float acc[4] = {(r == lane) ? 1.f : 0.f, 0.f, 0.f, 0.f};
+            float2 a01 = make_float2((r == lane) ? 1.f : 0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int m = 0; m < (r + 3) / 4; ++m) {
+            for (int m = 0; m < r / 4; ++m) {
                 const float4 a4 = *reinterpret_cast<const float4 *>(sA + r * 36 + 4 * m);
-                if (4 * m + 0 < r) acc[0] -= a4.x * x[4 * m + 0];
-                if (4 * m + 1 < r) acc[1] -= a4.y * x[4 * m + 1];
-                if (4 * m + 2 < r) acc[2] -= a4.z * x[4 * m + 2];
-                if (4 * m + 3 < r) acc[3] -= a4.w * x[4 * m + 3];
+                a01 = fma2(make_float2(a4.x, a4.y), x2[2 * m], a01);
+                a23 = fma2(make_float2(a4.z, a4.w), x2[2 * m + 1], a23);
             }
-            x[r] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            if (r & 3) {   // the partial group q = 4 floor(r/4) .. r-1
+                const int q0 = 4 * (r / 4);
+                const float4 a4 = *reinterpret_cast<const float4 *>(sA + r * 36 + q0);
+                a01.x = fmaf(a4.x, x2[q0 / 2].x, a01.x);
+                if (r - q0 > 1) a01.y = fmaf(a4.y, x2[q0 / 2].y, a01.y);
+                if (r - q0 > 2) a23.x = fmaf(a4.z, x2[q0 / 2 + 1].x, a23.x);
+            }
+            const float xr = (a01.x + a01.y) + (a23.x + a23.y);
+            if (r & 1) x2[r / 2].y = xr; else x2[r / 2].x = xr;
         }
+        if (lane == 0) KDA_TRACE_EVENT(7, s);
         const float bc = sbeta_all[vs * C + lane];
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&bars[B_SA_FREE]);       // A read
+            mbar_arrive(&bars[B_VEMPTY + vs]);   // beta read
+        }
         uint8_t *ab = smem + OFF_AB + buf * 8192;
 #pragma unroll
-        for (int r = 0; r < C; ++r)
-            *reinterpret_cast<__nv_bfloat16 *>(ab + sw128(r, 64 + 2 * lane)) =
-                __float2bfloat16_rn(r >= lane ? bc * x[r] : 0.f);
+        for (int m = 0; m < 4; ++m) {
+            float t[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { t[2 * i] = bc * x2[4 * m + i].x; t[2 * i + 1] = bc * x2[4 * m + i].y; }
+            store_chunk_f16(ab + sw128(lane, 64 + 16 * m), t);   // row = column `lane` of Bt
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            if (s >= 2) wait_bar(&bars[B_D1_FREE + buf], ((s >> 1) - 1) & 1, misc);   // D1 outputs read
+            if (s >= 1) wait_bar(&bars[B_PR_FREE], (s - 1) & 1, misc);   // P, R^T of s-1 read
             tc_fence_after();
-            issue_wu(tm, sb, buf, vs, &bars[B_WU_DONE]);
+            issue_pr(tm, sb, buf, &bars[B_PR_DONE]);
+            KDA_TRACE_EVENT(8, s);
         }
-        __syncwarp();
-        if (misc->abort) break;
+        if (__any_sync(0xffffffffu, misc->abort != 0)) break;
     }
     if (lane == 0) drain_mmas(&bars[B_DRAIN + 2], misc);
 }
@@ -732,9 +850,9 @@ __device__ void producer_role(const Params &p, const CUtensorMap *mq, const CUte
     }
     // never leave the CTA with copies in flight
     for (int s = (issued > kQStages ? issued - kQStages : 0); s < issued; ++s)
-        mbar_wait(&bars[B_QFULL + s % kQStages], (s / kQStages) & 1, &misc->abort, kTimeout);
+        mbar_wait(&bars[B_QFULL + s % kQStages], (s / kQStages) & 1, &misc->zero, kTimeout);
     for (int s = (issued > kVStages ? issued - kVStages : 0); s < issued; ++s)
-        mbar_wait(&bars[B_VFULL + s % kVStages], (s / kVStages) & 1, &misc->abort, kTimeout);
+        mbar_wait(&bars[B_VFULL + s % kVStages], (s / kVStages) & 1, &misc->zero, kTimeout);
 }
 
 template <typename TO>
@@ -761,9 +879,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&bars[B_VFULL + s], 1 + 32);   // expect_tx arrival + one per lane (beta)
-            mbar_init(&bars[B_VEMPTY + s], 1);
+            mbar_init(&bars[B_VEMPTY + s], 2);       // the chain (V product) and the solver (beta)
         }
-        for (int b = B_GRAM_DONE; b < B_COUNT; ++b) mbar_init(&bars[b], 1);
+        for (int b = B_OPS_READY; b < B_COUNT; ++b) mbar_init(&bars[b], 1);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -773,10 +891,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         tmem_alloc(&misc->tmem_base, TM_COLS);
         tmem_relinquish();
     }
-    // zero rows 32..63 of both [Aqk | Bt] buffers (the N=64 U product reads them as zeros)
-    for (int e = threadIdx.x; e < 2 * 32 * 32; e += kThreads) {
-        const int b = e >> 10, rw = (e >> 5) & 31, word = e & 31;
-        reinterpret_cast<uint32_t *>(smem + OFF_AB + b * 8192 + (32 + rw) * 128)[word] = 0u;
+    // the constant B operand [I | 0] of the V product (bf16, rows n = 0..63, K = 32 tokens) in
+    // bytes 64..127 of rows 0..63 of both KK buffers
+    for (int e = threadIdx.x; e < 2 * 64 * 16; e += kThreads) {
+        const int b = e >> 10, row = (e >> 4) & 63, wd = e & 15;
+        const uint32_t lo = (row == 2 * wd) ? 0x3F80u : 0u, hi = (row == 2 * wd + 1) ? 0x3F80u : 0u;
+        *reinterpret_cast<uint32_t *>(smem + OFF_KK + b * 16384 + sw128(row, 64 + 4 * wd)) = lo | (hi << 16);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -796,9 +916,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         producer_role(p, &mq, &mk, &mg, &mv, smem, bars, misc, h, nsteps);
     } else if (warp == 1) {
         solver_role(smem, bars, misc, nsteps);
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp < 4) {
+        gram_role(smem, bars, misc, nsteps);
+    } else if (warp < 8) {
         chain_role<TO>(p, smem, bars, misc, h, nsteps);
-    } else if (warp >= 8) {
+    } else {
         prep_role(smem, bars, misc, nsteps);
     }
     tc_fence_before();
@@ -895,5 +1017,12 @@ int launch_prefill_tc(const void *q, const void *k, const void *v, const void *g
     if (out_dtype == KDA_BF16) return launch_typed<__nv_bfloat16>(mq, mk, mg, mv, p, (int)blocks, stream);
     return launch_typed<float>(mq, mk, mg, mv, p, (int)blocks, stream);
 }
+
+#ifdef KDA_TRACE
+extern "C" int kda_trace_read(long long *dst)
+{
+    return cudaMemcpyFromSymbol(dst, g_kda_trace, sizeof(g_kda_trace)) == cudaSuccess ? 0 : 1;
+}
+#endif
 
 }  // namespace kda
