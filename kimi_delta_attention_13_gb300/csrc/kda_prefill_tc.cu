@@ -59,18 +59,20 @@ constexpr int kThreads = 512;
 constexpr long long kTimeout = 4000000000ll;     // bounded waits: 4e9 SM cycles (~2 s)
 
 // shared memory map (bytes from a 1024-aligned base)
-constexpr int kQStages = 2;                                // q, k, g ring (read by prep)
+constexpr int kQStages = 1;                                // q, k, g stage (read by prep)
+constexpr int kSlots = 3;                                  // depth of the prep -> chain buffers
 constexpr int kVStages = 3;                                // v ring (read by the V product)
 constexpr uint32_t TILE_BYTES = 2 * C * 128;               // 64 channels x 32 rows x 2 halves
 constexpr uint32_t QSTAGE_BYTES = 3 * TILE_BYTES;          // q, k, g
 constexpr uint32_t OFF_QRING = 0;
 constexpr uint32_t OFF_VRING = OFF_QRING + kQStages * QSTAGE_BYTES;
-// per step parity: MMA1 B operand [-K~ | Q~] fp16, rows = key channel, 64 tokens (MN-major)
+// per slot (step mod 3): MMA1 B operand [-K~ | Q~] fp16, rows = key channel, 64 tokens (MN-major)
 constexpr uint32_t OFF_MMA1B = OFF_VRING + kVStages * TILE_BYTES;
-// per step parity, rows = key channel: bytes 0..63 Kbar fp16 (A of the R product), then R fp16
-// (B of the state update); bytes 64..127 of rows 0..63: the constant [I | 0] (B of the V product)
-constexpr uint32_t OFF_KK = OFF_MMA1B + 2 * 16384;
-// per step parity, rows = token: bytes 0..63 Aqk fp16 (A of the P product), then P fp16 (B of
+// two buffers of 128-byte rows (row = key channel); slot k uses bytes 64*(k&1) .. +63 of buffer
+// k>>1: Kbar fp16 (A of the R product), then R fp16 (B of the state update).  Bytes 64..127 of
+// rows 0..63 of buffer 1 hold the constant [I | 0] (B of the V product).
+constexpr uint32_t OFF_KK = OFF_MMA1B + kSlots * 16384;
+// per slot, rows = token (32 rows): bytes 0..63 Aqk fp16 (A of the P product), then P fp16 (B of
 // the output product); bytes 64..127 Bt^T fp16 (B of the P and R products)
 constexpr uint32_t OFF_AB = OFF_KK + 2 * 16384;
 // Gram operands, fp32 K-major (tf32 product), 4 regions of 32 channels each.  A has M = 128 rows
@@ -78,10 +80,10 @@ constexpr uint32_t OFF_AB = OFF_KK + 2 * 16384;
 // it, so the real rows land in TMEM lanes 64..127 (read by warps 2 and 3) and the 64 leading rows
 // read the previous region (or the AB buffers), whose results are ignored.
 constexpr uint32_t GA_REGION = 64 * 128, GB_REGION = 48 * 128;
-constexpr uint32_t OFF_GA = OFF_AB + 2 * 8192;                       // Gram A: 4 x 8 KB
+constexpr uint32_t OFF_GA = OFF_AB + kSlots * 4096;                  // Gram A: 4 x 8 KB
 constexpr uint32_t OFF_GB = OFF_GA + 4 * GA_REGION;                  // Gram B: 4 x 6 KB (N = 48)
-constexpr uint32_t OFF_BC = OFF_GB + 4 * GB_REGION;                  // step decay b_C, x2
-constexpr uint32_t OFF_SA = OFF_BC + 2 * D * 4;                      // A (fp32) 32 x 36
+constexpr uint32_t OFF_BC = OFF_GB + 4 * GB_REGION;                  // step decay b_C, per slot
+constexpr uint32_t OFF_SA = OFF_BC + kSlots * D * 4;                 // A (fp32) 32 x 36
 constexpr uint32_t OFF_TOT = OFF_SA + C * 36 * 4;                    // per-quarter decay totals
 constexpr uint32_t OFF_BETA = OFF_TOT + 4 * 64 * 8;                  // beta per v stage
 constexpr uint32_t OFF_BARS = OFF_BETA + kVStages * C * 4;
@@ -92,14 +94,22 @@ constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;                   // alignmen
 static_assert(SMEM_ALLOC <= 232448, "shared memory per block");
 static_assert(OFF_GA >= GA_REGION, "the first Gram region's leading rows stay inside the buffer");
 
+// byte offsets of a slot's buffers; Kbar / R addresses add the slot's half-row offset before the
+// swizzle: kk_base(k) + sw128(row, kk_half(k) + byte)
+__host__ __device__ constexpr uint32_t mma1b_off(int k) { return OFF_MMA1B + k * 16384; }
+__host__ __device__ constexpr uint32_t kk_base(int k) { return OFF_KK + (k >> 1) * 16384; }
+__host__ __device__ constexpr uint32_t kk_half(int k) { return (k & 1) * 64; }
+__host__ __device__ constexpr uint32_t ab_off(int k) { return OFF_AB + k * 4096; }
+constexpr int kEyeSlot = 3;   // the [I | 0] constant sits where a fourth Kbar slot would be
+
 // TMEM column map
 constexpr uint32_t TM_S32 = 0;      // fp32 state S^T (lane j, column = key channel)
 constexpr uint32_t TM_SBF = 128;    // fp16 copy, A operand (64 columns)
 constexpr uint32_t TM_D1 = 192;     // 2 x 64: [V^T -> Dl^T | Y^T -> O^T]
 constexpr uint32_t TM_VBF = 320;    // fp16 Dl^T, A operand (16 columns)
-constexpr uint32_t TM_DG = 352;     // Gram (48 columns)
-constexpr uint32_t TM_DP = 416;     // P (lanes 0..31, 32 columns)
-constexpr uint32_t TM_DR = 448;     // R^T (lane = key channel, 32 columns)
+constexpr uint32_t TM_DG = 352;     // Gram, 2 x 48 columns (step parity)
+constexpr uint32_t TM_DP = 448;     // P (lanes 0..31, 32 columns)
+constexpr uint32_t TM_DR = 480;     // R^T (lane = key channel, 32 columns)
 constexpr uint32_t TM_COLS = 512;
 
 // instruction descriptors (M = 128 everywhere)
@@ -110,24 +120,25 @@ constexpr uint32_t I_MMA1 = idesc_f32acc(128, 64, FMT_F16, 0, 1);
 constexpr uint32_t I_MMA2 = idesc_f32acc(128, 32, FMT_F16, 0, 0);
 constexpr uint32_t I_MMA3 = idesc_f32acc(128, 128, FMT_F16, 0, 0);
 
-// mbarriers.  A handoff that a group can run two steps ahead of is double-buffered by step
-// parity, so that no waiter can ever be two phases behind the barrier it polls.
+// mbarriers.  A handoff that a group can run ahead of has one barrier per buffer slot, so that no
+// waiter can ever be two phases behind the barrier it polls.
 enum Bar {
-    B_QFULL = 0,                 // + q stage (2): TMA landed q, k, g
-    B_QEMPTY = 2,                // + q stage (2): prep read them
-    B_VFULL = 4,                 // + v stage (3): TMA landed v (+ beta stored)
-    B_VEMPTY = 7,                // + v stage (3): the V product and the solver are done with it
-    B_OPS_READY = 10,            // + step parity (2): prep wrote the step's operands and b_C
-    B_GRAM_DONE = 12,            // Gram product complete
-    B_A_READY = 13,              // A and Aqk of the step are in shared memory
-    B_SA_FREE = 14,              // the solver read A
-    B_PR_DONE = 15,              // P and R^T products complete
-    B_PR_FREE = 16,              // the chain read P and R^T out of TMEM
-    B_MMA1_DONE = 17,            // state reads complete
-    B_MMA3_DONE = 18,            // output and state-update products complete
-    B_OPS_FREE = 19,             // + step parity (2): every product of the step completed
-    B_DRAIN = 21,                // + issuing group (3): end-of-kernel drain of in-flight MMAs
-    B_COUNT = 24
+    B_QFULL = 0,                 // TMA landed q, k, g
+    B_QEMPTY = 1,                // prep read them
+    B_VFULL = 2,                 // + v stage (3): TMA landed v (+ beta stored)
+    B_VEMPTY = 5,                // + v stage (3): the V product and the solver are done with it
+    B_OPS_READY = 8,             // + slot (3): prep wrote the step's operands and b_C
+    B_GRAM_DONE = 11,            // + step parity (2): Gram product complete
+    B_EXTR_DONE = 13,            // + step parity (2): warps 2-3 read the Gram accumulator
+    B_A_READY = 15,              // A and Aqk of the step are in shared memory
+    B_SA_FREE = 16,              // the solver read A
+    B_BT_READY = 17,             // + slot (3): Bt of the step is in shared memory
+    B_PR_DONE = 20,              // P and R^T products complete
+    B_MMA1_DONE = 21,            // state reads complete
+    B_MMA3_DONE = 22,            // output and state-update products complete
+    B_OPS_FREE = 23,             // + slot (3): every product of the step completed
+    B_DRAIN = 26,                // + issuing group (2): end-of-kernel drain of in-flight MMAs
+    B_COUNT = 28
 };
 static_assert(B_COUNT <= (int)NUM_BARS, "barrier slots");
 
@@ -288,16 +299,16 @@ __device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t bytes) { return
 __device__ __forceinline__ void issue_vi(uint32_t tm, uint32_t sb, int buf, int vs)
 {
     const uint64_t a = smem_desc(sb + OFF_VRING + vs * TILE_BYTES, 4096, 1024);
-    const uint64_t b = smem_desc(sb + OFF_KK + buf * 16384 + 64, 0, 1024);
+    const uint64_t b = smem_desc(sb + kk_base(kEyeSlot) + kk_half(kEyeSlot), 0, 1024);
     const uint32_t d = tm + TM_D1 + 64 * buf;
     mma_ss(d, a, b, I_VI, 0);
     mma_ss(d, desc_at(a, 2048), desc_at(b, 32), I_VI, 1);
 }
 
 // state reads of a step: Dl^T = V^T - S^T K~^T (onto V^T), Y^T = S^T Q~^T (onto zeros)
-__device__ __forceinline__ void issue_mma1(uint32_t tm, uint32_t sb, int buf, uint64_t *done)
+__device__ __forceinline__ void issue_mma1(uint32_t tm, uint32_t sb, int buf, int slot, uint64_t *done)
 {
-    const uint64_t b = smem_desc(sb + OFF_MMA1B + buf * 16384, 16384, 1024);
+    const uint64_t b = smem_desc(sb + mma1b_off(slot), 16384, 1024);
     const uint32_t d = tm + TM_D1 + 64 * buf, a = tm + TM_SBF;
 #pragma unroll
     for (int k = 0; k < 8; ++k) mma_ts(d, a + 8 * k, desc_at(b, 2048 * k), I_MMA1, 1);
@@ -305,10 +316,10 @@ __device__ __forceinline__ void issue_mma1(uint32_t tm, uint32_t sb, int buf, ui
 }
 
 // outputs O^T += Dl^T P^T and the state update S^T += Dl^T R
-__device__ __forceinline__ void issue_mma23(uint32_t tm, uint32_t sb, int buf, uint64_t *done)
+__device__ __forceinline__ void issue_mma23(uint32_t tm, uint32_t sb, int buf, int slot, uint64_t *done)
 {
-    const uint64_t bp = smem_desc(sb + OFF_AB + buf * 8192, 0, 1024);
-    const uint64_t br = smem_desc(sb + OFF_KK + buf * 16384, 0, 1024);
+    const uint64_t bp = smem_desc(sb + ab_off(slot), 0, 1024);
+    const uint64_t br = smem_desc(sb + kk_base(slot) + kk_half(slot), 0, 1024);
     const uint32_t a = tm + TM_VBF;
     mma_ts(tm + TM_D1 + 64 * buf + 32, a, bp, I_MMA2, 1);
     mma_ts(tm + TM_D1 + 64 * buf + 32, a + 8, desc_at(bp, 32), I_MMA2, 1);
@@ -319,23 +330,23 @@ __device__ __forceinline__ void issue_mma23(uint32_t tm, uint32_t sb, int buf, u
 
 // Gram of a step (tf32: K = 8 channels, 32 bytes, per instruction); k-rows land in TMEM lanes
 // 64..95, q-rows in lanes 96..127
-__device__ __forceinline__ void issue_gram(uint32_t tm, uint32_t sb, uint64_t *done)
+__device__ __forceinline__ void issue_gram(uint32_t tm, uint32_t sb, int gb, uint64_t *done)
 {
     const uint64_t a = smem_desc(sb + OFF_GA - GA_REGION, 0, 1024);
     const uint64_t b = smem_desc(sb + OFF_GB, 0, 1024);
 #pragma unroll
     for (int k = 0; k < 16; ++k)
-        mma_ss_tf32(tm + TM_DG, desc_at(a, (k >> 2) * GA_REGION + (k & 3) * 32),
+        mma_ss_tf32(tm + TM_DG + 48 * gb, desc_at(a, (k >> 2) * GA_REGION + (k & 3) * 32),
                     desc_at(b, (k >> 2) * GB_REGION + (k & 3) * 32), I_GRAM, k > 0);
     mma_commit(done);
 }
 
 // P = Aqk Bt (rows 0..31 of the A operand are Aqk: lanes 0..31) and R^T = Kbar^T Bt (lane = key
 // channel); both with B = Bt^T rows
-__device__ __forceinline__ void issue_pr(uint32_t tm, uint32_t sb, int buf, uint64_t *done)
+__device__ __forceinline__ void issue_pr(uint32_t tm, uint32_t sb, int slot, uint64_t *done)
 {
-    const uint64_t ab = smem_desc(sb + OFF_AB + buf * 8192, 0, 1024);
-    const uint64_t kk = smem_desc(sb + OFF_KK + buf * 16384, 0, 1024);
+    const uint64_t ab = smem_desc(sb + ab_off(slot), 0, 1024);
+    const uint64_t kk = smem_desc(sb + kk_base(slot) + kk_half(slot), 0, 1024);
     const uint64_t bt = desc_at(ab, 64);
     mma_ss(tm + TM_DP, ab, bt, I_PR, 0);
     mma_ss(tm + TM_DP, desc_at(ab, 32), desc_at(bt, 32), I_PR, 1);
@@ -391,18 +402,24 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
     }
     if (j == 0) {
         tc_fence_after();
-        issue_mma1(tm, sb, 0, &bars[B_MMA1_DONE]);
+        issue_mma1(tm, sb, 0, 0, &bars[B_MMA1_DONE]);
     }
 
     TO *out = reinterpret_cast<TO *>(p.out);
     for (int s = 0; s < nsteps; ++s) {
-        const int buf = s & 1, vs = s % kVStages;
+        const int buf = s & 1, vs = s % kVStages, slot = s % kSlots, nslot = (s + 1) % kSlots;
         const uint32_t ph = s & 1;
         const long long t0 = start + (long long)s * C;
         const int valid = (int)((end - t0) < C ? (end - t0) : C);
         const bool last = (s == nsteps - 1);
 
-        // while the state reads run: R (all lanes) and P (lanes 0..31) into their operand buffers
+        // P and R^T of the step (Bt from the solver), then, while the state reads run, R (all
+        // lanes) and P (lanes 0..31) into their operand buffers
+        if (j == 0) {
+            wait_bar(&bars[B_BT_READY + slot], (s / kSlots) & 1, misc);
+            tc_fence_after();
+            issue_pr(tm, sb, slot, &bars[B_PR_DONE]);
+        }
         wait_bar(&bars[B_PR_DONE], ph, misc);
         if (j == 0) KDA_TRACE_EVENT(9, s);
         tc_fence_after();
@@ -411,17 +428,17 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
             float t[8];
             tmem_ld32(tb + TM_DR, r);
             tmem_wait_ld();
-            uint8_t *kk = smem + OFF_KK + buf * 16384;
+            uint8_t *kk = smem + kk_base(slot);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) t[i] = __uint_as_float(r[8 * m + i]);
-                store_chunk_f16(kk + sw128(j, 16 * m), t);            // R row = key channel j
+                store_chunk_f16(kk + sw128(j, kk_half(slot) + 16 * m), t);   // R row = key channel j
             }
             if (wq == 0) {
                 tmem_ld32(tb + TM_DP, r);
                 tmem_wait_ld();
-                uint8_t *ab = smem + OFF_AB + buf * 8192;
+                uint8_t *ab = smem + ab_off(slot);
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
 #pragma unroll
@@ -448,66 +465,69 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
         tc_fence_before();
         if (!gs.sync(misc)) break;
         if (j == 0) {
-            mbar_arrive(&bars[B_PR_FREE]);         // P and R^T read: the solver may issue again
             mbar_arrive(&bars[B_VEMPTY + vs]);     // the V product of this step has completed
             tc_fence_after();
-            issue_mma23(tm, sb, buf, &bars[B_MMA3_DONE]);
+            issue_mma23(tm, sb, buf, slot, &bars[B_MMA3_DONE]);
             KDA_TRACE_EVENT(12, s);
         }
 
-        // updated state S_{s+1}: checkpoint / final state, fp16 copy for the next state read,
-        // and the fp32 state pre-multiplied by the next step's decay
+        // updated state S_{s+1}: checkpoint / final state and the fp16 copy for the next state
+        // read first, so that the read is issued early; then the fp32 state pre-multiplied by
+        // the next step's decay (needed only by the next state update)
         wait_bar(&bars[B_MMA3_DONE], ph, misc);
-        if (j == 0) KDA_TRACE_EVENT(13, s);
         tc_fence_after();
-        if (j == 0) mbar_arrive(&bars[B_OPS_FREE + buf]);   // this step's operand buffers are free
-        if (!last) wait_bar(&bars[B_OPS_READY + (buf ^ 1)], ((s + 1) >> 1) & 1, misc);   // b_C(s+1)
-        if (j == 0) KDA_TRACE_EVENT(14, s);
+        if (j == 0) KDA_TRACE_EVENT(13, s);
+        if (j == 0) mbar_arrive(&bars[B_OPS_FREE + slot]);   // this step's operand buffers are free
         const long long done = (long long)(s + 1) * C;
         const bool ckpt = p.ckpt_stride > 0 && done <= end - start && (done % p.ckpt_stride) == 0;
         float *ck = nullptr;
         if (ckpt)
             ck = p.ckpts + ((misc->first_ckpt + done / p.ckpt_stride - 1) * p.H + h) * (long long)D * D;
-        const float *bcn = bc_all + (buf ^ 1) * D;
-        for (int c0 = 0; c0 < D; c0 += 64) {
-            uint32_t r[64], rb[32];
-            tmem_ld32(tb + TM_S32 + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-            tmem_ld32(tb + TM_S32 + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t r[32], rb[16];
+            tmem_ld32(tb + TM_S32 + c0, r);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) rb[i] = pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-            tmem_st16(tb + TM_SBF + c0 / 2, *reinterpret_cast<uint32_t(*)[16]>(&rb[0]));
-            tmem_st16(tb + TM_SBF + c0 / 2 + 16, *reinterpret_cast<uint32_t(*)[16]>(&rb[16]));
+            for (int i = 0; i < 16; ++i) rb[i] = pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            tmem_st16(tb + TM_SBF + c0 / 2, rb);
             if (ck) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) ck[(long long)(c0 + i) * D + j] = __uint_as_float(r[i]);
+                for (int i = 0; i < 32; ++i) ck[(long long)(c0 + i) * D + j] = __uint_as_float(r[i]);
             }
-            if (last) {
-                if (p.final_state) {
+            if (last && p.final_state) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) p.final_state[sbase + (long long)(c0 + i) * D + j] = __uint_as_float(r[i]);
-                }
-            } else {
+                for (int i = 0; i < 32; ++i) p.final_state[sbase + (long long)(c0 + i) * D + j] = __uint_as_float(r[i]);
+            }
+        }
+        if (!last) wait_bar(&bars[B_OPS_READY + nslot], ((s + 1) / kSlots) & 1, misc);   // step s+1
+        if (j == 0) KDA_TRACE_EVENT(14, s);
+        tmem_wait_st();
+        tc_fence_before();
+        if (!gs.sync(misc)) break;
+        if (j == 0) KDA_TRACE_EVENT(15, s);
+        if (!last && j == 0) {   // next step's state reads overlap the rest of this step
+            tc_fence_after();
+            issue_mma1(tm, sb, buf ^ 1, nslot, &bars[B_MMA1_DONE]);
+            KDA_TRACE_EVENT(16, s);
+        }
+        if (!last) {
+            const float *bcn = bc_all + nslot * D;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tb + TM_S32 + c0, r);
+                tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 64; i += 4) {
+                for (int i = 0; i < 32; i += 4) {
                     const float4 b4 = *reinterpret_cast<const float4 *>(bcn + c0 + i);
                     const float2 lo = mul2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), make_float2(b4.x, b4.y));
                     const float2 hi = mul2(make_float2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])), make_float2(b4.z, b4.w));
                     r[i] = __float_as_uint(lo.x); r[i + 1] = __float_as_uint(lo.y);
                     r[i + 2] = __float_as_uint(hi.x); r[i + 3] = __float_as_uint(hi.y);
                 }
-                tmem_st32(tb + TM_S32 + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                tmem_st32(tb + TM_S32 + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                tmem_st32(tb + TM_S32 + c0, r);
             }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        if (!gs.sync(misc)) break;
-        if (j == 0) KDA_TRACE_EVENT(15, s);
-        if (!last && j == 0) {   // next step's state reads overlap this step's output epilogue
-            tc_fence_after();
-            issue_mma1(tm, sb, buf ^ 1, &bars[B_MMA1_DONE]);
-            KDA_TRACE_EVENT(16, s);
         }
 
         // outputs of this step: O^T[j][r]
@@ -562,9 +582,9 @@ __device__ __forceinline__ void store_tf32x2(uint8_t *addr, float2 v)
 //   F = cumulative retention from the own tile's start through the token,
 //   G = retention after the token through the own tile's end,
 //   E = from the step's start through the token,  X = after the token through the step's end.
-__device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg, int p, int buf,
+__device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg, int p, int slot,
                                               int valid, Misc *misc, GroupSync &gs, bool &ok,
-                                              uint64_t *gram_done, int s)
+                                              uint64_t *bars, uint64_t *q_empty, int s)
 {
     constexpr float LOG2E = 1.4426950408889634f;
     const int cp = p & 63, qr = p >> 6, tile = qr >> 1;
@@ -594,33 +614,31 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
     }
     tot[qr * 64 + cp] = f[7];
     ok = gs.sync(misc) && ok;
-    if (s >= 1) wait_bar(gram_done, (s - 1) & 1, misc);   // the previous Gram read its operands
+    // the previous Gram has read its operands
+    if (s >= 1) wait_bar(&bars[B_GRAM_DONE + ((s - 1) & 1)], ((s - 1) >> 1) & 1, misc);
     if (p == 0) KDA_TRACE_EVENT(1, s);
     const float2 P0 = tot[cp], P1 = tot[64 + cp], P2 = tot[128 + cp], P3 = tot[192 + cp];
     const float2 B0 = mul2(P0, P1), B1 = mul2(P2, P3);
     const float2 one = make_float2(1.f, 1.f);
     const float2 pre = (qr & 1) ? (qr == 1 ? P0 : P2) : one;
     const float2 suf = (qr & 1) ? one : (qr == 0 ? P1 : P3);
-    if (qr == 0) reinterpret_cast<float2 *>(smem + OFF_BC + buf * D * 4)[cp] = mul2(B0, B1);
+    if (qr == 0) reinterpret_cast<float2 *>(smem + OFF_BC + slot * D * 4)[cp] = mul2(B0, B1);
     const float2 emul = tile ? mul2(pre, B0) : pre;      // E = f * emul
     const float2 xmul = tile ? suf : mul2(suf, B1);      // X = gl * xmul
     // 1/F = G / (tile total): F G is the tile's total retention for every token of the tile, so
     // one reciprocal per channel replaces one per token (the total is >= e^-80, a normal float)
     const float2 Bt = tile ? B1 : B0;
     const float2 ginv = mul2(suf, make_float2(__fdividef(1.f, Bt.x), __fdividef(1.f, Bt.y)));
-    uint8_t *mma1b = smem + OFF_MMA1B + buf * 16384;
-    uint8_t *kk = smem + OFF_KK + buf * 16384;
+    uint8_t *mma1b = smem + mma1b_off(slot);
+    uint8_t *kk = smem + kk_base(slot);
+    const uint32_t kh = kk_half(slot);
     uint8_t *ga_c = smem + OFF_GA + (c0 >> 5) * GA_REGION;
     uint8_t *gb_c = smem + OFF_GB + (c0 >> 5) * GB_REGION;
     const uint32_t cb = (c0 & 31) * 4;
-    float qt0[8], qt1[8], kt0[8], kt1[8], kb0[8], kb1[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int r = 8 * qr + i;
         const float2 F = mul2(f[i], pre), G = mul2(gl[i], suf);
-        const float2 E = mul2(f[i], emul), X = mul2(gl[i], xmul);
-        const float2 qt = mul2(qv[i], E), kt = mul2(kv[i], E), kb = mul2(kv[i], X);
-        qt0[i] = qt.x; qt1[i] = qt.y; kt0[i] = kt.x; kt1[i] = kt.y; kb0[i] = kb.x; kb1[i] = kb.y;
         // Gram operands, fp32 K-major (tf32 product): row = token (A: k rows 0..31, q rows
         // 32..63; B: k/F rows 0..31, tile-0 k*G rows 32..47), column = channel
         store_tf32x2(ga_c + sw128(r, cb), mul2(kv[i], F));                                  // K_L
@@ -628,15 +646,32 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
         store_tf32x2(gb_c + sw128(r, cb), mul2(kv[i], mul2(gl[i], ginv)));                // k/F
         if (tile == 0) store_tf32x2(gb_c + sw128(32 + r, cb), mul2(kv[i], G));              // k*G
     }
-    // operands of the state products (double-buffered), 8 tokens = one 16-byte chunk per row
+    // the Gram product can start while the operands of the state products are written
+    fence_proxy_async_smem();
+    ok = gs.sync(misc) && ok;
+    if (p == 0) {
+        mbar_arrive(q_empty);   // q, k, g of the step are all in registers
+        // the Gram accumulator of this parity was read two steps ago
+        if (s >= 2) wait_bar(&bars[B_EXTR_DONE + (s & 1)], ((s >> 1) - 1) & 1, misc);
+        tc_fence_after();
+        issue_gram(misc->tmem_base, smem_u32(smem), s & 1, &bars[B_GRAM_DONE + (s & 1)]);
+    }
+    float qt0[8], qt1[8], kt0[8], kt1[8], kb0[8], kb1[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float2 E = mul2(f[i], emul), X = mul2(gl[i], xmul);
+        const float2 qt = mul2(qv[i], E), kt = mul2(kv[i], E), kb = mul2(kv[i], X);
+        qt0[i] = qt.x; qt1[i] = qt.y; kt0[i] = kt.x; kt1[i] = kt.y; kb0[i] = kb.x; kb1[i] = kb.y;
+    }
+    // operands of the state products (one slot per step), 8 tokens = one 16-byte chunk per row
 #pragma unroll
     for (int i = 0; i < 8; ++i) { kt0[i] = -kt0[i]; kt1[i] = -kt1[i]; }
     store_chunk_f16(mma1b + sw128(c0, qr * 16), kt0);                // -K~  (MMA1 B, N=r)
     store_chunk_f16(mma1b + sw128(c0 + 1, qr * 16), kt1);
     store_chunk_f16(mma1b + sw128(c0, (4 + qr) * 16), qt0);          // Q~   (MMA1 B, N=32+r)
     store_chunk_f16(mma1b + sw128(c0 + 1, (4 + qr) * 16), qt1);
-    store_chunk_f16(kk + sw128(c0, qr * 16), kb0);                   // Kbar (R product A, k=r)
-    store_chunk_f16(kk + sw128(c0 + 1, qr * 16), kb1);
+    store_chunk_f16(kk + sw128(c0, kh + qr * 16), kb0);              // Kbar (R product A, k=r)
+    store_chunk_f16(kk + sw128(c0 + 1, kh + qr * 16), kb1);
 }
 
 __device__ void prep_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
@@ -647,27 +682,27 @@ __device__ void prep_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
 
     for (int s = 0; s < nsteps; ++s) {
         bool ok = true;
-        const int qs = s % kQStages, buf = s & 1;
+        const int qs = s % kQStages, slot = s % kSlots;
         const long long t0 = start + (long long)s * C;
         const int valid = (int)((end - t0) < C ? (end - t0) : C);
-        if (s >= 2) wait_bar(&bars[B_OPS_FREE + buf], ((s >> 1) - 1) & 1, misc);
+        if (s >= kSlots) wait_bar(&bars[B_OPS_FREE + slot], ((s / kSlots) - 1) & 1, misc);
         wait_bar(&bars[B_QFULL + qs], (s / kQStages) & 1, misc);
         if (p == 0) KDA_TRACE_EVENT(0, s);
-        prep_operands(smem, smem + OFF_QRING + qs * QSTAGE_BYTES, p, buf, valid, misc, gs, ok,
-                      &bars[B_GRAM_DONE], s);
+        prep_operands(smem, smem + OFF_QRING + qs * QSTAGE_BYTES, p, slot, valid, misc, gs, ok,
+                      bars, &bars[B_QEMPTY + qs], s);
         fence_proxy_async_smem();
         ok = gs.sync(misc) && ok;
         if (!ok) break;
         if (p == 0) {
-            mbar_arrive(&bars[B_QEMPTY + qs]);        // q, k, g of this step fully read
-            mbar_arrive(&bars[B_OPS_READY + buf]);    // Gram operands, MMA1 B, Kbar, b_C written
+            mbar_arrive(&bars[B_OPS_READY + slot]);   // MMA1 B, Kbar, b_C written
             KDA_TRACE_EVENT(2, s);
         }
     }
+    if (p == 0) drain_mmas(&bars[B_DRAIN + 1], misc);
 }
 
 // ------------------------------------------------------------------------------------------------
-// Gram group (warps 2 and 3): warp 2's lane 0 issues each step's Gram product; warp 2 then reads
+// Gram group (warps 2 and 3): from each step's Gram accumulator (issued by prep), warp 2 reads
 // A = strict_lower(beta_r Gram_kk) (TMEM lanes 64..95) for the solver and warp 3 reads
 // Aqk = lower_incl_diag(Gram_qk) (lanes 96..127) as the A operand of the P product.
 
@@ -675,30 +710,23 @@ __device__ void gram_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
 {
     const int w = (threadIdx.x >> 5) - 2;      // 0: A, 1: Aqk
     const int lane = threadIdx.x & 31;
-    const uint32_t tm = misc->tmem_base;
-    const uint32_t tb = tm + ((uint32_t)(32 * (2 + w)) << 16);
-    const uint32_t sb = smem_u32(smem);
+    const uint32_t tb = misc->tmem_base + ((uint32_t)(32 * (2 + w)) << 16);
     float *sA = reinterpret_cast<float *>(smem + OFF_SA);
     const float *sbeta_all = reinterpret_cast<const float *>(smem + OFF_BETA);
-    const bool issuer = (w == 0 && lane == 0);
+    const bool leader = (w == 0 && lane == 0);
     GroupSync gs{3, 64};
 
-    if (issuer) {
-        wait_bar(&bars[B_OPS_READY + 0], 0, misc);
-        tc_fence_after();
-        issue_gram(tm, sb, &bars[B_GRAM_DONE]);
-    }
     for (int s = 0; s < nsteps; ++s) {
         const int vs = s % kVStages, buf = s & 1;
         const float *sbeta = sbeta_all + vs * C;
         wait_bar(&bars[B_VFULL + vs], (s / kVStages) & 1, misc);   // beta
-        wait_bar(&bars[B_GRAM_DONE], s & 1, misc);
+        wait_bar(&bars[B_GRAM_DONE + buf], (s >> 1) & 1, misc);
         if (w == 0 && s >= 1) wait_bar(&bars[B_SA_FREE], (s - 1) & 1, misc);
-        if (issuer) KDA_TRACE_EVENT(4, s);
+        if (leader) KDA_TRACE_EVENT(4, s);
         tc_fence_after();
         uint32_t r0[32], r1[16];
-        tmem_ld32(tb + TM_DG, r0);
-        tmem_ld16(tb + TM_DG + 32, r1);
+        tmem_ld32(tb + TM_DG + 48 * buf, r0);
+        tmem_ld16(tb + TM_DG + 48 * buf + 32, r1);
         tmem_wait_ld();
         const int r = lane;   // token row
         // Gram(r, i): row tile 0 -> column i; row tile 1 -> column 32 + i for i in tile 0 (right
@@ -718,7 +746,7 @@ __device__ void gram_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
                 *reinterpret_cast<float4 *>(sA + r * 36 + 4 * m) = v;
             }
         } else {
-            uint8_t *ab = smem + OFF_AB + buf * 8192;
+            uint8_t *ab = smem + ab_off(s % kSlots);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 float t[8];
@@ -730,18 +758,12 @@ __device__ void gram_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
         }
         tc_fence_before();
         if (!gs.sync(misc)) break;              // both warps have read the Gram accumulator
-        if (issuer) {
+        if (leader) {
             mbar_arrive(&bars[B_A_READY]);
+            mbar_arrive(&bars[B_EXTR_DONE + buf]);   // the Gram accumulator may be reused
             KDA_TRACE_EVENT(5, s);
-            if (s + 1 < nsteps) {
-                wait_bar(&bars[B_OPS_READY + (buf ^ 1)], ((s + 1) >> 1) & 1, misc);
-                tc_fence_after();
-                issue_gram(tm, sb, &bars[B_GRAM_DONE]);
-                KDA_TRACE_EVENT(3, s + 1);
-            }
         }
     }
-    if (issuer) drain_mmas(&bars[B_DRAIN + 1], misc);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -752,12 +774,10 @@ __device__ void gram_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
 __device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
 {
     const int lane = threadIdx.x & 31;
-    const uint32_t tm = misc->tmem_base;
-    const uint32_t sb = smem_u32(smem);
     const float *sA = reinterpret_cast<const float *>(smem + OFF_SA);
     const float *sbeta_all = reinterpret_cast<const float *>(smem + OFF_BETA);
     for (int s = 0; s < nsteps; ++s) {
-        const int vs = s % kVStages, buf = s & 1;
+        const int vs = s % kVStages;
         const bool ok = wait_bar(&bars[B_A_READY], s & 1, misc);
         if (!__all_sync(0xffffffffu, ok)) break;
         if (lane == 0) KDA_TRACE_EVENT(6, s);
@@ -786,10 +806,11 @@ __device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nstep
         const float bc = sbeta_all[vs * C + lane];
         __syncwarp();
         if (lane == 0) {
+            KDA_TRACE_EVENT(18, s);
             mbar_arrive(&bars[B_SA_FREE]);       // A read
             mbar_arrive(&bars[B_VEMPTY + vs]);   // beta read
         }
-        uint8_t *ab = smem + OFF_AB + buf * 8192;
+        uint8_t *ab = smem + ab_off(s % kSlots);
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             float t[8];
@@ -797,17 +818,15 @@ __device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nstep
             for (int i = 0; i < 4; ++i) { t[2 * i] = bc * x2[4 * m + i].x; t[2 * i + 1] = bc * x2[4 * m + i].y; }
             store_chunk_f16(ab + sw128(lane, 64 + 16 * m), t);   // row = column `lane` of Bt
         }
+        if (lane == 0) KDA_TRACE_EVENT(19, s);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            if (s >= 1) wait_bar(&bars[B_PR_FREE], (s - 1) & 1, misc);   // P, R^T of s-1 read
-            tc_fence_after();
-            issue_pr(tm, sb, buf, &bars[B_PR_DONE]);
+            mbar_arrive(&bars[B_BT_READY + s % kSlots]);   // the chain issues P and R^T
             KDA_TRACE_EVENT(8, s);
         }
         if (__any_sync(0xffffffffu, misc->abort != 0)) break;
     }
-    if (lane == 0) drain_mmas(&bars[B_DRAIN + 2], misc);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -838,6 +857,15 @@ __device__ void producer_role(const Params &p, const CUtensorMap *mq, const CUte
                 for (int half = 0; half < 2; ++half)
                     tma_load_3d(qkg + x * TILE_BYTES + half * 4096, maps[x], &bars[B_QFULL + qs],
                                 half * 64, h, (int)t0);
+            // the next step's q, k, g into L2, so that their load after this stage is released
+            // does not wait on HBM
+            if (s + 1 < nsteps) {
+#pragma unroll
+                for (int x = 0; x < 3; ++x)
+#pragma unroll
+                    for (int half = 0; half < 2; ++half)
+                        tma_prefetch_l2_3d(maps[x], half * 64, h, (int)(t0 + C));
+            }
             mbar_arrive_expect_tx(&bars[B_VFULL + vs], TILE_BYTES);
 #pragma unroll
             for (int half = 0; half < 2; ++half)
@@ -882,6 +910,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             mbar_init(&bars[B_VEMPTY + s], 2);       // the chain (V product) and the solver (beta)
         }
         for (int b = B_OPS_READY; b < B_COUNT; ++b) mbar_init(&bars[b], 1);
+        static_assert(B_OPS_READY == B_VEMPTY + kVStages, "barrier layout");
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -891,12 +920,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         tmem_alloc(&misc->tmem_base, TM_COLS);
         tmem_relinquish();
     }
-    // the constant B operand [I | 0] of the V product (bf16, rows n = 0..63, K = 32 tokens) in
-    // bytes 64..127 of rows 0..63 of both KK buffers
-    for (int e = threadIdx.x; e < 2 * 64 * 16; e += kThreads) {
-        const int b = e >> 10, row = (e >> 4) & 63, wd = e & 15;
+    // the constant B operand [I | 0] of the V product (bf16, rows n = 0..63, K = 32 tokens)
+    for (int e = threadIdx.x; e < 64 * 16; e += kThreads) {
+        const int row = e >> 4, wd = e & 15;
         const uint32_t lo = (row == 2 * wd) ? 0x3F80u : 0u, hi = (row == 2 * wd + 1) ? 0x3F80u : 0u;
-        *reinterpret_cast<uint32_t *>(smem + OFF_KK + b * 16384 + sw128(row, 64 + 4 * wd)) = lo | (hi << 16);
+        *reinterpret_cast<uint32_t *>(smem + kk_base(kEyeSlot) + sw128(row, kk_half(kEyeSlot) + 4 * wd)) =
+            lo | (hi << 16);
     }
     fence_proxy_async_smem();
     tc_fence_before();
