@@ -86,13 +86,16 @@ constexpr uint32_t OFF_BC = OFF_GB + 4 * GB_REGION;                  // step dec
 constexpr uint32_t OFF_SA = OFF_BC + kSlots * D * 4;                 // A (fp32) 32 x 36
 constexpr uint32_t OFF_TOT = OFF_SA + C * 36 * 4;                    // per-quarter decay totals
 constexpr uint32_t OFF_BETA = OFF_TOT + 4 * 64 * 8;                  // beta per v stage
-constexpr uint32_t OFF_BARS = OFF_BETA + kVStages * C * 4;
-constexpr uint32_t NUM_BARS = 32;
+// output tile of a full step, [32 tokens][128 channels] of the output type, stored by one TMA
+constexpr uint32_t OFF_OSTAGE = OFF_BETA + kVStages * C * 4;
+constexpr uint32_t OFF_BARS = OFF_OSTAGE + C * D * 4;
+constexpr uint32_t NUM_BARS = 40;
 constexpr uint32_t OFF_MISC = OFF_BARS + NUM_BARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;                   // alignment slack
 static_assert(SMEM_ALLOC <= 232448, "shared memory per block");
 static_assert(OFF_GA >= GA_REGION, "the first Gram region's leading rows stay inside the buffer");
+static_assert(OFF_OSTAGE % 128 == 0, "TMA store source alignment");
 
 // byte offsets of a slot's buffers; Kbar / R addresses add the slot's half-row offset before the
 // swizzle: kk_base(k) + sw128(row, kk_half(k) + byte)
@@ -125,8 +128,8 @@ constexpr uint32_t I_MMA3 = idesc_f32acc(128, 128, FMT_F16, 0, 0);
 enum Bar {
     B_QFULL = 0,                 // TMA landed q, k, g
     B_QEMPTY = 1,                // prep read them
-    B_VFULL = 2,                 // + v stage (3): TMA landed v (+ beta stored)
-    B_VEMPTY = 5,                // + v stage (3): the V product and the solver are done with it
+    B_VFULL = 2,                 // + v stage (3): TMA landed v
+    B_VEMPTY = 5,                // + v stage (3): the V product of the step completed
     B_OPS_READY = 8,             // + slot (3): prep wrote the step's operands and b_C
     B_GRAM_DONE = 11,            // + step parity (2): Gram product complete
     B_EXTR_DONE = 13,            // + step parity (2): warps 2-3 read the Gram accumulator
@@ -137,8 +140,11 @@ enum Bar {
     B_MMA1_DONE = 21,            // state reads complete
     B_MMA3_DONE = 22,            // output and state-update products complete
     B_OPS_FREE = 23,             // + slot (3): every product of the step completed
-    B_DRAIN = 26,                // + issuing group (2): end-of-kernel drain of in-flight MMAs
-    B_COUNT = 28
+    B_DRAIN = 26,                // + issuing thread (3): end-of-kernel drain of in-flight MMAs
+    B_SBF_READY = 29,            // the chain wrote the fp16 state copy the next state read uses
+    B_PR_FREE = 30,              // the chain read P and R^T out of TMEM
+    B_D1_FREE = 31,              // + step parity (2): the chain read a step's outputs
+    B_COUNT = 33
 };
 static_assert(B_COUNT <= (int)NUM_BARS, "barrier slots");
 
@@ -359,8 +365,8 @@ __device__ __forceinline__ void issue_pr(uint32_t tm, uint32_t sb, int slot, uin
 // chain group: thread j owns TMEM lane j = value channel j
 
 template <typename TO>
-__device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc *misc, int h,
-                           int nsteps)
+__device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem, uint64_t *bars,
+                           Misc *misc, int h, int nsteps)
 {
     const int j = threadIdx.x - 128;
     const int wq = j >> 5;  // TMEM sub-partition of this warp
@@ -373,14 +379,6 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
     const float *bc_all = reinterpret_cast<const float *>(smem + OFF_BC);
     GroupSync gs{1, 128};
 
-    // the V products of steps 0 and 1 go first: every later one is issued two steps ahead
-    if (j == 0) {
-        for (int s = 0; s < 2 && s < nsteps; ++s) {
-            wait_bar(&bars[B_VFULL + s], 0, misc);
-            tc_fence_after();
-            issue_vi(tm, sb, s, s);
-        }
-    }
     // initial state S^T[j][c] = S[c][j]: fp16 copy, and the fp32 state times step 0's decay
     wait_bar(&bars[B_OPS_READY + 0], 0, misc);
     for (int c0 = 0; c0 < D; c0 += 32) {
@@ -396,14 +394,8 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
     }
     tmem_wait_st();
     tc_fence_before();
-    if (!gs.sync(misc)) {
-        if (j == 0) drain_mmas(&bars[B_DRAIN + 0], misc);
-        return;
-    }
-    if (j == 0) {
-        tc_fence_after();
-        issue_mma1(tm, sb, 0, 0, &bars[B_MMA1_DONE]);
-    }
+    if (!gs.sync(misc)) return;
+    if (j == 0) mbar_arrive(&bars[B_SBF_READY]);   // the first state read may go
 
     TO *out = reinterpret_cast<TO *>(p.out);
     for (int s = 0; s < nsteps; ++s) {
@@ -413,13 +405,7 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
         const int valid = (int)((end - t0) < C ? (end - t0) : C);
         const bool last = (s == nsteps - 1);
 
-        // P and R^T of the step (Bt from the solver), then, while the state reads run, R (all
-        // lanes) and P (lanes 0..31) into their operand buffers
-        if (j == 0) {
-            wait_bar(&bars[B_BT_READY + slot], (s / kSlots) & 1, misc);
-            tc_fence_after();
-            issue_pr(tm, sb, slot, &bars[B_PR_DONE]);
-        }
+        // while the state reads run: R (all lanes) and P (lanes 0..31) into their operand buffers
         wait_bar(&bars[B_PR_DONE], ph, misc);
         if (j == 0) KDA_TRACE_EVENT(9, s);
         tc_fence_after();
@@ -465,6 +451,7 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
         tc_fence_before();
         if (!gs.sync(misc)) break;
         if (j == 0) {
+            mbar_arrive(&bars[B_PR_FREE]);         // P and R^T read: the next ones may be issued
             mbar_arrive(&bars[B_VEMPTY + vs]);     // the V product of this step has completed
             tc_fence_after();
             issue_mma23(tm, sb, buf, slot, &bars[B_MMA3_DONE]);
@@ -500,18 +487,46 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
                 for (int i = 0; i < 32; ++i) p.final_state[sbase + (long long)(c0 + i) * D + j] = __uint_as_float(r[i]);
             }
         }
-        if (!last) wait_bar(&bars[B_OPS_READY + nslot], ((s + 1) / kSlots) & 1, misc);   // step s+1
-        if (j == 0) KDA_TRACE_EVENT(14, s);
+        if (j == 0) {
+            KDA_TRACE_EVENT(14, s);
+            bulk_wait_read_all();   // the previous output tile has left the staging buffer
+        }
         tmem_wait_st();
         tc_fence_before();
         if (!gs.sync(misc)) break;
         if (j == 0) KDA_TRACE_EVENT(15, s);
-        if (!last && j == 0) {   // next step's state reads overlap the rest of this step
-            tc_fence_after();
-            issue_mma1(tm, sb, buf ^ 1, nslot, &bars[B_MMA1_DONE]);
+        if (!last && j == 0) mbar_arrive(&bars[B_SBF_READY]);   // the next state read may go
+        // outputs of this step: O^T[j][r].  A full step goes through the staging tile and one TMA
+        // store; a ragged last step (whose box would reach into the next sequence) is stored
+        // directly.
+        {
+            uint32_t r[32];
+            tmem_ld32(tb + TM_D1 + 64 * buf + 32, r);
+            tmem_wait_ld();
+            if (valid == C) {
+                TO *st = reinterpret_cast<TO *>(smem + OFF_OSTAGE) + j;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) store_out<TO>(st + i * D, __uint_as_float(r[i]));
+                fence_proxy_async_smem();
+            } else {
+                TO *o = out + (t0 * p.H + h) * (long long)D + j;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (i < valid) store_out<TO>(o + (long long)i * p.H * D, __uint_as_float(r[i]));
+            }
+        }
+        tc_fence_before();
+        if (!gs.sync(misc)) break;
+        if (j == 0) {
             KDA_TRACE_EVENT(16, s);
+            mbar_arrive(&bars[B_D1_FREE + buf]);   // outputs read: the V product two steps ahead
+            if (valid == C) {
+                tma_store_3d(mo, smem + OFF_OSTAGE, 0, h, (int)t0);
+                bulk_commit();
+            }
         }
         if (!last) {
+            wait_bar(&bars[B_OPS_READY + nslot], ((s + 1) / kSlots) & 1, misc);   // b_C(s+1)
             const float *bcn = bc_all + nslot * D;
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -529,27 +544,13 @@ __device__ void chain_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc 
                 tmem_st32(tb + TM_S32 + c0, r);
             }
         }
-
-        // outputs of this step: O^T[j][r]
-        {
-            uint32_t r[32];
-            tmem_ld32(tb + TM_D1 + 64 * buf + 32, r);
-            tmem_wait_ld();
-            TO *o = out + (t0 * p.H + h) * (long long)D + j;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (i < valid) store_out<TO>(o + (long long)i * p.H * D, __uint_as_float(r[i]));
-        }
-        tc_fence_before();
-        if (!gs.sync(misc)) break;
         if (j == 0) KDA_TRACE_EVENT(17, s);
-        if (j == 0 && s + 2 < nsteps) {   // D1 of this parity is free: V product two steps ahead
-            wait_bar(&bars[B_VFULL + (s + 2) % kVStages], ((s + 2) / kVStages) & 1, misc);
-            tc_fence_after();
-            issue_vi(tm, sb, buf, (s + 2) % kVStages);
-        }
+
     }
-    if (j == 0) drain_mmas(&bars[B_DRAIN + 0], misc);
+    if (j == 0) {
+        drain_mmas(&bars[B_DRAIN + 0], misc);
+        bulk_wait_all();   // the last output tiles are written before the CTA leaves
+    }
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -706,20 +707,28 @@ __device__ void prep_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
 // A = strict_lower(beta_r Gram_kk) (TMEM lanes 64..95) for the solver and warp 3 reads
 // Aqk = lower_incl_diag(Gram_qk) (lanes 96..127) as the A operand of the P product.
 
-__device__ void gram_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
+__device__ void gram_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc *misc, int h,
+                          int nsteps)
 {
     const int w = (threadIdx.x >> 5) - 2;      // 0: A, 1: Aqk
     const int lane = threadIdx.x & 31;
     const uint32_t tb = misc->tmem_base + ((uint32_t)(32 * (2 + w)) << 16);
     float *sA = reinterpret_cast<float *>(smem + OFF_SA);
-    const float *sbeta_all = reinterpret_cast<const float *>(smem + OFF_BETA);
+    float *sbeta_all = reinterpret_cast<float *>(smem + OFF_BETA);
     const bool leader = (w == 0 && lane == 0);
+    const long long start = misc->start, end = misc->end;
     GroupSync gs{3, 64};
+    // beta of token `lane` of step t (warp 2), loaded one step ahead
+    auto load_beta = [&](int t) -> float {
+        const long long tok = start + (long long)t * C + lane;
+        return tok < end ? __bfloat162float(p.beta[tok * p.H + h]) : 0.f;
+    };
+    float bnext = (w == 0) ? load_beta(0) : 0.f;
 
     for (int s = 0; s < nsteps; ++s) {
-        const int vs = s % kVStages, buf = s & 1;
-        const float *sbeta = sbeta_all + vs * C;
-        wait_bar(&bars[B_VFULL + vs], (s / kVStages) & 1, misc);   // beta
+        const int buf = s & 1;
+        const float br = bnext;
+        if (w == 0 && s + 1 < nsteps) bnext = load_beta(s + 1);
         wait_bar(&bars[B_GRAM_DONE + buf], (s >> 1) & 1, misc);
         if (w == 0 && s >= 1) wait_bar(&bars[B_SA_FREE], (s - 1) & 1, misc);
         if (leader) KDA_TRACE_EVENT(4, s);
@@ -735,7 +744,8 @@ __device__ void gram_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
             return __uint_as_float((r >= 16 && i < 16) ? r1[i & 15] : r0[i & 31]);
         };
         if (w == 0) {
-            const float nbr = -sbeta[r];   // sA holds -A
+            sbeta_all[buf * C + r] = br;    // for the solver
+            const float nbr = -br;          // sA holds -A
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
                 float4 v;
@@ -777,7 +787,6 @@ __device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nstep
     const float *sA = reinterpret_cast<const float *>(smem + OFF_SA);
     const float *sbeta_all = reinterpret_cast<const float *>(smem + OFF_BETA);
     for (int s = 0; s < nsteps; ++s) {
-        const int vs = s % kVStages;
         const bool ok = wait_bar(&bars[B_A_READY], s & 1, misc);
         if (!__all_sync(0xffffffffu, ok)) break;
         if (lane == 0) KDA_TRACE_EVENT(6, s);
@@ -803,12 +812,11 @@ __device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nstep
             if (r & 1) x2[r / 2].y = xr; else x2[r / 2].x = xr;
         }
         if (lane == 0) KDA_TRACE_EVENT(7, s);
-        const float bc = sbeta_all[vs * C + lane];
+        const float bc = sbeta_all[(s & 1) * C + lane];
         __syncwarp();
         if (lane == 0) {
             KDA_TRACE_EVENT(18, s);
-            mbar_arrive(&bars[B_SA_FREE]);       // A read
-            mbar_arrive(&bars[B_VEMPTY + vs]);   // beta read
+            mbar_arrive(&bars[B_SA_FREE]);       // A and beta read
         }
         uint8_t *ab = smem + ab_off(s % kSlots);
 #pragma unroll
@@ -830,64 +838,101 @@ __device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nstep
 }
 
 // ------------------------------------------------------------------------------------------------
-// TMA producer (warp 0)
+// asynchronous issuer (lane 0 of warp 0): every TMA load, and the chain's V products, state reads
+// and P / R^T products, each issued as soon as its inputs are ready.  The barriers are polled
+// without blocking, so that no ready operation waits behind another one; every condition below
+// is checked only after its previous phase has been observed, so a parity test is never ahead.
 
-__device__ void producer_role(const Params &p, const CUtensorMap *mq, const CUtensorMap *mk,
-                              const CUtensorMap *mg, const CUtensorMap *mv, uint8_t *smem,
-                              uint64_t *bars, Misc *misc, int h, int nsteps)
+__device__ void issuer_role(const Params &p, const CUtensorMap *mq, const CUtensorMap *mk,
+                            const CUtensorMap *mg, const CUtensorMap *mv, uint8_t *smem,
+                            uint64_t *bars, Misc *misc, int h, int nsteps)
 {
-    const int lane = threadIdx.x & 31;
-    const long long start = misc->start, end = misc->end;
-    float *sbeta_all = reinterpret_cast<float *>(smem + OFF_BETA);
-    int issued = 0;
-    for (int s = 0; s < nsteps; ++s) {
-        if (misc->abort) break;
-        const int qs = s % kQStages, vs = s % kVStages;
-        if (s >= kQStages && !wait_bar(&bars[B_QEMPTY + qs], ((s / kQStages) - 1) & 1, misc)) break;
-        if (s >= kVStages && !wait_bar(&bars[B_VEMPTY + vs], ((s / kVStages) - 1) & 1, misc)) break;
-        const long long t0 = start + (long long)s * C;
-        uint8_t *qkg = smem + OFF_QRING + qs * QSTAGE_BYTES;
-        uint8_t *vt = smem + OFF_VRING + vs * TILE_BYTES;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[B_QFULL + qs], QSTAGE_BYTES);
-            const CUtensorMap *maps[3] = {mq, mk, mg};
+    const uint32_t tm = misc->tmem_base;
+    const uint32_t sb = smem_u32(smem);
+    const long long start = misc->start;
+    const CUtensorMap *maps[3] = {mq, mk, mg};
+    int sq = 0, sv = 0, cvi = 0, c1 = 0, cp = 0;
+    long long last = clock64();
+    while (c1 < nsteps || cp < nsteps) {
+        bool prog = false;
+        // q, k, g of step sq (one stage: free once prep holds step sq-1 in registers)
+        if (sq < nsteps && (sq == 0 || mbar_test_wait(&bars[B_QEMPTY], (sq - 1) & 1))) {
+            const int t0 = (int)(start + (long long)sq * C);
+            mbar_arrive_expect_tx(&bars[B_QFULL], QSTAGE_BYTES);
 #pragma unroll
             for (int x = 0; x < 3; ++x)
 #pragma unroll
                 for (int half = 0; half < 2; ++half)
-                    tma_load_3d(qkg + x * TILE_BYTES + half * 4096, maps[x], &bars[B_QFULL + qs],
-                                half * 64, h, (int)t0);
-            // the next step's q, k, g into L2, so that their load after this stage is released
-            // does not wait on HBM
-            if (s + 1 < nsteps) {
+                    tma_load_3d(smem + OFF_QRING + x * TILE_BYTES + half * 4096, maps[x], &bars[B_QFULL],
+                                half * 64, h, t0);
+            if (sq + 1 < nsteps) {   // the next step's tiles into L2
 #pragma unroll
                 for (int x = 0; x < 3; ++x)
 #pragma unroll
-                    for (int half = 0; half < 2; ++half)
-                        tma_prefetch_l2_3d(maps[x], half * 64, h, (int)(t0 + C));
+                    for (int half = 0; half < 2; ++half) tma_prefetch_l2_3d(maps[x], half * 64, h, t0 + C);
             }
-            mbar_arrive_expect_tx(&bars[B_VFULL + vs], TILE_BYTES);
+            ++sq;
+            prog = true;
+        }
+        // v of step sv (three stages: free once the V product of step sv-3 has completed)
+        if (sv < nsteps && (sv < kVStages || mbar_test_wait(&bars[B_VEMPTY + sv % kVStages], ((sv / kVStages) - 1) & 1))) {
+            const int t0 = (int)(start + (long long)sv * C);
+            uint8_t *vt = smem + OFF_VRING + (sv % kVStages) * TILE_BYTES;
+            mbar_arrive_expect_tx(&bars[B_VFULL + sv % kVStages], TILE_BYTES);
 #pragma unroll
             for (int half = 0; half < 2; ++half)
-                tma_load_3d(vt + half * 4096, mv, &bars[B_VFULL + vs], half * 64, h, (int)t0);
+                tma_load_3d(vt + half * 4096, mv, &bars[B_VFULL + sv % kVStages], half * 64, h, t0);
+            ++sv;
+            prog = true;
         }
-        const long long t = t0 + lane;
-        sbeta_all[vs * C + lane] = t < end ? __bfloat162float(p.beta[t * p.H + h]) : 0.f;
-        mbar_arrive(&bars[B_VFULL + vs]);
-        issued = s + 1;
+        // V product of step cvi: its v landed, and the chain read the outputs of step cvi-2
+        if (cvi < sv && mbar_test_wait(&bars[B_VFULL + cvi % kVStages], (cvi / kVStages) & 1) &&
+            (cvi < 2 || mbar_test_wait(&bars[B_D1_FREE + (cvi & 1)], ((cvi - 2) >> 1) & 1))) {
+            tc_fence_after();
+            issue_vi(tm, sb, cvi & 1, cvi % kVStages);
+            ++cvi;
+            prog = true;
+        }
+        // state reads of step c1: after its V product, the chain's fp16 state copy and prep's
+        // operands
+        if (c1 < cvi && mbar_test_wait(&bars[B_SBF_READY], c1 & 1) &&
+            mbar_test_wait(&bars[B_OPS_READY + c1 % kSlots], (c1 / kSlots) & 1)) {
+            tc_fence_after();
+            issue_mma1(tm, sb, c1 & 1, c1 % kSlots, &bars[B_MMA1_DONE]);
+            ++c1;
+            prog = true;
+        }
+        // P and R^T of step cp: Bt from the solver, and the chain read those of step cp-1
+        if (cp < nsteps && mbar_test_wait(&bars[B_BT_READY + cp % kSlots], (cp / kSlots) & 1) &&
+            (cp == 0 || mbar_test_wait(&bars[B_PR_FREE], (cp - 1) & 1))) {
+            tc_fence_after();
+            issue_pr(tm, sb, cp % kSlots, &bars[B_PR_DONE]);
+            ++cp;
+            prog = true;
+        }
+        if (prog) {
+            last = clock64();
+        } else {
+            if (misc->abort) break;
+            if (clock64() - last > kTimeout) {
+                fail(misc);
+                break;
+            }
+            __nanosleep(32);
+        }
     }
-    // never leave the CTA with copies in flight
-    for (int s = (issued > kQStages ? issued - kQStages : 0); s < issued; ++s)
-        mbar_wait(&bars[B_QFULL + s % kQStages], (s / kQStages) & 1, &misc->zero, kTimeout);
-    for (int s = (issued > kVStages ? issued - kVStages : 0); s < issued; ++s)
-        mbar_wait(&bars[B_VFULL + s % kVStages], (s / kVStages) & 1, &misc->zero, kTimeout);
+    // never leave the CTA with copies or products in flight
+    if (sq > 0) mbar_wait(&bars[B_QFULL], (sq - 1) & 1, &misc->zero, kTimeout);
+    for (int t = (sv > kVStages ? sv - kVStages : 0); t < sv; ++t)
+        mbar_wait(&bars[B_VFULL + t % kVStages], (t / kVStages) & 1, &misc->zero, kTimeout);
+    drain_mmas(&bars[B_DRAIN + 2], misc);
 }
 
 template <typename TO>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                   const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUtensorMap mv,
-                  const Params p)
+                  const __grid_constant__ CUtensorMap mo, const Params p)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     // 1024-byte aligned base by pointer arithmetic on the shared array, so that the compiler keeps
@@ -906,8 +951,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             mbar_init(&bars[B_QEMPTY + s], 1);
         }
         for (int s = 0; s < kVStages; ++s) {
-            mbar_init(&bars[B_VFULL + s], 1 + 32);   // expect_tx arrival + one per lane (beta)
-            mbar_init(&bars[B_VEMPTY + s], 2);       // the chain (V product) and the solver (beta)
+            mbar_init(&bars[B_VFULL + s], 1);        // the expect_tx arrival
+            mbar_init(&bars[B_VEMPTY + s], 1);
         }
         for (int b = B_OPS_READY; b < B_COUNT; ++b) mbar_init(&bars[b], 1);
         static_assert(B_OPS_READY == B_VEMPTY + kVStages, "barrier layout");
@@ -942,13 +987,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 p.final_state[sbase + e] = p.init ? p.init[sbase + e] : 0.f;
         }
     } else if (warp == 0) {
-        producer_role(p, &mq, &mk, &mg, &mv, smem, bars, misc, h, nsteps);
+        if (threadIdx.x == 0) issuer_role(p, &mq, &mk, &mg, &mv, smem, bars, misc, h, nsteps);
     } else if (warp == 1) {
         solver_role(smem, bars, misc, nsteps);
     } else if (warp < 4) {
-        gram_role(smem, bars, misc, nsteps);
+        gram_role(p, smem, bars, misc, h, nsteps);
     } else if (warp < 8) {
-        chain_role<TO>(p, smem, bars, misc, h, nsteps);
+        chain_role<TO>(p, &mo, smem, bars, misc, h, nsteps);
     } else {
         prep_role(smem, bars, misc, nsteps);
     }
@@ -976,6 +1021,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
+// output tiles: [T, H, 128] of fp32 or bf16, box = 128 channels x 1 head x 32 tokens, unswizzled
+bool make_out_map(CUtensorMap *map, void *base, int H, int64_t T, bool f32)
+{
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t es = f32 ? 4 : 2;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)H * D * es};
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)C}, estr[3] = {1, 1, 1};
+    return enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap *map, const void *base, int H, int64_t T)
 {
     auto enc = encode_fn();
@@ -990,7 +1049,8 @@ bool make_map(CUtensorMap *map, const void *base, int H, int64_t T)
 
 template <typename TO>
 int launch_typed(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mg,
-                 const CUtensorMap &mv, const Params &p, int blocks, cudaStream_t stream)
+                 const CUtensorMap &mv, const CUtensorMap &mo, const Params &p, int blocks,
+                 cudaStream_t stream)
 {
     static std::once_flag once;
     static cudaError_t attr_rc = cudaSuccess;
@@ -999,7 +1059,7 @@ int launch_typed(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap
                                        SMEM_ALLOC);
     });
     if (attr_rc != cudaSuccess) return KDA_ERR_CUDA;
-    prefill_tc_kernel<TO><<<blocks, kThreads, SMEM_ALLOC, stream>>>(mq, mk, mg, mv, p);
+    prefill_tc_kernel<TO><<<blocks, kThreads, SMEM_ALLOC, stream>>>(mq, mk, mg, mv, mo, p);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -1028,9 +1088,10 @@ int launch_prefill_tc(const void *q, const void *k, const void *v, const void *g
     const int64_t blocks = (int64_t)n_seqs * n_heads;
     if (blocks == 0) return KDA_OK;
     if (blocks > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
-    CUtensorMap mq, mk, mg, mv;
+    CUtensorMap mq, mk, mg, mv, mo;
     if (!make_map(&mq, q, n_heads, total_tokens) || !make_map(&mk, k, n_heads, total_tokens) ||
-        !make_map(&mg, g, n_heads, total_tokens) || !make_map(&mv, v, n_heads, total_tokens))
+        !make_map(&mg, g, n_heads, total_tokens) || !make_map(&mv, v, n_heads, total_tokens) ||
+        !make_out_map(&mo, out, n_heads, total_tokens, out_dtype != KDA_BF16))
         return KDA_ERR_CUDA;
     Params p;
     p.beta = static_cast<const __nv_bfloat16 *>(beta);
@@ -1043,8 +1104,8 @@ int launch_prefill_tc(const void *q, const void *k, const void *v, const void *g
     p.final_state = final_state;
     p.ckpt_stride = ckpt_stride;
     p.ckpts = ckpts;
-    if (out_dtype == KDA_BF16) return launch_typed<__nv_bfloat16>(mq, mk, mg, mv, p, (int)blocks, stream);
-    return launch_typed<float>(mq, mk, mg, mv, p, (int)blocks, stream);
+    if (out_dtype == KDA_BF16) return launch_typed<__nv_bfloat16>(mq, mk, mg, mv, mo, p, (int)blocks, stream);
+    return launch_typed<float>(mq, mk, mg, mv, mo, p, (int)blocks, stream);
 }
 
 #ifdef KDA_TRACE
