@@ -615,6 +615,7 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
     }
     tot[qr * 64 + cp] = f[7];
     ok = gs.sync(misc) && ok;
+    if (p == 0) mbar_arrive(q_empty);   // q, k, g of the step are all in registers
     // the previous Gram has read its operands
     if (s >= 1) wait_bar(&bars[B_GRAM_DONE + ((s - 1) & 1)], ((s - 1) >> 1) & 1, misc);
     if (p == 0) KDA_TRACE_EVENT(1, s);
@@ -651,7 +652,6 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
     fence_proxy_async_smem();
     ok = gs.sync(misc) && ok;
     if (p == 0) {
-        mbar_arrive(q_empty);   // q, k, g of the step are all in registers
         // the Gram accumulator of this parity was read two steps ago
         if (s >= 2) wait_bar(&bars[B_EXTR_DONE + (s & 1)], ((s >> 1) - 1) & 1, misc);
         tc_fence_after();
@@ -839,7 +839,7 @@ __device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nstep
 
 // ------------------------------------------------------------------------------------------------
 // asynchronous issuer (lane 0 of warp 0): every TMA load, and the chain's V products, state reads
-// and P / R^T products, each issued as soon as its inputs are ready.  The barriers are polled
+// and P / R^T products, each issued as soon as its inputs are ready (the chain's first).  The barriers are polled
 // without blocking, so that no ready operation waits behind another one; every condition below
 // is checked only after its previous phase has been observed, so a parity test is never ahead.
 
@@ -855,6 +855,47 @@ __device__ void issuer_role(const Params &p, const CUtensorMap *mq, const CUtens
     long long last = clock64();
     while (c1 < nsteps || cp < nsteps) {
         bool prog = false;
+        // the chain's products first (they are on its critical path), then the loads
+        // state reads of step c1: after its V product, the chain's fp16 state copy and prep's
+        // operands
+        if (c1 < cvi && mbar_test_wait(&bars[B_SBF_READY], c1 & 1) &&
+            mbar_test_wait(&bars[B_OPS_READY + c1 % kSlots], (c1 / kSlots) & 1)) {
+            KDA_TRACE_EVENT(21, c1);
+            tc_fence_after();
+            issue_mma1(tm, sb, c1 & 1, c1 % kSlots, &bars[B_MMA1_DONE]);
+            KDA_TRACE_EVENT(20, c1);
+            ++c1;
+            prog = true;
+        }
+        // P and R^T of step cp: Bt from the solver, and the chain read those of step cp-1
+        if (cp < nsteps && mbar_test_wait(&bars[B_BT_READY + cp % kSlots], (cp / kSlots) & 1) &&
+            (cp == 0 || mbar_test_wait(&bars[B_PR_FREE], (cp - 1) & 1))) {
+            tc_fence_after();
+            issue_pr(tm, sb, cp % kSlots, &bars[B_PR_DONE]);
+            KDA_TRACE_EVENT(3, cp);
+            ++cp;
+            prog = true;
+        }
+        // V product of step cvi: its v landed, and the chain read the outputs of step cvi-2
+        if (cvi < sv && mbar_test_wait(&bars[B_VFULL + cvi % kVStages], (cvi / kVStages) & 1) &&
+            (cvi < 2 || mbar_test_wait(&bars[B_D1_FREE + (cvi & 1)], ((cvi - 2) >> 1) & 1))) {
+            tc_fence_after();
+            issue_vi(tm, sb, cvi & 1, cvi % kVStages);
+            KDA_TRACE_EVENT(22, cvi);
+            ++cvi;
+            prog = true;
+        }
+        // v of step sv (three stages: free once the V product of step sv-3 has completed)
+        if (sv < nsteps && (sv < kVStages || mbar_test_wait(&bars[B_VEMPTY + sv % kVStages], ((sv / kVStages) - 1) & 1))) {
+            const int t0 = (int)(start + (long long)sv * C);
+            uint8_t *vt = smem + OFF_VRING + (sv % kVStages) * TILE_BYTES;
+            mbar_arrive_expect_tx(&bars[B_VFULL + sv % kVStages], TILE_BYTES);
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+                tma_load_3d(vt + half * 4096, mv, &bars[B_VFULL + sv % kVStages], half * 64, h, t0);
+            ++sv;
+            prog = true;
+        }
         // q, k, g of step sq (one stage: free once prep holds step sq-1 in registers)
         if (sq < nsteps && (sq == 0 || mbar_test_wait(&bars[B_QEMPTY], (sq - 1) & 1))) {
             const int t0 = (int)(start + (long long)sq * C);
@@ -872,42 +913,6 @@ __device__ void issuer_role(const Params &p, const CUtensorMap *mq, const CUtens
                     for (int half = 0; half < 2; ++half) tma_prefetch_l2_3d(maps[x], half * 64, h, t0 + C);
             }
             ++sq;
-            prog = true;
-        }
-        // v of step sv (three stages: free once the V product of step sv-3 has completed)
-        if (sv < nsteps && (sv < kVStages || mbar_test_wait(&bars[B_VEMPTY + sv % kVStages], ((sv / kVStages) - 1) & 1))) {
-            const int t0 = (int)(start + (long long)sv * C);
-            uint8_t *vt = smem + OFF_VRING + (sv % kVStages) * TILE_BYTES;
-            mbar_arrive_expect_tx(&bars[B_VFULL + sv % kVStages], TILE_BYTES);
-#pragma unroll
-            for (int half = 0; half < 2; ++half)
-                tma_load_3d(vt + half * 4096, mv, &bars[B_VFULL + sv % kVStages], half * 64, h, t0);
-            ++sv;
-            prog = true;
-        }
-        // V product of step cvi: its v landed, and the chain read the outputs of step cvi-2
-        if (cvi < sv && mbar_test_wait(&bars[B_VFULL + cvi % kVStages], (cvi / kVStages) & 1) &&
-            (cvi < 2 || mbar_test_wait(&bars[B_D1_FREE + (cvi & 1)], ((cvi - 2) >> 1) & 1))) {
-            tc_fence_after();
-            issue_vi(tm, sb, cvi & 1, cvi % kVStages);
-            ++cvi;
-            prog = true;
-        }
-        // state reads of step c1: after its V product, the chain's fp16 state copy and prep's
-        // operands
-        if (c1 < cvi && mbar_test_wait(&bars[B_SBF_READY], c1 & 1) &&
-            mbar_test_wait(&bars[B_OPS_READY + c1 % kSlots], (c1 / kSlots) & 1)) {
-            tc_fence_after();
-            issue_mma1(tm, sb, c1 & 1, c1 % kSlots, &bars[B_MMA1_DONE]);
-            ++c1;
-            prog = true;
-        }
-        // P and R^T of step cp: Bt from the solver, and the chain read those of step cp-1
-        if (cp < nsteps && mbar_test_wait(&bars[B_BT_READY + cp % kSlots], (cp / kSlots) & 1) &&
-            (cp == 0 || mbar_test_wait(&bars[B_PR_FREE], (cp - 1) & 1))) {
-            tc_fence_after();
-            issue_pr(tm, sb, cp % kSlots, &bars[B_PR_DONE]);
-            ++cp;
             prog = true;
         }
         if (prog) {
