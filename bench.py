@@ -56,6 +56,24 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The maximum of `value` over all ranks of the default process group (any backend: a CPU
+    tensor for gloo, a device tensor for NCCL).  Replicas finish when the slowest one does."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: float, slowest_ms: float, world: int) -> float:
+    """Whole-job throughput of `world` replicas that each process `units_per_rank` units, over
+    the slowest rank's time (weak scaling: the work per rank is fixed)."""
+    return world * units_per_rank / (slowest_ms / 1e3)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -227,11 +245,9 @@ def run_gb300(args):
     barrier()
     clk = clocks.stop()
     if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dev)
         per_ms = total_ms / args.steps
-    tokens_per_s = world * T1 * args.steps / (total_ms / 1e3)
+    tokens_per_s = replica_throughput(T1 * args.steps, total_ms, world)
     bytes_alg = T1 * H * BYTES_PER_TOKEN_HEAD + H * STATE_BYTES
     flops_alg = T1 * H * FLOP_PER_TOKEN_HEAD
     achieved_gbs = bytes_alg / (per_ms / 1e3) / 1e9
@@ -256,6 +272,8 @@ def run_gb300(args):
         e2e_step()
     barrier()
     e2e_ms, e2e_per = cuda_time_ms(e2e_step, max(3, args.steps // 2), stream)
+    if world > 1:
+        e2e_per = max_over_ranks(e2e_per, dev)
     h2d = sum(v.numel() * v.element_size() for v in hx.values())
     d2h = h_out.numel() * 4 + h_fin.numel() * 4
     del hx, h_out, h_fin
