@@ -148,6 +148,18 @@ int kda_state_copy(float *dst, const int64_t *dst_idx, int64_t n_dst_slots, cons
  */
 int kda_device_status(int32_t *status, void *stream);
 
+/*
+ * kda_diag_device_timeout -- failure-detection check.  Launches one CTA on `stream` whose bounded
+ * device wait is on a barrier that nothing completes; after `timeout_cycles` SM clock cycles
+ * (1 .. 4e9; 2e6 is about 1 ms) the wait gives up and records KDA_ERR_DEVICE_TIMEOUT in the device
+ * error word, through the same wait routine every kernel of the library uses.  A following
+ * kda_device_status() returns that code and clears it; the CUDA context stays usable.  The pages
+ * have no counterpart: it exists so that a caller (or a test) can see an expired device wait
+ * surface as an error status instead of a hang.
+ * Errors: KDA_ERR_INVALID_ARG (cycles out of range), KDA_ERR_CUDA.
+ */
+int kda_diag_device_timeout(int64_t timeout_cycles, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,7 +20,7 @@ from . import _lib
 from ._lib import KDAError
 
 __all__ = ["prefill", "prefill_recurrent", "decode", "state_copy", "device_status", "prefill_path",
-           "num_checkpoints", "KDAError", "load"]
+           "num_checkpoints", "KDAError", "load", "diag_device_timeout"]
 
 _DTYPES = {torch.bfloat16: _lib.KDA_BF16, torch.float32: _lib.KDA_F32}
 
@@ -188,3 +188,13 @@ def device_status(stream=None, device=None) -> int:
     st = ctypes.c_int32(0)
     _lib.check(lib.kda_device_status(ctypes.byref(st), _stream(dev, stream)), "kda_device_status")
     return int(st.value)
+
+
+def diag_device_timeout(timeout_cycles: int = 2_000_000, stream=None, device=None) -> None:
+    """Enqueue the library's failure-detection check: one CTA whose bounded device wait expires
+    after `timeout_cycles` SM cycles and records KDA_ERR_DEVICE_TIMEOUT, read back (and cleared)
+    by device_status()."""
+    lib = _lib.load()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _lib.check(lib.kda_diag_device_timeout(int(timeout_cycles), _stream(dev, stream)),
+               "kda_diag_device_timeout")

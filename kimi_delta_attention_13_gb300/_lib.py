@@ -31,6 +31,7 @@ SIGNATURES = {
                                    _vp]),
     "kda_state_copy": (ctypes.c_int, [_vp, _vp, _i64, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp]),
     "kda_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _vp]),
+    "kda_diag_device_timeout": (ctypes.c_int, [_i64, _vp]),
 }
 
 _LIB = None

@@ -136,6 +136,12 @@ int kda_state_copy(float *dst, const int64_t *dst_idx, int64_t n_dst_slots, cons
                              (cudaStream_t)stream);
 }
 
+int kda_diag_device_timeout(int64_t timeout_cycles, void *stream)
+{
+    if (timeout_cycles < 1 || timeout_cycles > 4000000000LL) return KDA_ERR_INVALID_ARG;
+    return kda::launch_wait_timeout_probe((long long)timeout_cycles, (cudaStream_t)stream);
+}
+
 int kda_device_status(int32_t *status, void *stream)
 {
     if (!status) return KDA_ERR_INVALID_ARG;

@@ -1070,6 +1070,32 @@ int launch_typed(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap
 
 }  // namespace
 
+namespace {
+
+// One CTA whose bounded wait is on a barrier that nothing ever completes: the same wait the prefill
+// kernel uses gives up after `cycles` SM cycles and records the timeout in the device error word.
+__global__ void wait_timeout_probe_kernel(long long cycles)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, &abort_flag, cycles))
+        atomicExch(&g_prefill_tc_error, KDA_ERR_DEVICE_TIMEOUT);
+}
+
+}  // namespace
+
+int launch_wait_timeout_probe(long long cycles, cudaStream_t stream)
+{
+    wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(cycles);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 int read_and_clear_status_prefill_tc(cudaStream_t s, int32_t *status)
 {
     int host = 0, zero = 0;

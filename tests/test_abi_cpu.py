@@ -117,3 +117,8 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(4, 2, 128)
     with pytest.raises(ValueError, match="CUDA"):
         kda.prefill(x, x, x, x, torch.zeros(4, 2))
+
+
+def test_diag_timeout_rejects_out_of_range_cycles(lib):
+    assert lib.kda_diag_device_timeout(0, None) == 1              # KDA_ERR_INVALID_ARG
+    assert lib.kda_diag_device_timeout(4_000_000_001, None) == 1
