@@ -310,6 +310,10 @@ def run_gb300(args):
     del src, dst
     torch.cuda.empty_cache()
 
+    reuse = prefix_reuse_figure(dev, stream)
+    assert kda.device_status() == 0
+    torch.cuda.empty_cache()
+
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -348,6 +352,7 @@ def run_gb300(args):
                    "bytes_alg": dec_bytes},
         "state_copy": {"workload": "64 states x 96 heads gathered by index (403 MB)",
                        "GB/s": cp_gbs, "frac": cp_gbs / hbm_peak, "ms": cp_ms},
+        "prefix_reuse": reuse,
         "gpu_launches": args.steps,
         "clocks": clk,
         "cpu_baseline": base,
@@ -357,6 +362,58 @@ def run_gb300(args):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def prefix_reuse_figure(dev, stream, n_req: int = 4, prefix: int = 16384, new_tokens: int = 1024,
+                        stride: int = 4096):
+    """Cache-hit prefill: `n_req` requests share a cached `prefix`-token sequence (checkpoints
+    every `stride` tokens) and each adds `new_tokens` tokens. The cache-hit path restores the
+    state at the prefix boundary (one kda_state_copy) and prefills only the new tokens; the full
+    path prefills prefix + new tokens of every request."""
+    import torch
+
+    import kimi_delta_attention_13_gb300 as kda
+    from kimi_delta_attention_13_gb300 import synth
+    from kimi_delta_attention_13_gb300.prefix_cache import CheckpointStore, resume_prefill
+
+    keys = ("q", "k", "v", "g", "beta")
+    base = synth.make_inputs([prefix], heads=H, dtype="bf16", seed=7, device=dev)
+    _, _, ck = kda.prefill(*[base[k] for k in keys], ckpt_stride=stride, lengths=[prefix], stream=stream)
+    store = CheckpointStore(prefix // stride, H, device=dev)
+    store.add_checkpoints(["base"], ck, stride, [prefix], stream=stream)
+    del ck
+    new = synth.make_inputs([new_tokens] * n_req, heads=H, dtype="bf16", seed=8, device=dev)
+    slot, covered = store.lookup("base", prefix)
+    lens_hit = [new_tokens] * n_req
+    full = {k: torch.cat([t for i in range(n_req)
+                          for t in (base[k], new[k][i * new_tokens:(i + 1) * new_tokens])], 0)
+            for k in keys}
+    lens_full = [prefix + new_tokens] * n_req
+    cu_full = torch.tensor([0] + [sum(lens_full[:i + 1]) for i in range(n_req)], device=dev,
+                           dtype=torch.int32)
+    out_hit = torch.empty(n_req * new_tokens, H, D, device=dev)
+    out_full = torch.empty(sum(lens_full), H, D, device=dev)
+    fin = torch.empty(n_req, H, D, D, device=dev)
+
+    def hit():
+        resume_prefill(store, [slot] * n_req, *[new[k] for k in keys], new["cu_seqlens"], lens_hit,
+                       out=out_hit, final_state=fin, stream=stream)
+
+    def miss():
+        kda.prefill(*[full[k] for k in keys], cu_full, None, out=out_full, final_state=fin,
+                    lengths=lens_full, stream=stream)
+
+    for fn in (hit, miss):
+        fn()
+    _, hit_ms = cuda_time_ms(hit, 5, stream)
+    _, miss_ms = cuda_time_ms(miss, 3, stream)
+    served = n_req * (prefix + new_tokens)
+    return {"workload": f"{n_req} requests x ({prefix}-token cached prefix, checkpoints every "
+                        f"{stride}) + {new_tokens} new tokens, H={H}",
+            "cache_hit_ms": hit_ms, "full_prefill_ms": miss_ms,
+            "cache_hit_tokens_per_s": served / (hit_ms / 1e3),
+            "new_tokens_per_s": n_req * new_tokens / (hit_ms / 1e3),
+            "speedup": miss_ms / hit_ms, "restored_from_tokens": covered}
 
 
 def kbuild_source_hash() -> str:
