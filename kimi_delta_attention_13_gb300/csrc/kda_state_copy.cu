@@ -4,8 +4,8 @@
 // restarts a sequence from a stored KDA state at the same token boundary as the global
 // attention cache; this kernel moves such states between slot arrays:
 //     dst[dst_idx[i]] = src[src_idx[i]],  one slot = H * d_k * d_v fp32.
-// Pure HBM copy: 128-bit loads and stores, gridDim.y walks the slots, gridDim.x x blockDim.x
-// threads stride through one slot.  Indices outside their slot range skip the copy and set
+// Pure HBM copy: 128-bit streaming loads and stores, four loads in flight per thread ahead of
+// their stores; gridDim.y walks the slots, gridDim.x x blockDim.x threads stride through one slot.  Indices outside their slot range skip the copy and set
 // this unit's sticky error word.
 #include "kda_internal.cuh"
 
@@ -20,6 +20,7 @@ state_copy_kernel(V *__restrict__ dst, const int64_t *__restrict__ dst_idx, int6
                   const V *__restrict__ src, const int64_t *__restrict__ src_idx, int64_t n_src,
                   int64_t n, int64_t unit_vecs)
 {
+    constexpr int U = 4;   // loads in flight per thread before their stores
     for (int64_t i = blockIdx.y; i < n; i += gridDim.y) {
         const int64_t d = dst_idx ? dst_idx[i] : i;
         const int64_t s = src_idx ? src_idx[i] : i;
@@ -29,9 +30,16 @@ state_copy_kernel(V *__restrict__ dst, const int64_t *__restrict__ dst_idx, int6
         }
         V *out = dst + d * unit_vecs;
         const V *in = src + s * unit_vecs;
-        for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < unit_vecs;
-             e += (int64_t)gridDim.x * blockDim.x)
-            out[e] = __ldcs(in + e);
+        const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+        for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < unit_vecs; e += U * stride) {
+            V v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (e + u * stride < unit_vecs) v[u] = __ldcs(in + e + u * stride);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (e + u * stride < unit_vecs) __stcs(out + e + u * stride, v[u]);
+        }
     }
 }
 
@@ -62,8 +70,8 @@ int launch_state_copy(float *dst, const int64_t *dst_idx, int64_t n_dst, const f
     const unsigned ys = (unsigned)(n < 65535 ? n : 65535);
     if (unit_floats % 4 == 0) {
         const int64_t vecs = unit_floats / 4;
-        // enough blocks per slot that all SMs stream when few slots are copied
-        int64_t bx = (4LL * sms + ys - 1) / ys;
+        // enough blocks per slot that every SM is fully occupied (8 blocks of 256 threads)
+        int64_t bx = (8LL * sms + ys - 1) / ys;
         const int64_t need = (vecs + 255) / 256;
         if (bx > need) bx = need;
         if (bx < 1) bx = 1;
@@ -71,7 +79,7 @@ int launch_state_copy(float *dst, const int64_t *dst_idx, int64_t n_dst, const f
             reinterpret_cast<float4 *>(dst), dst_idx, n_dst, reinterpret_cast<const float4 *>(src),
             src_idx, n_src, n, vecs);
     } else {
-        int64_t bx = (4LL * sms + ys - 1) / ys;
+        int64_t bx = (8LL * sms + ys - 1) / ys;
         const int64_t need = (unit_floats + 255) / 256;
         if (bx > need) bx = need;
         if (bx < 1) bx = 1;
