@@ -85,7 +85,8 @@ constexpr uint32_t OFF_GB = OFF_GA + 4 * GA_REGION;                  // Gram B: 
 constexpr uint32_t OFF_BC = OFF_GB + 4 * GB_REGION;                  // step decay b_C, per slot
 constexpr uint32_t OFF_SA = OFF_BC + kSlots * D * 4;                 // A (fp32) 32 x 36
 constexpr uint32_t OFF_TOT = OFF_SA + C * 36 * 4;                    // per-quarter decay totals
-constexpr uint32_t OFF_BETA = OFF_TOT + 4 * 64 * 8;                  // beta per v stage
+constexpr uint32_t OFF_TB = OFF_TOT + 4 * 64 * 8;                    // T00 | T11 blocks, x2
+constexpr uint32_t OFF_BETA = OFF_TB + 2 * 2048;                     // beta per step parity
 // output tile of a full step, [32 tokens][128 channels] of the output type, stored by one TMA
 constexpr uint32_t OFF_OSTAGE = OFF_BETA + kVStages * C * 4;
 constexpr uint32_t OFF_BARS = OFF_OSTAGE + C * D * 4;
@@ -144,7 +145,8 @@ enum Bar {
     B_SBF_READY = 29,            // the chain wrote the fp16 state copy the next state read uses
     B_PR_FREE = 30,              // the chain read P and R^T out of TMEM
     B_D1_FREE = 31,              // + step parity (2): the chain read a step's outputs
-    B_COUNT = 33
+    B_T_READY = 33,              // + step parity (2): phase 1 of the solve wrote T00 and T11
+    B_COUNT = 35
 };
 static_assert(B_COUNT <= (int)NUM_BARS, "barrier slots");
 
@@ -703,135 +705,260 @@ __device__ void prep_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
 }
 
 // ------------------------------------------------------------------------------------------------
-// Gram group (warps 2 and 3): from each step's Gram accumulator (issued by prep), warp 2 reads
-// A = strict_lower(beta_r Gram_kk) (TMEM lanes 64..95) for the solver and warp 3 reads
-// Aqk = lower_incl_diag(Gram_qk) (lanes 96..127) as the A operand of the P product.
+// Two-warp block solve of T = (I + A)^-1 for the 32x32 strictly lower A, in 16x16 blocks:
+//   T = [[T00, 0], [T10, T11]],  T00 = (I + A00)^-1,  T11 = (I + A11)^-1,  T10 = T11 (-A10) T00.
+// Phase 1 (one warp): lane L < 16 forms column L of T00, lane L >= 16 column L-16 of T11, by a
+// 16-row forward substitution.  Phase 2 (two warps, columns 0..7 and 8..15 of T10): M = (-A10) T00
+// and T10 = T11 M, four rows per lane.  Shared memory holds -A (row stride 36) and, per step, T00
+// by columns and T11 by rows.
 
-__device__ void gram_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc *misc, int h,
-                          int nsteps)
+constexpr uint32_t TB_BYTES = 2 * 16 * 16 * 4;   // T00 columns + T11 rows, fp32
+static_assert(TB_BYTES == 2048, "shared-memory map reserves 2 KB per T-block buffer");
+
+// column (lane & 15) of T00 (lanes 0..15) or of T11 (lanes 16..31)
+__device__ __forceinline__ void solve_diag_blocks(const float *nA, int lane, float2 x2[8])
 {
-    const int w = (threadIdx.x >> 5) - 2;      // 0: A, 1: Aqk
+    const int base = (lane >> 4) * 16, c = lane & 15;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float *row = nA + (base + i) * 36 + base;
+        float2 a01 = make_float2((i == c) ? 1.f : 0.f, 0.f), a23 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < i / 4; ++m) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(row + 4 * m);
+            a01 = fma2(make_float2(a4.x, a4.y), x2[2 * m], a01);
+            a23 = fma2(make_float2(a4.z, a4.w), x2[2 * m + 1], a23);
+        }
+        if (i & 3) {
+            const int q0 = 4 * (i / 4);
+            const float4 a4 = *reinterpret_cast<const float4 *>(row + q0);
+            a01.x = fmaf(a4.x, x2[q0 / 2].x, a01.x);
+            if (i - q0 > 1) a01.y = fmaf(a4.y, x2[q0 / 2].y, a01.y);
+            if (i - q0 > 2) a23.x = fmaf(a4.z, x2[q0 / 2 + 1].x, a23.x);
+        }
+        const float xi = (a01.x + a01.y) + (a23.x + a23.y);
+        if (i & 1) x2[i / 2].y = xi; else x2[i / 2].x = xi;
+    }
+}
+
+// rows 4*(lane>>3) .. +3 of column c = 8*half + (lane & 7) of T10
+__device__ __forceinline__ void solve_offdiag(const float *nA, const float *tb, int half, int lane,
+                                              float t10[4])
+{
+    const int c = 8 * half + (lane & 7), rq = lane >> 3;
+    float2 tc[8];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const float4 v = *reinterpret_cast<const float4 *>(tb + c * 16 + 4 * g);
+        tc[2 * g] = make_float2(v.x, v.y);
+        tc[2 * g + 1] = make_float2(v.z, v.w);
+    }
+    float m4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float *row = nA + (16 + 4 * rq + k) * 36;
+        float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(row + 4 * g);
+            a01 = fma2(make_float2(a4.x, a4.y), tc[2 * g], a01);
+            a23 = fma2(make_float2(a4.z, a4.w), tc[2 * g + 1], a23);
+        }
+        m4[k] = (a01.x + a01.y) + (a23.x + a23.y);
+    }
+    float2 mc[8];   // M[:, c] from the four lanes of column c
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+        const int src = (lane & 7) + 8 * rr;
+        mc[2 * rr] = make_float2(__shfl_sync(0xffffffffu, m4[0], src), __shfl_sync(0xffffffffu, m4[1], src));
+        mc[2 * rr + 1] = make_float2(__shfl_sync(0xffffffffu, m4[2], src), __shfl_sync(0xffffffffu, m4[3], src));
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float *row = tb + 256 + (4 * rq + k) * 16;
+        float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const float4 t4 = *reinterpret_cast<const float4 *>(row + 4 * g);
+            a01 = fma2(make_float2(t4.x, t4.y), mc[2 * g], a01);
+            a23 = fma2(make_float2(t4.z, t4.w), mc[2 * g + 1], a23);
+        }
+        t10[k] = (a01.x + a01.y) + (a23.x + a23.y);
+    }
+}
+
+// phase 1 outputs: T00 columns and T11 rows to `tb`, and the Bt^T rows they fill
+// (row c = beta_c T[:, c], fp16, bytes 64..127 of the AB slot's 128-byte rows)
+__device__ __forceinline__ void store_diag_blocks(float *tb, uint8_t *ab, int lane, const float2 x2[8],
+                                                  float bc)
+{
+    const int c = lane & 15;
+    float t[8];
+    if (lane < 16) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            *reinterpret_cast<float4 *>(tb + c * 16 + 4 * g) =
+                make_float4(x2[2 * g].x, x2[2 * g].y, x2[2 * g + 1].x, x2[2 * g + 1].y);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { t[2 * i] = bc * x2[4 * m + i].x; t[2 * i + 1] = bc * x2[4 * m + i].y; }
+            store_chunk_f16(ab + sw128(lane, 64 + 16 * m), t);    // rows 0..15 of column `lane`
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            tb[256 + (2 * i) * 16 + c] = x2[i].x;
+            tb[256 + (2 * i + 1) * 16 + c] = x2[i].y;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = 0.f;
+        store_chunk_f16(ab + sw128(lane, 64), t);                 // rows 0..15: zero
+        store_chunk_f16(ab + sw128(lane, 80), t);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { t[2 * i] = bc * x2[4 * m + i].x; t[2 * i + 1] = bc * x2[4 * m + i].y; }
+            store_chunk_f16(ab + sw128(lane, 96 + 16 * m), t);    // rows 16..31 of column `lane`
+        }
+    }
+}
+
+// phase 2 output: rows 16 + 4*(lane>>3) .. +3 of Bt^T row c (fp16, one 8-byte store)
+__device__ __forceinline__ void store_offdiag(uint8_t *ab, int half, int lane, const float t10[4], float bc)
+{
+    const int c = 8 * half + (lane & 7), rq = lane >> 3;
+    const uint32_t lo = pack_f16x2(bc * t10[0], bc * t10[1]), hi = pack_f16x2(bc * t10[2], bc * t10[3]);
+    *reinterpret_cast<uint2 *>(ab + sw128(c, 96 + 8 * rq)) = make_uint2(lo, hi);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Gram rows of a step: row r of the accumulator, column i of the 32 tokens.  Row tile 0 -> column
+// i; row tile 1 -> column 32 + i for i in tile 0 (right operand relative to the end of tile 0),
+// column i for i in tile 1.
+
+struct GramRow {
+    uint32_t r0[32], r1[16];
+    __device__ __forceinline__ void load(uint32_t taddr)
+    {
+        tmem_ld32(taddr, r0);
+        tmem_ld16(taddr + 32, r1);
+        tmem_wait_ld();
+    }
+    __device__ __forceinline__ float at(int r, int i) const
+    {
+        return __uint_as_float((r >= 16 && i < 16) ? r1[i & 15] : r0[i & 31]);
+    }
+};
+
+// warp 2: A = strict_lower(beta_r Gram_kk) (TMEM lanes 64..95) into shared memory (negated) for the
+// solver warps, with beta, which this warp loads one step ahead.
+
+__device__ void a_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc *misc, int h, int nsteps)
+{
     const int lane = threadIdx.x & 31;
-    const uint32_t tb = misc->tmem_base + ((uint32_t)(32 * (2 + w)) << 16);
+    const uint32_t tb = misc->tmem_base + ((uint32_t)64 << 16);
     float *sA = reinterpret_cast<float *>(smem + OFF_SA);
     float *sbeta_all = reinterpret_cast<float *>(smem + OFF_BETA);
-    const bool leader = (w == 0 && lane == 0);
     const long long start = misc->start, end = misc->end;
-    GroupSync gs{3, 64};
-    // beta of token `lane` of step t (warp 2), loaded one step ahead
     auto load_beta = [&](int t) -> float {
         const long long tok = start + (long long)t * C + lane;
         return tok < end ? __bfloat162float(p.beta[tok * p.H + h]) : 0.f;
     };
-    float bnext = (w == 0) ? load_beta(0) : 0.f;
-
+    float bnext = load_beta(0);
     for (int s = 0; s < nsteps; ++s) {
         const int buf = s & 1;
         const float br = bnext;
-        if (w == 0 && s + 1 < nsteps) bnext = load_beta(s + 1);
-        wait_bar(&bars[B_GRAM_DONE + buf], (s >> 1) & 1, misc);
-        if (w == 0 && s >= 1) wait_bar(&bars[B_SA_FREE], (s - 1) & 1, misc);
-        if (leader) KDA_TRACE_EVENT(4, s);
+        if (s + 1 < nsteps) bnext = load_beta(s + 1);
+        bool ok = wait_bar(&bars[B_GRAM_DONE + buf], (s >> 1) & 1, misc);
+        if (s >= 1) ok = wait_bar(&bars[B_SA_FREE], (s - 1) & 1, misc) && ok;   // A of s-1 read
+        if (!__all_sync(0xffffffffu, ok)) break;
+        if (lane == 0) KDA_TRACE_EVENT(4, s);
         tc_fence_after();
-        uint32_t r0[32], r1[16];
-        tmem_ld32(tb + TM_DG + 48 * buf, r0);
-        tmem_ld16(tb + TM_DG + 48 * buf + 32, r1);
-        tmem_wait_ld();
-        const int r = lane;   // token row
-        // Gram(r, i): row tile 0 -> column i; row tile 1 -> column 32 + i for i in tile 0 (right
-        // operand relative to the end of tile 0), column i for i in tile 1
-        auto gram = [&](int i) -> float {
-            return __uint_as_float((r >= 16 && i < 16) ? r1[i & 15] : r0[i & 31]);
-        };
-        if (w == 0) {
-            sbeta_all[buf * C + r] = br;    // for the solver
-            const float nbr = -br;          // sA holds -A
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                float4 v;
-                v.x = (4 * m + 0 < r) ? nbr * gram(4 * m + 0) : 0.f;
-                v.y = (4 * m + 1 < r) ? nbr * gram(4 * m + 1) : 0.f;
-                v.z = (4 * m + 2 < r) ? nbr * gram(4 * m + 2) : 0.f;
-                v.w = (4 * m + 3 < r) ? nbr * gram(4 * m + 3) : 0.f;
-                *reinterpret_cast<float4 *>(sA + r * 36 + 4 * m) = v;
-            }
-        } else {
-            uint8_t *ab = smem + ab_off(s % kSlots);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                float t[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) t[i] = (8 * m + i <= r) ? gram(8 * m + i) : 0.f;
-                store_chunk_f16(ab + sw128(r, m * 16), t);          // Aqk row r
-            }
-            fence_proxy_async_smem();
-        }
+        GramRow g;
+        g.load(tb + TM_DG + 48 * buf);
         tc_fence_before();
-        if (!gs.sync(misc)) break;              // both warps have read the Gram accumulator
-        if (leader) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_EXTR_DONE + buf]);
+        const int r = lane;   // token row
+        sbeta_all[buf * C + r] = br;
+        const float nbr = -br;           // sA holds -A
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            float4 v;
+            v.x = (4 * m + 0 < r) ? nbr * g.at(r, 4 * m + 0) : 0.f;
+            v.y = (4 * m + 1 < r) ? nbr * g.at(r, 4 * m + 1) : 0.f;
+            v.z = (4 * m + 2 < r) ? nbr * g.at(r, 4 * m + 2) : 0.f;
+            v.w = (4 * m + 3 < r) ? nbr * g.at(r, 4 * m + 3) : 0.f;
+            *reinterpret_cast<float4 *>(sA + r * 36 + 4 * m) = v;
+        }
+        __syncwarp();
+        if (lane == 0) {
             mbar_arrive(&bars[B_A_READY]);
-            mbar_arrive(&bars[B_EXTR_DONE + buf]);   // the Gram accumulator may be reused
             KDA_TRACE_EVENT(5, s);
         }
     }
 }
 
-// ------------------------------------------------------------------------------------------------
-// solver (warp 1): T = (I + A)^-1 for the 32x32 strictly lower A, one column per lane, by forward
-// substitution x_r = delta_rc - sum_{q<r} A[r][q] x_q (shared memory holds -A); row c of Bt^T = beta_c T[:, c] (fp16, the B
-// operand of the P and R products); then P and R^T are issued.
+// solver warps.  Warp 1: phase 1 of the block solve (T00, T11) and half 0 of phase 2; warp 3: Aqk
+// = lower_incl_diag(Gram_qk) (TMEM lanes 96..127) into the P product's A operand, and half 1 of
+// phase 2.  Together they write Bt^T = (T diag(beta))^T (fp16, the B operand of the P and R
+// products, which the issuer starts once both have signalled).
 
-__device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
+__device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps, int half)
 {
     const int lane = threadIdx.x & 31;
-    const float *sA = reinterpret_cast<const float *>(smem + OFF_SA);
+    const float *nA = reinterpret_cast<const float *>(smem + OFF_SA);
     const float *sbeta_all = reinterpret_cast<const float *>(smem + OFF_BETA);
     for (int s = 0; s < nsteps; ++s) {
-        const bool ok = wait_bar(&bars[B_A_READY], s & 1, misc);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        if (lane == 0) KDA_TRACE_EVENT(6, s);
-        // x_r = delta_{r,lane} + sum_{q<r} (-A[r][q]) x_q, two packed accumulators per row
-        float2 x2[C / 2];
-#pragma unroll
-        for (int r = 0; r < C; ++r) {
-            float2 a01 = make_float2((r == lane) ? 1.f : 0.f, 0.f), a23 = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int m = 0; m < r / 4; ++m) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(sA + r * 36 + 4 * m);
-                a01 = fma2(make_float2(a4.x, a4.y), x2[2 * m], a01);
-                a23 = fma2(make_float2(a4.z, a4.w), x2[2 * m + 1], a23);
+        const int buf = s & 1, slot = s % kSlots;
+        float *tblk = reinterpret_cast<float *>(smem + OFF_TB + buf * TB_BYTES);
+        uint8_t *ab = smem + ab_off(slot);
+        bool ok;
+        if (half == 0) {
+            ok = wait_bar(&bars[B_A_READY], s & 1, misc);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            if (lane == 0) KDA_TRACE_EVENT(6, s);
+            float2 x2[8];
+            solve_diag_blocks(nA, lane, x2);
+            store_diag_blocks(tblk, ab, lane, x2, sbeta_all[buf * C + lane]);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bars[B_T_READY + buf]);   // T00 and T11 for the other half of phase 2
+                KDA_TRACE_EVENT(7, s);
             }
-            if (r & 3) {   // the partial group q = 4 floor(r/4) .. r-1
-                const int q0 = 4 * (r / 4);
-                const float4 a4 = *reinterpret_cast<const float4 *>(sA + r * 36 + q0);
-                a01.x = fmaf(a4.x, x2[q0 / 2].x, a01.x);
-                if (r - q0 > 1) a01.y = fmaf(a4.y, x2[q0 / 2].y, a01.y);
-                if (r - q0 > 2) a23.x = fmaf(a4.z, x2[q0 / 2 + 1].x, a23.x);
+        } else {
+            // Aqk of the step (q-rows of the Gram)
+            ok = wait_bar(&bars[B_GRAM_DONE + buf], (s >> 1) & 1, misc);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            GramRow g;
+            g.load(misc->tmem_base + ((uint32_t)96 << 16) + TM_DG + 48 * buf);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_EXTR_DONE + buf]);
+            const int r = lane;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                float t[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) t[i] = (8 * m + i <= r) ? g.at(r, 8 * m + i) : 0.f;
+                store_chunk_f16(ab + sw128(r, m * 16), t);          // Aqk row r
             }
-            const float xr = (a01.x + a01.y) + (a23.x + a23.y);
-            if (r & 1) x2[r / 2].y = xr; else x2[r / 2].x = xr;
+            ok = wait_bar(&bars[B_T_READY + buf], (s >> 1) & 1, misc);
+            if (!__all_sync(0xffffffffu, ok)) break;
         }
-        if (lane == 0) KDA_TRACE_EVENT(7, s);
-        const float bc = sbeta_all[(s & 1) * C + lane];
+        float t10[4];
+        solve_offdiag(nA, tblk, half, lane, t10);
+        const float bc = sbeta_all[buf * C + 8 * half + (lane & 7)];
         __syncwarp();
-        if (lane == 0) {
-            KDA_TRACE_EVENT(18, s);
-            mbar_arrive(&bars[B_SA_FREE]);       // A and beta read
-        }
-        uint8_t *ab = smem + ab_off(s % kSlots);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            float t[8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) { t[2 * i] = bc * x2[4 * m + i].x; t[2 * i + 1] = bc * x2[4 * m + i].y; }
-            store_chunk_f16(ab + sw128(lane, 64 + 16 * m), t);   // row = column `lane` of Bt
-        }
-        if (lane == 0) KDA_TRACE_EVENT(19, s);
+        if (lane == 0) mbar_arrive(&bars[B_SA_FREE]);   // A and beta of the step read
+        store_offdiag(ab, half, lane, t10, bc);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive(&bars[B_BT_READY + s % kSlots]);   // the chain issues P and R^T
-            KDA_TRACE_EVENT(8, s);
+            mbar_arrive(&bars[B_BT_READY + slot]);     // this warp's part of Aqk and Bt written
+            if (half == 0) KDA_TRACE_EVENT(8, s);
         }
         if (__any_sync(0xffffffffu, misc->abort != 0)) break;
     }
@@ -960,6 +1087,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             mbar_init(&bars[B_VEMPTY + s], 1);
         }
         for (int b = B_OPS_READY; b < B_COUNT; ++b) mbar_init(&bars[b], 1);
+        for (int b = 0; b < 2; ++b) mbar_init(&bars[B_EXTR_DONE + b], 2);   // warps 2 and 3
+        mbar_init(&bars[B_SA_FREE], 2);                                      // solver warps 1 and 3
+        for (int b = 0; b < kSlots; ++b) mbar_init(&bars[B_BT_READY + b], 2);
         static_assert(B_OPS_READY == B_VEMPTY + kVStages, "barrier layout");
         fence_barrier_init();
     }
@@ -993,10 +1123,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         }
     } else if (warp == 0) {
         if (threadIdx.x == 0) issuer_role(p, &mq, &mk, &mg, &mv, smem, bars, misc, h, nsteps);
-    } else if (warp == 1) {
-        solver_role(smem, bars, misc, nsteps);
-    } else if (warp < 4) {
-        gram_role(p, smem, bars, misc, h, nsteps);
+    } else if (warp == 1 || warp == 3) {
+        solver_role(smem, bars, misc, nsteps, warp == 3);
+    } else if (warp == 2) {
+        a_role(p, smem, bars, misc, h, nsteps);
     } else if (warp < 8) {
         chain_role<TO>(p, &mo, smem, bars, misc, h, nsteps);
     } else {
