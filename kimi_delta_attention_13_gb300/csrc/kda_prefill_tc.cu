@@ -17,7 +17,9 @@
 // With Dl = V - K~ S0 and Bt = T diag(beta), every product that involves the state is
 //   Dl = V - K~ S0,   O = Q~ S0 + P Dl  (P = Aqk Bt),   S_C = diag(b_C) S0 + R^T Dl  (R = Bt^T Kbar),
 // so the state reads need only the scaled q and k of the step, and P and R, which do not depend on
-// the state, are formed beside the chain.  Every exponential that can exceed 1 is formed inside
+// the state, are formed beside the chain.  The kernel carries -Dl, -P and -R (the identity of the V
+// product is -I and the solver writes -Bt): the products are unchanged and no operand needs an
+// explicit negation.
 // one 16-token tile or relative to a tile boundary, so each such factor lies within e^80 (Gram
 // blocks: left operand relative to its own tile start, right operand relative to the row tile's
 // start); factors <= 1 may underflow, which only drops terms below fp32 resolution.
@@ -66,11 +68,11 @@ constexpr uint32_t TILE_BYTES = 2 * C * 128;               // 64 channels x 32 r
 constexpr uint32_t QSTAGE_BYTES = 3 * TILE_BYTES;          // q, k, g
 constexpr uint32_t OFF_QRING = 0;
 constexpr uint32_t OFF_VRING = OFF_QRING + kQStages * QSTAGE_BYTES;
-// per slot (step mod 3): MMA1 B operand [-K~ | Q~] fp16, rows = key channel, 64 tokens (MN-major)
+// per slot (step mod 3): MMA1 B operand [K~ | Q~] fp16, rows = key channel, 64 tokens (MN-major)
 constexpr uint32_t OFF_MMA1B = OFF_VRING + kVStages * TILE_BYTES;
 // two buffers of 128-byte rows (row = key channel); slot k uses bytes 64*(k&1) .. +63 of buffer
 // k>>1: Kbar fp16 (A of the R product), then R fp16 (B of the state update).  Bytes 64..127 of
-// rows 0..63 of buffer 1 hold the constant [I | 0] (B of the V product).
+// rows 0..63 of buffer 1 hold the constant [-I | 0] (B of the V product).
 constexpr uint32_t OFF_KK = OFF_MMA1B + kSlots * 16384;
 // per slot, rows = token (32 rows): bytes 0..63 Aqk fp16 (A of the P product), then P fp16 (B of
 // the output product); bytes 64..127 Bt^T fp16 (B of the P and R products)
@@ -104,7 +106,7 @@ __host__ __device__ constexpr uint32_t mma1b_off(int k) { return OFF_MMA1B + k *
 __host__ __device__ constexpr uint32_t kk_base(int k) { return OFF_KK + (k >> 1) * 16384; }
 __host__ __device__ constexpr uint32_t kk_half(int k) { return (k & 1) * 64; }
 __host__ __device__ constexpr uint32_t ab_off(int k) { return OFF_AB + k * 4096; }
-constexpr int kEyeSlot = 3;   // the [I | 0] constant sits where a fourth Kbar slot would be
+constexpr int kEyeSlot = 3;   // the [-I | 0] constant sits where a fourth Kbar slot would be
 
 // TMEM column map
 constexpr uint32_t TM_S32 = 0;      // fp32 state S^T (lane j, column = key channel)
@@ -303,7 +305,7 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
 // units; every operand here lies below 256 KB, so the field never carries)
 __device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
-// D1 of a step: [V^T | 0] = V^T [I | 0] (v tile as an MN-major A operand, exact in fp32)
+// D1 of a step: [-V^T | 0] = V^T [-I | 0] (v tile as an MN-major A operand, exact in fp32)
 __device__ __forceinline__ void issue_vi(uint32_t tm, uint32_t sb, int buf, int vs)
 {
     const uint64_t a = smem_desc(sb + OFF_VRING + vs * TILE_BYTES, 4096, 1024);
@@ -313,7 +315,7 @@ __device__ __forceinline__ void issue_vi(uint32_t tm, uint32_t sb, int buf, int 
     mma_ss(d, desc_at(a, 2048), desc_at(b, 32), I_VI, 1);
 }
 
-// state reads of a step: Dl^T = V^T - S^T K~^T (onto V^T), Y^T = S^T Q~^T (onto zeros)
+// state reads of a step: -Dl^T = -V^T + S^T K~^T (onto -V^T), Y^T = S^T Q~^T (onto zeros)
 __device__ __forceinline__ void issue_mma1(uint32_t tm, uint32_t sb, int buf, int slot, uint64_t *done)
 {
     const uint64_t b = smem_desc(sb + mma1b_off(slot), 16384, 1024);
@@ -667,9 +669,7 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
         qt0[i] = qt.x; qt1[i] = qt.y; kt0[i] = kt.x; kt1[i] = kt.y; kb0[i] = kb.x; kb1[i] = kb.y;
     }
     // operands of the state products (one slot per step), 8 tokens = one 16-byte chunk per row
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { kt0[i] = -kt0[i]; kt1[i] = -kt1[i]; }
-    store_chunk_f16(mma1b + sw128(c0, qr * 16), kt0);                // -K~  (MMA1 B, N=r)
+    store_chunk_f16(mma1b + sw128(c0, qr * 16), kt0);                // K~   (MMA1 B, N=r)
     store_chunk_f16(mma1b + sw128(c0 + 1, qr * 16), kt1);
     store_chunk_f16(mma1b + sw128(c0, (4 + qr) * 16), qt0);          // Q~   (MMA1 B, N=32+r)
     store_chunk_f16(mma1b + sw128(c0 + 1, (4 + qr) * 16), qt1);
@@ -921,7 +921,7 @@ __device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nstep
             if (lane == 0) KDA_TRACE_EVENT(6, s);
             float2 x2[8];
             solve_diag_blocks(nA, lane, x2);
-            store_diag_blocks(tblk, ab, lane, x2, sbeta_all[buf * C + lane]);
+            store_diag_blocks(tblk, ab, lane, x2, -sbeta_all[buf * C + lane]);
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&bars[B_T_READY + buf]);   // T00 and T11 for the other half of phase 2
@@ -950,7 +950,7 @@ __device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nstep
         }
         float t10[4];
         solve_offdiag(nA, tblk, half, lane, t10);
-        const float bc = sbeta_all[buf * C + 8 * half + (lane & 7)];
+        const float bc = -sbeta_all[buf * C + 8 * half + (lane & 7)];
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_SA_FREE]);   // A and beta of the step read
         store_offdiag(ab, half, lane, t10, bc);
@@ -1100,10 +1100,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         tmem_alloc(&misc->tmem_base, TM_COLS);
         tmem_relinquish();
     }
-    // the constant B operand [I | 0] of the V product (bf16, rows n = 0..63, K = 32 tokens)
+    // the constant B operand [-I | 0] of the V product (bf16, rows n = 0..63, K = 32 tokens)
     for (int e = threadIdx.x; e < 64 * 16; e += kThreads) {
         const int row = e >> 4, wd = e & 15;
-        const uint32_t lo = (row == 2 * wd) ? 0x3F80u : 0u, hi = (row == 2 * wd + 1) ? 0x3F80u : 0u;
+        const uint32_t lo = (row == 2 * wd) ? 0xBF80u : 0u, hi = (row == 2 * wd + 1) ? 0xBF80u : 0u;
         *reinterpret_cast<uint32_t *>(smem + kk_base(kEyeSlot) + sw128(row, kk_half(kEyeSlot) + 4 * wd)) =
             lo | (hi << 16);
     }
