@@ -966,9 +966,11 @@ __device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nstep
 
 // ------------------------------------------------------------------------------------------------
 // asynchronous issuer (lane 0 of warp 0): every TMA load, and the chain's V products, state reads
-// and P / R^T products, each issued as soon as its inputs are ready (the chain's first).  The barriers are polled
-// without blocking, so that no ready operation waits behind another one; every condition below
-// is checked only after its previous phase has been observed, so a parity test is never ahead.
+// and P / R^T products, each issued as soon as its inputs are ready (the chain's first).  The
+// barriers are polled without blocking, so that no ready operation waits behind another one;
+// every condition below is checked only after its previous phase has been observed, so a parity
+// test is never ahead.  The next step's q, k, g need no L2 prefetch: prep releases the stage as
+// soon as it holds them in registers.
 
 __device__ void issuer_role(const Params &p, const CUtensorMap *mq, const CUtensorMap *mk,
                             const CUtensorMap *mg, const CUtensorMap *mv, uint8_t *smem,
@@ -1033,12 +1035,6 @@ __device__ void issuer_role(const Params &p, const CUtensorMap *mq, const CUtens
                 for (int half = 0; half < 2; ++half)
                     tma_load_3d(smem + OFF_QRING + x * TILE_BYTES + half * 4096, maps[x], &bars[B_QFULL],
                                 half * 64, h, t0);
-            if (sq + 1 < nsteps) {   // the next step's tiles into L2
-#pragma unroll
-                for (int x = 0; x < 3; ++x)
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) tma_prefetch_l2_3d(maps[x], half * 64, h, t0 + C);
-            }
             ++sq;
             prog = true;
         }
