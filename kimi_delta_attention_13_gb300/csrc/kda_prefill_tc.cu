@@ -20,22 +20,29 @@
 // the state, are formed beside the chain.  The kernel carries -Dl, -P and -R (the identity of the V
 // product is -I and the solver writes -Bt): the products are unchanged and no operand needs an
 // explicit negation.
-// one 16-token tile or relative to a tile boundary, so each such factor lies within e^80 (Gram
-// blocks: left operand relative to its own tile start, right operand relative to the row tile's
-// start); factors <= 1 may underflow, which only drops terms below fp32 resolution.
+// Every decay factor that scales an operand spans at most one 16-token tile or is taken relative
+// to a tile boundary, so each such factor lies within e^80 (Gram blocks: left operand relative to
+// its own tile start, right operand relative to the row tile's start); factors <= 1 may underflow,
+// which only drops terms below fp32 resolution.
 //
-// Work split: one CTA per (sequence, head), 512 threads; each group issues its own MMAs:
-//   warp 0        TMA producer: q, k, g, v tiles (32 tokens x 128, 128-byte swizzle) + beta
-//   warp 1        TMEM allocation; the solver: T = (I + A)^-1 by column forward substitution
-//                 (lane = column), Bt = T diag(beta) as MMA operand; issues P and R^T = Kbar^T Bt
-//   warps 2..3    Gram: issue the step's Gram product, read A (warp 2) and Aqk (warp 3) out of it
-//   warps 4..7    chain: thread j <-> TMEM lane j <-> value channel j.  fp32 state S^T in TMEM
-//                 (pre-multiplied by the step's decay), its fp16 copy in TMEM as the A operand
-//                 of the state reads; issues V (identity product), the state reads, the output
-//                 and state-update products; copies P and R into their operand buffers while the
-//                 state reads run; writes outputs, checkpoints and the final state
-//   warps 8..15   prep: decay cumprods and every scaled operand of a step, up to two steps ahead
-//                 of the chain.
+// Work split: one CTA per (sequence, head), 512 threads.  tcgen05.mma issue costs the issuing
+// thread tens of cycles per instruction, so the MMAs are spread over threads that would otherwise
+// wait:
+//   warp 0 lane 0  asynchronous issuer: TMA loads of q, k, g (one stage) and v (three stages), the
+//                  V products, the state reads and the P / R^T products, each as soon as its
+//                  inputs are ready (the q, k, g load first: prep waits on it)
+//   warp 1         TMEM allocation; the solve's diagonal blocks T00, T11 and half of T10
+//   warp 2         issues the step's Gram product and reads -A out of it (with beta, loaded one
+//                  step ahead)
+//   warp 3         reads Aqk out of the Gram; the other half of T10.  Warps 1 and 3 write
+//                  -Bt^T = -(T diag(beta))^T, the B operand of the P and R^T products
+//   warps 4..7     chain: thread j <-> TMEM lane j <-> value channel j.  fp32 state S^T in TMEM
+//                  (pre-multiplied by the step's decay), its fp16 copy in TMEM as the A operand
+//                  of the state reads; copies P and R into their operand buffers, forms Dl,
+//                  issues the output and state-update products; writes outputs (TMA store),
+//                  checkpoints and the final state
+//   warps 8..15    prep: decay cumprods and every scaled operand of a step, up to three steps
+//                  ahead of the chain
 // Accumulators and A operands live in TMEM (512 columns); B operands in shared memory.
 //
 // Precision: the max-error bound (2e-2 x RMS on outputs, 1e-2 on states) needs ~1e-3 relative
@@ -148,7 +155,8 @@ enum Bar {
     B_PR_FREE = 30,              // the chain read P and R^T out of TMEM
     B_D1_FREE = 31,              // + step parity (2): the chain read a step's outputs
     B_T_READY = 33,              // + step parity (2): phase 1 of the solve wrote T00 and T11
-    B_COUNT = 35
+    B_GOPS_READY = 35,           // prep wrote the Gram operands of the step
+    B_COUNT = 36
 };
 static_assert(B_COUNT <= (int)NUM_BARS, "barrier slots");
 
@@ -609,6 +617,9 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
                                make_float2(LOG2E, LOG2E));
         f[i] = make_float2(ex2_approx(gc.x), ex2_approx(gc.y));
     }
+    // this warp holds its part of q, k, g in registers: release the stage (one arrival per warp)
+    __syncwarp();
+    if ((p & 31) == 0) mbar_arrive(q_empty);
     // quarter-local products: gl = after the token to the quarter end, f = through the token
     {
         float2 acc = make_float2(1.f, 1.f);
@@ -619,7 +630,6 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
     }
     tot[qr * 64 + cp] = f[7];
     ok = gs.sync(misc) && ok;
-    if (p == 0) mbar_arrive(q_empty);   // q, k, g of the step are all in registers
     // the previous Gram has read its operands
     if (s >= 1) wait_bar(&bars[B_GRAM_DONE + ((s - 1) & 1)], ((s - 1) >> 1) & 1, misc);
     if (p == 0) KDA_TRACE_EVENT(1, s);
@@ -652,15 +662,11 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
         store_tf32x2(gb_c + sw128(r, cb), mul2(kv[i], mul2(gl[i], ginv)));                // k/F
         if (tile == 0) store_tf32x2(gb_c + sw128(32 + r, cb), mul2(kv[i], G));              // k*G
     }
-    // the Gram product can start while the operands of the state products are written
+    // the Gram product can start (warp 2 issues it) while the operands of the state products
+    // are written
     fence_proxy_async_smem();
     ok = gs.sync(misc) && ok;
-    if (p == 0) {
-        // the Gram accumulator of this parity was read two steps ago
-        if (s >= 2) wait_bar(&bars[B_EXTR_DONE + (s & 1)], ((s >> 1) - 1) & 1, misc);
-        tc_fence_after();
-        issue_gram(misc->tmem_base, smem_u32(smem), s & 1, &bars[B_GRAM_DONE + (s & 1)]);
-    }
+    if (p == 0) mbar_arrive(&bars[B_GOPS_READY]);
     float qt0[8], qt1[8], kt0[8], kt1[8], kb0[8], kb1[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -701,7 +707,6 @@ __device__ void prep_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nsteps)
             KDA_TRACE_EVENT(2, s);
         }
     }
-    if (p == 0) drain_mmas(&bars[B_DRAIN + 1], misc);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -868,6 +873,17 @@ __device__ void a_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc *mis
     float bnext = load_beta(0);
     for (int s = 0; s < nsteps; ++s) {
         const int buf = s & 1;
+        // the Gram of the step: its operands are written, and the accumulator of this parity was
+        // read two steps ago
+        if (lane == 0) {
+            bool go = wait_bar(&bars[B_GOPS_READY], s & 1, misc);
+            if (go && s >= 2) go = wait_bar(&bars[B_EXTR_DONE + buf], ((s >> 1) - 1) & 1, misc);
+            if (go) {
+                tc_fence_after();
+                issue_gram(misc->tmem_base, smem_u32(smem), buf, &bars[B_GRAM_DONE + buf]);
+            }
+        }
+        __syncwarp();
         const float br = bnext;
         if (s + 1 < nsteps) bnext = load_beta(s + 1);
         bool ok = wait_bar(&bars[B_GRAM_DONE + buf], (s >> 1) & 1, misc);
@@ -898,6 +914,7 @@ __device__ void a_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc *mis
             KDA_TRACE_EVENT(5, s);
         }
     }
+    if (lane == 0) drain_mmas(&bars[B_DRAIN + 1], misc);
 }
 
 // solver warps.  Warp 1: phase 1 of the block solve (T00, T11) and half 0 of phase 2; warp 3: Aqk
@@ -966,11 +983,12 @@ __device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nstep
 
 // ------------------------------------------------------------------------------------------------
 // asynchronous issuer (lane 0 of warp 0): every TMA load, and the chain's V products, state reads
-// and P / R^T products, each issued as soon as its inputs are ready (the chain's first).  The
+// and P / R^T products, each issued as soon as its inputs are ready.  The q, k, g load goes first
+// in every round: its single stage is the loop prep waits on (prep -> release -> load -> prep),
+// so it is released per warp as soon as the values are in registers and reissued at once.  The
 // barriers are polled without blocking, so that no ready operation waits behind another one;
 // every condition below is checked only after its previous phase has been observed, so a parity
-// test is never ahead.  The next step's q, k, g need no L2 prefetch: prep releases the stage as
-// soon as it holds them in registers.
+// test is never ahead.
 
 __device__ void issuer_role(const Params &p, const CUtensorMap *mq, const CUtensorMap *mk,
                             const CUtensorMap *mg, const CUtensorMap *mv, uint8_t *smem,
@@ -984,6 +1002,20 @@ __device__ void issuer_role(const Params &p, const CUtensorMap *mq, const CUtens
     long long last = clock64();
     while (c1 < nsteps || cp < nsteps) {
         bool prog = false;
+        // q, k, g of step sq (one stage: free once prep holds step sq-1 in registers)
+        if (sq < nsteps && (sq == 0 || mbar_test_wait(&bars[B_QEMPTY], (sq - 1) & 1))) {
+            const int t0 = (int)(start + (long long)sq * C);
+            mbar_arrive_expect_tx(&bars[B_QFULL], QSTAGE_BYTES);
+#pragma unroll
+            for (int x = 0; x < 3; ++x)
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+                    tma_load_3d(smem + OFF_QRING + x * TILE_BYTES + half * 4096, maps[x], &bars[B_QFULL],
+                                half * 64, h, t0);
+            KDA_TRACE_EVENT(19, sq);
+            ++sq;
+            prog = true;
+        }
         // the chain's products first (they are on its critical path), then the loads
         // state reads of step c1: after its V product, the chain's fp16 state copy and prep's
         // operands
@@ -1022,20 +1054,8 @@ __device__ void issuer_role(const Params &p, const CUtensorMap *mq, const CUtens
 #pragma unroll
             for (int half = 0; half < 2; ++half)
                 tma_load_3d(vt + half * 4096, mv, &bars[B_VFULL + sv % kVStages], half * 64, h, t0);
+            KDA_TRACE_EVENT(18, sv);
             ++sv;
-            prog = true;
-        }
-        // q, k, g of step sq (one stage: free once prep holds step sq-1 in registers)
-        if (sq < nsteps && (sq == 0 || mbar_test_wait(&bars[B_QEMPTY], (sq - 1) & 1))) {
-            const int t0 = (int)(start + (long long)sq * C);
-            mbar_arrive_expect_tx(&bars[B_QFULL], QSTAGE_BYTES);
-#pragma unroll
-            for (int x = 0; x < 3; ++x)
-#pragma unroll
-                for (int half = 0; half < 2; ++half)
-                    tma_load_3d(smem + OFF_QRING + x * TILE_BYTES + half * 4096, maps[x], &bars[B_QFULL],
-                                half * 64, h, t0);
-            ++sq;
             prog = true;
         }
         if (prog) {
@@ -1076,7 +1096,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(&bars[B_QFULL + s], 1);        // the expect_tx arrival
-            mbar_init(&bars[B_QEMPTY + s], 1);
+            mbar_init(&bars[B_QEMPTY + s], 8);        // one arrival per prep warp
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&bars[B_VFULL + s], 1);        // the expect_tx arrival
