@@ -81,8 +81,71 @@ def dist_env():
     return rank, world, local
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML (the library nvidia-smi uses) every
+    2 ms on a thread, so that a timed region of a few milliseconds still gets samples.  Read only;
+    unavailable where the driver library is missing."""
+
+    # clock-event reason bits of the NVML API
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, gpu_index: int, period_s: float = 0.002):
+        import ctypes
+        import threading
+
+        self.samples = []
+        self.max_mhz = None
+        self.period = period_s
+        self._stop = threading.Event()
+        self._thread = None
+        self._lib = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            handle = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(handle)) != 0:
+                return
+            self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+            mx = ctypes.c_uint(0)
+            if lib.nvmlDeviceGetMaxClockInfo(handle, ctypes.c_int(1), ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self._lib, self._handle = lib, handle
+        except (OSError, AttributeError):
+            self._lib = None
+
+    def _run(self):
+        import ctypes
+        import time
+
+        mhz, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        while not self._stop.is_set():
+            if self._lib.nvmlDeviceGetClockInfo(self._handle, ctypes.c_int(1), ctypes.byref(mhz)) == 0:
+                r = 0
+                if self._reasons_fn is not None and self._reasons_fn(self._handle, ctypes.byref(rs)) == 0:
+                    r = rs.value
+                self.samples.append((float(mhz.value), r))
+            time.sleep(self.period)
+
+    def start(self):
+        import threading
+
+        if self._lib is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        return self.samples
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples during the timed region."""
+    """Clock / throttle samples during the timed region: nvidia-smi every 100 ms, and NVML every
+    2 ms (the timed region of a default run is shorter than nvidia-smi's start-up)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -92,6 +155,7 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.nvml = NvmlSampler(gpu_index)
 
     def start(self):
         try:
@@ -103,30 +167,43 @@ class ClockSampler:
                 stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+        self.nvml.start()
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
+        fast = self.nvml.stop()
         rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
-        os.unlink(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
-        smax = max((float(r[2]) for r in rows if r[2].replace(".", "").isdigit()), default=None)
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
-        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": smax, "reasons": reasons,
-                "samples": len(rows)}
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        return summarize_clocks(rows, fast, self.nvml.max_mhz)
+
+
+def summarize_clocks(smi_rows, nvml_samples, nvml_max_mhz):
+    """Median SM clock, maximum SM clock and the throttle reasons seen, over nvidia-smi rows
+    (`ClockSampler.FIELDS`, as strings) and NVML samples (MHz, reason bits)."""
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    sm = [float(r[1]) for r in smi_rows if r[1].replace(".", "").isdigit()]
+    sm += [m for m, _ in nvml_samples]
+    maxes = [float(r[2]) for r in smi_rows if r[2].replace(".", "").isdigit()]
+    if nvml_max_mhz is not None:
+        maxes.append(nvml_max_mhz)
+    reasons = {names[i] for r in smi_rows for i in range(4) if r[5 + i].lower() == "active"}
+    reasons |= {n for _, bits in nvml_samples for b, n in NvmlSampler.REASON_BITS.items() if bits & b}
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    sm.sort()
+    return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(maxes) if maxes else None,
+            "reasons": sorted(reasons), "samples": len(sm),
+            "sources": {"nvidia_smi_100ms": len(smi_rows), "nvml_2ms": len(nvml_samples)}}
 
 
 def cuda_time_ms(fn, steps, stream):
