@@ -7,7 +7,9 @@ compiles it with gcc and marshals numpy arrays.
 
 Source of the computation: "Kimi K3 im Detail" (flozi.net), section "Sequenz-Mixing:
 KDA-Zustand und globale MLA" -- per-head recurrent state, channel-wise retention, scalar
-delta-rule write gate, read S_t^T q_t after the token's own update, log-decay floor -5.
+delta-rule write gate, read S_t^T q_t after the token's own update, log-decay floor -5; around
+it, the width-4 short convolution of the projections and the input-dependent output gate (the
+readings taken where the page gives no formula are stated in ``kda_oracle.c``).
 """
 from __future__ import annotations
 
@@ -69,6 +71,11 @@ class Oracle:
         lib.kda_oracle_decode.restype = ctypes.c_int
         lib.kda_oracle_num_ckpts.argtypes = [ip, i64, i64]
         lib.kda_oracle_num_ckpts.restype = i64
+        lib.kda_oracle_premix.argtypes = [dp, dp, dp, dp, dp, dp, dp, ip, i64, i64, i64,
+                                          ctypes.c_double, dp, dp, dp, dp, dp]
+        lib.kda_oracle_premix.restype = ctypes.c_int
+        lib.kda_oracle_output_gate.argtypes = [dp, dp, i64, dp]
+        lib.kda_oracle_output_gate.restype = ctypes.c_int
         self._lib = lib
 
     def prefill(self, q, k, v, g, beta, cu_seqlens=None, init_state=None, ckpt_stride: int = 0,
@@ -126,6 +133,44 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle decode failed with code {rc}")
         return out, S
+
+    def premix(self, xq, xk, xv, a, b, w, hist=None, cu_seqlens=None, eps: float = 1e-6):
+        """Short convolution of the q, k, v projections, q/k normalisation and the gates.
+
+        xq, xk, xv, a: [T, H, d]; b: [T, H]; w: [3, H*d, 4] (taps on x_{t-3} .. x_t);
+        hist: [N, 3, 3, H*d] or None (zeros); cu_seqlens: [N+1] (default [0, T]).
+        Returns (q, k, v, g, beta) in fp64 with the shapes of (xq, xk, xv, a, b)."""
+        xq, xk, xv, a, b, w = (_f64(x) for x in (xq, xk, xv, a, b, w))
+        T, H, d = xq.shape
+        assert xk.shape == xq.shape and xv.shape == xq.shape and a.shape == xq.shape
+        assert b.shape == (T, H) and w.shape == (3, H * d, 4)
+        if cu_seqlens is None:
+            cu_seqlens = [0, T]
+        cu = np.ascontiguousarray(np.asarray(
+            cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens, dtype=np.int64))
+        N = cu.shape[0] - 1
+        assert cu[0] == 0 and cu[-1] == T
+        hs = None
+        if hist is not None:
+            hs = _f64(hist)
+            assert hs.shape == (N, 3, 3, H * d)
+        outs = [np.zeros((T, H, d)) for _ in range(4)] + [np.zeros((T, H))]
+        rc = self._lib.kda_oracle_premix(_ptr(xq), _ptr(xk), _ptr(xv), _ptr(a), _ptr(b), _ptr(w),
+                                         _ptr(hs), cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                         N, H, d, float(eps), *[_ptr(o) for o in outs])
+        if rc != 0:
+            raise ValueError(f"oracle premix failed with code {rc}")
+        return tuple(outs)
+
+    def output_gate(self, o, z):
+        """out = o * sigmoid(z), elementwise, fp64 (o and z of the same shape)."""
+        o, z = _f64(o), _f64(z)
+        assert o.shape == z.shape
+        out = np.zeros(o.shape)
+        rc = self._lib.kda_oracle_output_gate(_ptr(o), _ptr(z), o.size, _ptr(out))
+        if rc != 0:
+            raise ValueError(f"oracle output gate failed with code {rc}")
+        return out
 
 
 _DEFAULT: Optional[Oracle] = None

@@ -31,6 +31,9 @@
  *                           in parallel and passes the recurrent state between chunks.
  * and the one-token update used by decode:
  *   kda_oracle_decode    -- one step of the recurrence on each (sequence, head), in place.
+ * Around the recurrence (readings at each function):
+ *   kda_oracle_premix        -- short convolution of the projections, q/k normalisation, gates;
+ *   kda_oracle_output_gate   -- the input-dependent output gate.
  *
  * Layouts (row-major, last index contiguous):
  *   q, k, g : [T_total, H, d_k]     v, out : [T_total, H, d_v]     beta : [T_total, H]
@@ -352,5 +355,87 @@ int kda_oracle_decode(const double *q, const double *k, const double *v, const d
         }
     }
     free(r);
+    return KDA_ORACLE_OK;
+}
+
+/*
+ * Pre-mixer: what turns the KDA projections into the recurrence's inputs.  The page ("Kimi K3
+ * im Detail", section "Sequenz-Mixing: KDA-Zustand und globale MLA", first paragraph) names a
+ * short convolution of width 4 for the KDA projections and nothing else.  Readings fixed here:
+ *   - the convolution is causal and depthwise (one 4-tap filter per channel of each of the q, k
+ *     and v projections), with no activation after it;
+ *   - inputs before a sequence's first token are its conv history: zeros, or the three rows
+ *     given in hist (the last three projected tokens of a prefix this sequence continues);
+ *   - q and k are L2-normalised per (token, head) after the convolution (the workloads feed the
+ *     recurrence unit-norm q and k):  q = y / max(||y||_2, eps);
+ *   - the decay and write gate come from pre-activations a and b as in the workloads' recipe:
+ *     g = clamp(-softplus(a), -5, 0),  beta = 1 / (1 + exp(-b)).
+ * Per channel c of head h (C = h*d + c) and tensor x in {q, k, v}, with taps w[x][C][0..3]:
+ *     y_t[C] = w[x][C][0] x_{t-3}[C] + w[x][C][1] x_{t-2}[C] + w[x][C][2] x_{t-1}[C] + w[x][C][3] x_t[C]
+ * Layouts: xq, xk, xv, a, q, k, v, g : [T, H, d];  b, beta : [T, H];  w : [3][H*d][4];
+ *          hist : [N][3 (q, k, v)][3 (t-3, t-2, t-1)][H*d] or NULL.
+ */
+static double premix_input(const double *x, const double *hist, int64_t xi, int64_t n,
+                           int64_t start, int64_t t, int64_t HD, int64_t col)
+{
+    if (t >= start) return x[t * HD + col];
+    int64_t back = start - t;                      /* 1, 2 or 3 tokens before the start */
+    if (!hist) return 0.0;
+    return hist[((n * 3 + xi) * 3 + (3 - back)) * HD + col];
+}
+
+int kda_oracle_premix(const double *xq, const double *xk, const double *xv, const double *a,
+                      const double *b, const double *w, const double *hist,
+                      const int64_t *cu_seqlens, int64_t n_seqs, int64_t n_heads, int64_t d,
+                      double eps, double *q, double *k, double *v, double *g, double *beta)
+{
+    if (n_seqs < 0 || n_heads < 1 || d < 1 || !(eps > 0.0)) return KDA_ORACLE_EINVAL;
+    const int64_t HD = n_heads * d;
+    const double *xs[3] = {xq, xk, xv};
+    double *ys[3] = {q, k, v};
+    for (int64_t n = 0; n < n_seqs; ++n) {
+        const int64_t start = cu_seqlens[n], end = cu_seqlens[n + 1];
+        if (end < start) return KDA_ORACLE_EINVAL;
+        for (int64_t t = start; t < end; ++t) {
+            for (int xi = 0; xi < 3; ++xi) {
+                for (int64_t col = 0; col < HD; ++col) {
+                    const double *tap = w + ((int64_t)xi * HD + col) * 4;
+                    double acc = 0.0;
+                    for (int i = 0; i < 4; ++i)
+                        acc += tap[i] * premix_input(xs[xi], hist, xi, n, start, t - 3 + i, HD, col);
+                    ys[xi][t * HD + col] = acc;
+                }
+            }
+            for (int64_t h = 0; h < n_heads; ++h) {
+                for (int xi = 0; xi < 2; ++xi) {           /* q and k: unit L2 norm per head */
+                    double *y = ys[xi] + t * HD + h * d;
+                    double ss = 0.0;
+                    for (int64_t c = 0; c < d; ++c) ss += y[c] * y[c];
+                    double nrm = sqrt(ss);
+                    if (nrm < eps) nrm = eps;
+                    for (int64_t c = 0; c < d; ++c) y[c] /= nrm;
+                }
+                for (int64_t c = 0; c < d; ++c) {
+                    const double x = a[t * HD + h * d + c];
+                    const double softplus = x > 30.0 ? x + log1p(exp(-x)) : log1p(exp(x));
+                    g[t * HD + h * d + c] = clamp_logdecay(-softplus);
+                }
+                beta[t * n_heads + h] = 1.0 / (1.0 + exp(-b[t * n_heads + h]));
+            }
+        }
+    }
+    return KDA_ORACLE_OK;
+}
+
+/*
+ * Output gate: the page (same section, third paragraph) gives KDA an input-dependent output gate
+ * acting on the output of its attention path.  Reading fixed here: an elementwise sigmoid gate,
+ * out = o * 1 / (1 + exp(-z)), with z the gate's pre-activation for the same (token, head,
+ * channel); no normalisation in front of it.
+ */
+int kda_oracle_output_gate(const double *o, const double *z, int64_t n, double *out)
+{
+    if (n < 0) return KDA_ORACLE_EINVAL;
+    for (int64_t i = 0; i < n; ++i) out[i] = o[i] / (1.0 + exp(-z[i]));
     return KDA_ORACLE_OK;
 }

@@ -279,6 +279,129 @@ def pin_tile_decay_floor(orc):
     assert _rel(f1[0], math.exp(-160.0) * c["init_state"][0]) < 1e-12
 
 
+# ---- pre-mixer and output gate ------------------------------------------------------------------
+# Page "Kimi K3 im Detail", section "Sequenz-Mixing: KDA-Zustand und globale MLA": a short
+# convolution of width 4 on the KDA projections (first paragraph) and an input-dependent output
+# gate on the mixer's output (third paragraph).  The readings the oracle takes (causal depthwise
+# taps, zero or given history, q/k L2 normalisation, g = clamp(-softplus(a), -5, 0),
+# beta = sigmoid(b), out = o * sigmoid(z)) are pinned here by a hand-worked case, closed forms and
+# invariants.
+
+
+def premix_case(seed, lengths, H=2, d=8, hist=False):
+    r = _rng(seed)
+    T = sum(lengths)
+    x = [r.standard_normal((T, H, d)) for _ in range(3)]
+    a = r.standard_normal((T, H, d))
+    b = r.standard_normal((T, H))
+    w = r.standard_normal((3, H * d, 4))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    hs = r.standard_normal((len(lengths), 3, 3, H * d)) if hist else None
+    return dict(xq=x[0], xk=x[1], xv=x[2], a=a, b=b, w=w, hist=hs, cu_seqlens=cu)
+
+
+def pin_premix_golden(orc):
+    gv = _read_golden("premix_d2.txt")
+    x = gv["x"].reshape(6, 1, 2)
+    w = np.stack([gv[n].reshape(2, 4) for n in ("wq", "wk", "wv")])
+    q, k, v, g, beta = orc.premix(x, x, x, gv["a"].reshape(6, 1, 2), gv["b"].reshape(6, 1), w,
+                                  cu_seqlens=gv["cu"].astype(np.int64))
+    for name, got in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        assert np.allclose(got.ravel(), gv[name], rtol=0, atol=1e-12), name
+
+
+def pin_premix_current_tap_only(orc):
+    # taps (0, 0, 0, 1): v is the projection itself, q and k its per-head unit vectors
+    c = premix_case(41, [7, 3], H=3)
+    c["w"][:] = [0.0, 0.0, 0.0, 1.0]
+    q, k, v, _, _ = orc.premix(**c)
+    assert np.array_equal(v, c["xv"])
+    assert _rel(q, _unit_rows(c["xq"])) < 1e-14 and _rel(k, _unit_rows(c["xk"])) < 1e-14
+
+
+def pin_premix_shift_resets_per_sequence(orc):
+    # taps (0, 0, 1, 0): v_t = x_(t-1) inside a sequence, zero on every sequence's first token
+    lengths = [5, 1, 7]
+    c = premix_case(42, lengths)
+    c["w"][:] = [0.0, 0.0, 1.0, 0.0]
+    _, _, v, _, _ = orc.premix(**c)
+    cu = c["cu_seqlens"]
+    for n in range(len(lengths)):
+        s, e = cu[n], cu[n + 1]
+        assert np.all(v[s] == 0.0)
+        assert np.array_equal(v[s + 1:e], c["xv"][s:e - 1])
+
+
+def pin_premix_history_is_a_prefix(orc):
+    # history rows h = the three tokens before the sequence: same as prefilling them and dropping
+    # their outputs (also for sequences shorter than the window)
+    for L in (1, 2, 6):
+        c = premix_case(43 + L, [L], hist=True)
+        H, d = c["xq"].shape[1:]
+        longer = {}
+        for i, name in enumerate(("xq", "xk", "xv")):
+            pre = c["hist"][0, i].reshape(3, H, d)
+            longer[name] = np.concatenate([pre, c[name]])
+        a = np.concatenate([np.zeros((3, H, d)), c["a"]])
+        b = np.concatenate([np.zeros((3, H)), c["b"]])
+        ref = orc.premix(longer["xq"], longer["xk"], longer["xv"], a, b, c["w"])
+        got = orc.premix(**c)
+        for x, y in zip(got, ref):
+            assert _rel(x, y[3:]) < 1e-14
+
+
+def pin_premix_varlen_packing(orc):
+    lengths = [4, 9, 2]
+    c = premix_case(47, lengths, hist=True)
+    packed = orc.premix(**c)
+    cu = c["cu_seqlens"]
+    for n in range(len(lengths)):
+        s, e = cu[n], cu[n + 1]
+        one = orc.premix(c["xq"][s:e], c["xk"][s:e], c["xv"][s:e], c["a"][s:e], c["b"][s:e],
+                         c["w"], hist=c["hist"][n:n + 1])
+        for x, y in zip(packed, one):
+            assert np.array_equal(x[s:e], y)
+
+
+def pin_premix_conv_is_linear_and_scale_free(orc):
+    c = premix_case(48, [11])
+    q1, k1, v1, _, _ = orc.premix(**c)
+    c2 = dict(c, xq=3.5 * c["xq"], xk=0.25 * c["xk"], xv=c["xv"] + c["xq"])
+    q2, k2, v2, _, _ = orc.premix(**c2)
+    c3 = dict(c, xv=c["xq"])
+    _, _, v3, _, _ = orc.premix(**c3)
+    assert _rel(q2, q1) < 1e-14 and _rel(k2, k1) < 1e-14            # positive scaling is undone
+    assert _rel(v2, v1 + v3) < 1e-14                                 # the convolution is linear
+    assert np.allclose(np.linalg.norm(q1, axis=-1), 1.0, atol=1e-14)
+
+
+def pin_premix_gates(orc):
+    cs = np.array([0.01, 0.5, 1.0, 2.5, 4.0, 4.999])
+    c = premix_case(49, [len(cs)], H=1, d=1)
+    c["a"] = np.log(np.expm1(cs)).reshape(-1, 1, 1)               # softplus(a) = c exactly
+    c["b"] = np.array([-3.0, -1.0, 0.0, 0.5, 1.0, 3.0]).reshape(-1, 1)
+    _, _, _, g, beta = orc.premix(**c)
+    assert np.allclose(g.ravel(), -cs, rtol=0, atol=1e-13)
+    c_neg = dict(c, b=-c["b"])
+    _, _, _, _, beta_neg = orc.premix(**c_neg)
+    assert np.allclose(beta + beta_neg, 1.0, rtol=0, atol=1e-15)    # sigmoid(-b) = 1 - sigmoid(b)
+    c_big = dict(c, a=np.full_like(c["a"], 5.5))                     # softplus(5.5) > 5: clamped
+    _, _, _, g_big, _ = orc.premix(**c_big)
+    assert np.all(g_big == -5.0)
+
+
+def pin_output_gate(orc):
+    r = _rng(50)
+    o = r.standard_normal((6, 2, 8))
+    assert np.array_equal(orc.output_gate(o, np.zeros_like(o)), o / 2)
+    l3 = np.full_like(o, math.log(3.0))
+    assert np.allclose(orc.output_gate(o, l3), 0.75 * o, rtol=1e-15, atol=0)
+    assert np.allclose(orc.output_gate(o, -l3), 0.25 * o, rtol=1e-15, atol=0)
+    z = r.standard_normal(o.shape)
+    assert np.allclose(orc.output_gate(o, z) + orc.output_gate(o, -z), o, rtol=0, atol=1e-15)
+    assert np.allclose(orc.output_gate(o, np.full_like(o, 50.0)), o, rtol=1e-15, atol=0)
+
+
 PINS = [
     pin_golden_scalar,
     pin_golden_two_channel,
@@ -295,4 +418,12 @@ PINS = [
     pin_varlen_packing,
     pin_decode_is_one_step,
     pin_tile_decay_floor,
+    pin_premix_golden,
+    pin_premix_current_tap_only,
+    pin_premix_shift_resets_per_sequence,
+    pin_premix_history_is_a_prefix,
+    pin_premix_varlen_packing,
+    pin_premix_conv_is_linear_and_scale_free,
+    pin_premix_gates,
+    pin_output_gate,
 ]

@@ -2,8 +2,10 @@
 
 The mistakes are the plausible ones: a flipped sign, a dropped term or gate, a decay on the
 wrong axis, a read before the write, a transposed read, a wrong operand, a missing clamp,
-a causal mask without its diagonal.  Each is a text substitution in a temporary copy of
-``oracle/kda_oracle.c``; the committed oracle is never modified.
+a causal mask without its diagonal; around the recurrence, reversed convolution taps, a
+convolution history that leaks across sequences, a wrong normalisation or gate function.  Each
+is a text substitution in a temporary copy of ``oracle/kda_oracle.c``; the committed oracle is
+never modified.
 """
 import pytest
 
@@ -49,6 +51,22 @@ MUTANTS = {
         "for (int64_t s = 0; s <= r; ++s) {", "for (int64_t s = 0; s < r; ++s) {"),
     "chunk_decay_reference_off_by_one": lambda s: s.replace(
         "exp(GC - G[s * dk + i])", "exp(GC - (s > 0 ? G[(s - 1) * dk + i] : 0.0))"),
+    # pre-mixer and output gate
+    "conv_taps_reversed": lambda s: s.replace(
+        "acc += tap[i] * premix_input(", "acc += tap[3 - i] * premix_input("),
+    "conv_history_not_reset": lambda s: s.replace(
+        "if (t >= start) return x[t * HD + col];", "if (t >= 0) return x[t * HD + col];"),
+    "conv_history_rows_reversed": lambda s: s.replace("* 3 + (3 - back)) * HD", "* 3 + (back - 1)) * HD"),
+    "norm_without_sqrt": lambda s: s.replace("double nrm = sqrt(ss);", "double nrm = ss;"),
+    "norm_over_all_heads": lambda s: s.replace(
+        "for (int64_t c = 0; c < d; ++c) ss += y[c] * y[c];",
+        "for (int64_t c = 0; c < d; ++c) ss += y[c] * y[c] + y[(c + d) % HD] * y[(c + d) % HD];"),
+    "v_normalised_too": lambda s: s.replace("for (int xi = 0; xi < 2; ++xi) {", "for (int xi = 0; xi < 3; ++xi) {"),
+    "softplus_sign": lambda s: s.replace("clamp_logdecay(-softplus)", "clamp_logdecay(softplus)"),
+    "softplus_without_log": lambda s: s.replace(": log1p(exp(x));", ": exp(x);"),
+    "beta_sign": lambda s: s.replace("1.0 / (1.0 + exp(-b[t * n_heads + h]))", "1.0 / (1.0 + exp(b[t * n_heads + h]))"),
+    "output_gate_sign": lambda s: s.replace("o[i] / (1.0 + exp(-z[i]))", "o[i] / (1.0 + exp(z[i]))"),
+    "output_gate_tanh": lambda s: s.replace("o[i] / (1.0 + exp(-z[i]))", "o[i] * tanh(z[i])"),
 }
 
 
