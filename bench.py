@@ -3,8 +3,9 @@
 decode state GB/s (N=256, H=96), against the HBM roofline.
 
 One step = one kda_prefill of the 8192-token, 96-head workload (inputs resident in HBM).
-The decode (256 sequences x 96 heads, 1.6 GB fp32 state updated in place) and a checkpoint
-restore (kda_state_copy of 64 states) are timed in the same run and reported beside it.
+The decode (256 sequences x 96 heads, 1.6 GB fp32 state updated in place), a checkpoint
+restore (kda_state_copy of 64 states), the pre-mixer and the output gate on the same token grid,
+and a prefix-reuse (cache-hit) prefill are timed in the same run and reported beside it.
 
     python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 
@@ -38,6 +39,7 @@ FLOP_PER_TOKEN_HEAD = 6 * D * D + 8 * 16 * D        # 114,688 (chunk C = 16 acco
 BYTES_PER_TOKEN_HEAD = 4 * D * 2 + 2 + D * 4        # q, k, v, g bf16 + beta bf16 + o fp32 = 1,538
 STATE_BYTES = D * D * 4                             # 65,536 per (sequence, head)
 DECODE_BYTES_PER_SEQ_HEAD = 2 * STATE_BYTES + 4 * D * 2 + 2 + D * 4   # 132,610
+PREMIX_BYTES_PER_TOKEN_HEAD = 2 * (4 * D * 2 + 2)    # xq, xk, xv, a, b in; q, k, v, g, beta out: 2,052
 
 
 def set_heads(heads: int) -> None:
@@ -387,6 +389,33 @@ def run_gb300(args):
     del src, dst
     torch.cuda.empty_cache()
 
+    # ---- pre-mixer and output gate on the T = 8192, H = 96 token grid ----------------------
+    px = synth.make_premix_inputs([T1], heads=H, d=D, dtype="bf16", seed=7, device=dev)
+    pout = tuple(torch.empty_like(px["xq"]) for _ in range(4)) + (torch.empty_like(px["b"]),)
+
+    def premix_step():
+        kda.premix(px["xq"], px["xk"], px["xv"], px["a"], px["b"], px["w"], out=pout, stream=stream)
+
+    for _ in range(3):
+        premix_step()
+    _, pm_ms = cuda_time_ms(premix_step, max(5, args.steps), stream)
+    pm_bytes = PREMIX_BYTES_PER_TOKEN_HEAD * T1 * H + 3 * H * D * 4 * 4
+    del px, pout
+    torch.cuda.empty_cache()
+    gx = synth.make_gate_inputs((T1, H, D), "f32", "bf16", seed=8, device=dev)
+    gout = torch.empty(T1, H, D, device=dev, dtype=torch.bfloat16)
+
+    def gate_step():
+        kda.output_gate(gx["o"], gx["z"], out=gout, stream=stream)
+
+    for _ in range(3):
+        gate_step()
+    _, og_ms = cuda_time_ms(gate_step, max(5, args.steps), stream)
+    og_bytes = T1 * H * D * (4 + 2 + 2)
+    assert kda.device_status() == 0
+    del gx, gout
+    torch.cuda.empty_cache()
+
     reuse = prefix_reuse_figure(dev, stream)
     assert kda.device_status() == 0
     torch.cuda.empty_cache()
@@ -424,6 +453,15 @@ def run_gb300(args):
                      "roofline_fraction": max(t_bytes, t_flops) / (per_ms / 1e3)},
         "e2e": {"value": world * T1 / (e2e_per / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_per},
+        "premix": {"workload": f"pre-mixer T={T1} H={H} d={D}: width-4 causal conv of xq/xk/xv, "
+                               "q/k L2 norm, decay and write gates, bf16 in and out",
+                   "GB/s": pm_bytes / (pm_ms / 1e3) / 1e9, "peak": hbm_peak,
+                   "frac": pm_bytes / (pm_ms / 1e3) / 1e9 / hbm_peak, "ms": pm_ms,
+                   "bytes_alg": pm_bytes},
+        "output_gate": {"workload": f"output gate T={T1} H={H} d={D}: fp32 o, bf16 z, bf16 out",
+                        "GB/s": og_bytes / (og_ms / 1e3) / 1e9, "peak": hbm_peak,
+                        "frac": og_bytes / (og_ms / 1e3) / 1e9 / hbm_peak, "ms": og_ms,
+                        "bytes_alg": og_bytes},
         "decode": {"workload": f"decode N={N_DEC} H={H} d={D}, fp32 state in place",
                    "GB/s": dec_gbs, "peak": hbm_peak, "frac": dec_gbs / hbm_peak, "ms": dec_ms,
                    "bytes_alg": dec_bytes},

@@ -142,6 +142,51 @@ int kda_state_copy(float *dst, const int64_t *dst_idx, int64_t n_dst_slots, cons
                    int32_t d_k, int32_t d_v, void *stream);
 
 /*
+ * kda_premix -- the pre-mixer: the recurrence's inputs q, k, v, g, beta from the KDA projections.
+ *
+ * The section cited above gives the KDA projections a short convolution of width 4 (first
+ * paragraph) and no formula; this call implements the plain reading, with q/k normalisation and
+ * the gate functions of the recurrence's input range:
+ *     y_t[c] = w[c][0] x_(t-3)[c] + w[c][1] x_(t-2)[c] + w[c][2] x_(t-1)[c] + w[c][3] x_t[c]
+ *              (causal, depthwise, no activation; per tensor x in {xq, xk, xv})
+ *     q_t = y^q_t / max(||y^q_t||_2, eps),  k_t likewise (per token and head),  v_t = y^v_t
+ *     g_t = clamp(-softplus(a_t), -5, 0),   beta_t = 1 / (1 + exp(-b_t))
+ * Tokens before a sequence's first token are its conv history: zeros, or three rows of `hist`
+ * (the last three projected tokens of the prefix the sequence continues, e.g. after a prefix
+ * restore or for a decode step packed as a one-token sequence).
+ *
+ *   xq, xk, xv, a     [total_tokens, H, d] `dtype` (bf16 or fp32) inputs.
+ *   b                 [total_tokens, H] `dtype`.
+ *   w                 fp32 [3, H*d, 4]: taps of the q, k and v filters, channel-major, tap 3
+ *                     on the current token.
+ *   hist              `dtype` [n_seqs, 3 (q, k, v), 3 (t-3, t-2, t-1), H*d], or NULL = zeros.
+ *   cu_seqlens, n_seqs, total_tokens   as for kda_prefill.
+ *   d                 8, 16, 32, 64, 128 or 256 (a head's channels).  eps > 0.
+ *   q, k, v, g        [total_tokens, H, d] `dtype` outputs; beta [total_tokens, H] `dtype`.
+ *                     They must not alias any input.
+ * Arithmetic is fp32; bf16 outputs are rounded to nearest.  Errors: KDA_ERR_INVALID_ARG,
+ * KDA_ERR_UNSUPPORTED_SHAPE (d), KDA_ERR_MISALIGNED, KDA_ERR_CUDA.
+ */
+int kda_premix(const void *xq, const void *xk, const void *xv, const void *a, const void *b,
+               const float *w, const void *hist, const int32_t *cu_seqlens, int32_t n_seqs,
+               int64_t total_tokens, int32_t n_heads, int32_t d, float eps, int32_t dtype, void *q,
+               void *k, void *v, void *g, void *beta, void *stream);
+
+/*
+ * kda_output_gate -- the input-dependent output gate on the recurrence's output.
+ *
+ * The section cited above gives KDA an input-dependent output gate acting on the output of its
+ * attention path (third paragraph) and no formula; this call implements the plain reading, an
+ * elementwise sigmoid gate:  out[i] = o[i] / (1 + exp(-z[i])),  i in [0, n).
+ *
+ *   o, z, out         n elements each, dtypes o_dtype, z_dtype, out_dtype (kda_dtype).  `out`
+ *                     may be `o` itself when out_dtype == o_dtype (in place); it must not be z.
+ * Arithmetic is fp32.  Errors: KDA_ERR_INVALID_ARG, KDA_ERR_MISALIGNED, KDA_ERR_CUDA.
+ */
+int kda_output_gate(const void *o, int32_t o_dtype, const void *z, int32_t z_dtype, void *out,
+                    int32_t out_dtype, int64_t n, void *stream);
+
+/*
  * kda_device_status -- synchronize `stream`, then read and clear the current device's sticky
  * error word (KDA_OK if no device-side error was recorded since the last read).  *status
  * receives the recorded kda_status.  Returns KDA_OK, or KDA_ERR_CUDA if the read failed.

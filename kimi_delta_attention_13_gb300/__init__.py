@@ -1,6 +1,7 @@
 """GB300-native Kimi Delta Attention (KDA): thin torch binding over the C ABI of libkda_gb300.
 
-The three calls (and the cross-check path) mirror include/kda.h.  This module only checks
+The three calls of the path (and the cross-check path), and the pre-mixer and output gate around
+it, mirror include/kda.h.  This module only checks
 tensor properties, allocates outputs with torch when the caller does not pass them, and
 hands raw device pointers plus the current CUDA stream to the library; every step of the
 computation runs in the library's CUDA kernels.  There is no CPU fallback: without the
@@ -20,7 +21,7 @@ from . import _lib
 from ._lib import KDAError
 
 __all__ = ["prefill", "prefill_recurrent", "decode", "state_copy", "device_status", "prefill_path",
-           "num_checkpoints", "KDAError", "load", "diag_device_timeout"]
+           "num_checkpoints", "KDAError", "load", "diag_device_timeout", "premix", "output_gate"]
 
 _DTYPES = {torch.bfloat16: _lib.KDA_BF16, torch.float32: _lib.KDA_F32}
 
@@ -154,6 +155,66 @@ def decode(q, k, v, g, beta, state, *, out=None, stream=None, out_dtype=torch.fl
     rc = lib.kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(out),
                         N, H, dk, dv, _DTYPES[dtype], _DTYPES[out.dtype], _stream(dev, stream))
     _lib.check(rc, "kda_decode")
+    return out
+
+
+def premix(xq, xk, xv, a, b, w, cu_seqlens=None, hist=None, *, eps: float = 1e-6, out=None,
+           stream=None):
+    """Pre-mixer (kda_premix): the recurrence's inputs from the KDA projections.
+
+    xq, xk, xv, a: [T, H, d]; b: [T, H] (bf16 or fp32, one dtype); w: fp32 [3, H*d, 4], the
+    width-4 causal taps of the q, k, v filters (tap 3 on the current token); cu_seqlens: int32
+    [N+1] or None; hist: [N, 3, 3, H*d] conv history (the three projected tokens before each
+    sequence, per q/k/v) or None for zeros.  Returns (q, k, v, g, beta): q and k L2-normalised
+    per (token, head), g = clamp(-softplus(a), -5, 0), beta = sigmoid(b); `out` may pass those
+    five tensors preallocated."""
+    lib = _lib.load()
+    dev, dtype = xq.device, xq.dtype
+    if dtype not in _DTYPES:
+        raise ValueError("premix inputs must be bfloat16 or float32")
+    T, H, d = xq.shape
+    for t, name, shp in ((xq, "xq", (T, H, d)), (xk, "xk", (T, H, d)), (xv, "xv", (T, H, d)),
+                         (a, "a", (T, H, d)), (b, "b", (T, H))):
+        _require(t, name, dev, dtype, shp)
+    _require(w, "w", dev, torch.float32, (3, H * d, 4))
+    if cu_seqlens is None:
+        n = 1
+    else:
+        _require(cu_seqlens, "cu_seqlens", dev, torch.int32)
+        n = cu_seqlens.numel() - 1
+    if hist is not None:
+        _require(hist, "hist", dev, dtype, (n, 3, 3, H * d))
+    if out is None:
+        out = tuple(torch.empty_like(xq) for _ in range(4)) + (torch.empty_like(b),)
+    else:
+        for t, name, shp in zip(out, ("q", "k", "v", "g", "beta"), [(T, H, d)] * 4 + [(T, H)]):
+            _require(t, name, dev, dtype, shp)
+    rc = lib.kda_premix(_ptr(xq), _ptr(xk), _ptr(xv), _ptr(a), _ptr(b), _ptr(w), _ptr(hist),
+                        _ptr(cu_seqlens), n, T, H, d, float(eps), _DTYPES[dtype],
+                        *[_ptr(t) for t in out], _stream(dev, stream))
+    _lib.check(rc, "kda_premix")
+    return tuple(out)
+
+
+def output_gate(o, z, *, out=None, out_dtype=None, stream=None):
+    """Input-dependent output gate (kda_output_gate): out = o * sigmoid(z), elementwise.
+    o and z: CUDA tensors of one shape (bf16 or fp32 each).  out: a tensor to fill (may be o
+    itself for an in-place gate), else a new one of `out_dtype` (default o.dtype)."""
+    lib = _lib.load()
+    dev = o.device
+    _require(o, "o", dev)
+    _require(z, "z", dev, shape=o.shape)
+    if o.dtype not in _DTYPES or z.dtype not in _DTYPES:
+        raise ValueError("o and z must be bfloat16 or float32")
+    if out is None:
+        out = torch.empty(o.shape, device=dev, dtype=out_dtype or o.dtype)
+    else:
+        _require(out, "out", dev, shape=o.shape)
+        if out.dtype not in _DTYPES:
+            raise ValueError("out must be bfloat16 or float32")
+    rc = lib.kda_output_gate(_ptr(o), _DTYPES[o.dtype], _ptr(z), _DTYPES[z.dtype], _ptr(out),
+                             _DTYPES[out.dtype], o.numel(), _stream(dev, stream))
+    _lib.check(rc, "kda_output_gate")
     return out
 
 

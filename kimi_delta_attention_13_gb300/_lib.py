@@ -32,6 +32,9 @@ SIGNATURES = {
     "kda_state_copy": (ctypes.c_int, [_vp, _vp, _i64, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp]),
     "kda_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _vp]),
     "kda_diag_device_timeout": (ctypes.c_int, [_i64, _vp]),
+    "kda_premix": (ctypes.c_int, [_vp] * 7 + [_vp, _i32, _i64, _i32, _i32, ctypes.c_float, _i32]
+                   + [_vp] * 5 + [_vp]),
+    "kda_output_gate": (ctypes.c_int, [_vp, _i32, _vp, _i32, _vp, _i32, _i64, _vp]),
 }
 
 _LIB = None

@@ -136,6 +136,46 @@ int kda_state_copy(float *dst, const int64_t *dst_idx, int64_t n_dst_slots, cons
                              (cudaStream_t)stream);
 }
 
+int kda_premix(const void *xq, const void *xk, const void *xv, const void *a, const void *b,
+               const float *w, const void *hist, const int32_t *cu_seqlens, int32_t n_seqs,
+               int64_t total_tokens, int32_t n_heads, int32_t d, float eps, int32_t dtype, void *q,
+               void *k, void *v, void *g, void *beta, void *stream)
+{
+    if (n_seqs < 0 || total_tokens < 0 || n_heads < 1 || d < 1 || bad_dtype(dtype) || !(eps > 0.f))
+        return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && n_seqs == 0) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;   // cu_seqlens are int32
+    if (!cu_seqlens && n_seqs > 1) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!xq || !xk || !xv || !a || !b || !w || !q || !k || !v || !g || !beta))
+        return KDA_ERR_INVALID_ARG;
+    if (d > 256 || (d & (d - 1)) != 0 || d < 8) return KDA_ERR_UNSUPPORTED_SHAPE;
+    const void *ptrs[] = {xq, xk, xv, a, b, w, hist, q, k, v, g, beta};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return KDA_ERR_MISALIGNED;
+    const void *ins[] = {xq, xk, xv, a, b, hist};
+    const void *outs[] = {q, k, v, g, beta};
+    for (const void *o : outs)
+        for (const void *i : ins)
+            if (o && o == i) return KDA_ERR_INVALID_ARG;
+    return launch_premix(xq, xk, xv, a, b, w, hist, cu_seqlens, n_seqs, total_tokens, n_heads, d,
+                         eps, dtype, q, k, v, g, beta, (cudaStream_t)stream);
+}
+
+int kda_output_gate(const void *o, int32_t o_dtype, const void *z, int32_t z_dtype, void *out,
+                    int32_t out_dtype, int64_t n, void *stream)
+{
+    if (n < 0 || bad_dtype(o_dtype) || bad_dtype(z_dtype) || bad_dtype(out_dtype))
+        return KDA_ERR_INVALID_ARG;
+    if (n > 0 && (!o || !z || !out)) return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {o, z, out};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+    // in place over o is fine (same element type: each element is read before it is written)
+    if (out && ((out == o && out_dtype != o_dtype) || out == z)) return KDA_ERR_INVALID_ARG;
+    return launch_output_gate(o, o_dtype, z, z_dtype, out, out_dtype, n, (cudaStream_t)stream);
+}
+
 int kda_diag_device_timeout(int64_t timeout_cycles, void *stream)
 {
     if (timeout_cycles < 1 || timeout_cycles > 4000000000LL) return KDA_ERR_INVALID_ARG;

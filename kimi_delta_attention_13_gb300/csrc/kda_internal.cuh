@@ -41,6 +41,12 @@ int launch_prefill_recurrent(const void *q, const void *k, const void *v, const 
                              int64_t total_tokens, int n_heads, int d_k, int d_v, int dtype,
                              int out_dtype, const float *init_state, void *out, float *final_state,
                              int ckpt_stride, float *ckpts, cudaStream_t stream);
+int launch_premix(const void *xq, const void *xk, const void *xv, const void *a, const void *b,
+                  const float *w, const void *hist, const int32_t *cu_seqlens, int n_seqs,
+                  long long total_tokens, int n_heads, int d, float eps, int dtype, void *q,
+                  void *k, void *v, void *g, void *beta, cudaStream_t stream);
+int launch_output_gate(const void *o, int o_dtype, const void *z, int z_dtype, void *out,
+                       int out_dtype, long long n, cudaStream_t stream);
 int launch_prefill_tc(const void *q, const void *k, const void *v, const void *g,
                       const void *beta, const int32_t *cu_seqlens, int n_seqs,
                       int64_t total_tokens, int n_heads, int out_dtype, const float *init_state,

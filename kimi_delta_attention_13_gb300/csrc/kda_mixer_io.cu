@@ -1,0 +1,331 @@
+// kda_mixer_io.cu -- the steps just around the KDA recurrence: the pre-mixer, which turns the q,
+// k, v projections and the gate pre-activations into the recurrence's inputs, and the output gate.
+//
+// Page "Kimi K3 im Detail", section "Sequenz-Mixing: KDA-Zustand und globale MLA": a short
+// convolution of width 4 for the KDA projections (first paragraph) and an input-dependent output
+// gate acting on the KDA path's output (third paragraph).  The page gives neither formula; the
+// readings implemented here are:
+//   y_t = w0 x_(t-3) + w1 x_(t-2) + w2 x_(t-1) + w3 x_t     causal depthwise, per channel, no
+//         activation; tokens before a sequence's start are its conv history (zeros or 3 rows)
+//   q = y_q / max(||y_q||_2, eps),  k = y_k / max(||y_k||_2, eps)   per (token, head);  v = y_v
+//   g = clamp(-softplus(a), -5, 0),  beta = 1 / (1 + exp(-b))
+//   out = o / (1 + exp(-z))
+//
+// Both kernels stream HBM once (the roofline is bytes / bandwidth): 16-byte vector loads and
+// stores of 8 channels per thread, fp32 arithmetic.  The pre-mixer walks a 32-token chunk per
+// thread with a 3-token register window and keeps the next 4 tokens' loads in flight; the chunk's
+// first tokens read their 3-token halo, which the neighbouring chunk (scheduled next to it: token
+// chunks are the fastest grid dimension) has just brought into L2.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kMixThreads = 128;   // 8 channels per thread: 1024 channels per block
+constexpr int kMixTokens = 32;     // tokens per pre-mixer block
+constexpr int kMixDepth = 4;       // tokens each pre-mixer thread keeps in flight
+
+// 8 consecutive elements <-> 8 floats (16-byte bf16 vector, or two 16-byte fp32 vectors)
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8])
+{
+    const uint4 r = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void load8(const float *p, float (&v)[8])
+{
+    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16 *p, const float (&v)[8])
+{
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ void store8(float *p, const float (&v)[8])
+{
+    *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4 *>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// 8 elements as loaded (packed bf16 stays packed until used): the prefetch ring's entries
+template <typename T>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+    uint4 u;
+    __device__ __forceinline__ void load(const __nv_bfloat16 *p) { u = *reinterpret_cast<const uint4 *>(p); }
+    __device__ __forceinline__ void unpack(float (&v)[8]) const
+    {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+template <>
+struct Raw8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const float *p)
+    {
+        a = *reinterpret_cast<const float4 *>(p);
+        b = *reinterpret_cast<const float4 *>(p + 4);
+    }
+    __device__ __forceinline__ void unpack(float (&v)[8]) const
+    {
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+};
+
+__device__ __forceinline__ float sigmoid(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// clamp(-softplus(a), -5, 0): softplus(a) >= 5 for a >= 4.9933, so larger a need no evaluation
+__device__ __forceinline__ float decay_gate(float a)
+{
+    return a >= 5.0f ? -5.0f : fmaxf(-log1pf(expf(a)), -5.0f);
+}
+
+struct PremixArgs {
+    const void *x[3];      // xq, xk, xv  [T, H, d]
+    const void *a;         // [T, H, d]
+    const void *b;         // [T, H]
+    const float *w;        // [3, H*d, 4]
+    const void *hist;      // [N, 3, 3, H*d] or null
+    const int32_t *cu;     // [N+1] or null (one sequence)
+    int n_seqs;
+    long long T;
+    int H, d;
+    float eps;
+    void *y[3];            // q, k, v  [T, H, d]
+    void *g;               // [T, H, d]
+    void *beta;            // [T, H]
+};
+
+// blockIdx.x: 32-token chunk, blockIdx.y: 1024-channel block; kV = false: blockIdx.z = 0 (q) or
+// 1 (k), normalised; kV = true: v with the gates.  Thread: 8 channels [col, col + 8) of one head.
+template <typename T, bool kV>
+__global__ void __launch_bounds__(kMixThreads) premix_kernel(const PremixArgs p)
+{
+    const int xi = kV ? 2 : blockIdx.z;
+    const long long HD = (long long)p.H * p.d;
+    const long long col = 8ll * ((long long)blockIdx.y * kMixThreads + threadIdx.x);
+    const bool active = col < HD;
+    const long long t0 = (long long)blockIdx.x * kMixTokens;
+    const long long t1 = min(t0 + kMixTokens, p.T);
+    const T *x = static_cast<const T *>(p.x[xi]);
+    T *y = static_cast<T *>(p.y[xi]);
+
+    // the sequence holding t0: the last n with cu[n] <= t0 (then cu[n+1] > t0)
+    int n = 0;
+    long long start = 0, next = p.T;
+    if (p.cu) {
+        int lo = 0, hi = p.n_seqs - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.cu[mid] <= t0) lo = mid; else hi = mid - 1;
+        }
+        n = lo;
+        start = p.cu[n];
+        next = p.cu[n + 1];
+    }
+
+    float wt[8][4];
+    if (active) {
+        const float4 *wp = reinterpret_cast<const float4 *>(p.w + ((long long)xi * HD + col) * 4);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float4 q4 = wp[c];
+            wt[c][0] = q4.x; wt[c][1] = q4.y; wt[c][2] = q4.z; wt[c][3] = q4.w;
+        }
+    }
+    // history row r (0, 1, 2 = the 3rd, 2nd, 1st token before the start) of sequence `seq`
+    auto hist_row = [&](int seq, int r, float (&v)[8]) {
+        if (active && p.hist) {
+            load8(static_cast<const T *>(p.hist) + (((long long)seq * 3 + xi) * 3 + r) * HD + col, v);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) v[c] = 0.f;
+        }
+    };
+    auto input = [&](long long t, float (&v)[8]) {   // t in [start - 3, t0)
+        if (t >= start) {
+            if (active) load8(x + t * HD + col, v);
+        } else {
+            hist_row(n, 3 - (int)(start - t), v);
+        }
+    };
+    float w3[8] = {}, w2[8] = {}, w1[8] = {};
+    input(t0 - 3, w3);
+    input(t0 - 2, w2);
+    input(t0 - 1, w1);
+    // the next kMixDepth tokens' x (and a) are in flight while one token is computed
+    const T *av_base = static_cast<const T *>(p.a);
+    Raw8<T> ring[kMixDepth], aring[kMixDepth];
+#pragma unroll
+    for (int j = 0; j < kMixDepth; ++j) {
+        const long long t = t0 + j;
+        if (active && t < t1) {
+            ring[j].load(x + t * HD + col);
+            if (kV) aring[j].load(av_base + t * HD + col);
+        }
+    }
+
+    const int group = p.d >> 3;   // threads per head (a power of two <= 32)
+    for (long long tb = t0; tb < t1; tb += kMixDepth) {
+#pragma unroll
+        for (int j = 0; j < kMixDepth; ++j) {
+            const long long t = tb + j;
+            if (t >= t1) break;
+            float cur[8], av[8];
+            ring[j].unpack(cur);
+            if (kV) aring[j].unpack(av);
+            if (active && t + kMixDepth < t1) {
+                ring[j].load(x + (t + kMixDepth) * HD + col);
+                if (kV) aring[j].load(av_base + (t + kMixDepth) * HD + col);
+            }
+            if (t == next) {
+                // a new sequence starts at t: its window is its own history
+                do {
+                    ++n;
+                    start = p.cu[n];
+                    next = p.cu[n + 1];
+                } while (next <= t);
+                hist_row(n, 0, w3);
+                hist_row(n, 1, w2);
+                hist_row(n, 2, w1);
+            }
+            float o[8];
+            float ss = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                o[c] = fmaf(wt[c][3], cur[c], fmaf(wt[c][2], w1[c], fmaf(wt[c][1], w2[c], wt[c][0] * w3[c])));
+                ss = fmaf(o[c], o[c], ss);
+                w3[c] = w2[c];
+                w2[c] = w1[c];
+                w1[c] = cur[c];
+            }
+            if (!kV) {
+                // per-head sum of squares over the head's `group` threads (aligned lane groups)
+                for (int m = group >> 1; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+                const float inv = 1.0f / fmaxf(sqrtf(ss), p.eps);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) o[c] *= inv;
+            }
+            if (!active) continue;
+            store8(y + t * HD + col, o);
+            if (kV) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) av[c] = decay_gate(av[c]);
+                store8(static_cast<T *>(p.g) + t * HD + col, av);
+                if (col % p.d == 0) {
+                    const long long hb = t * p.H + col / p.d;
+                    store_as(static_cast<T *>(p.beta) + hb, sigmoid(to_f32(static_cast<const T *>(p.b)[hb])));
+                }
+            }
+        }
+    }
+}
+
+// out = o * sigmoid(z) over n elements; 8 per thread and step of a grid-stride loop
+template <typename TO, typename TZ, typename TY>
+__global__ void __launch_bounds__(256) output_gate_kernel(const TO *o, const TZ *z, TY *out, long long n)
+{
+    const long long n8 = n >> 3;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+        float ov[8], zv[8];
+        load8(o + 8 * i, ov);
+        load8(z + 8 * i, zv);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) ov[c] *= sigmoid(zv[c]);
+        store8(out + 8 * i, ov);
+    }
+    if (blockIdx.x == 0 && threadIdx.x < (n & 7)) {
+        const long long i = 8 * n8 + threadIdx.x;
+        store_as(out + i, to_f32(o[i]) * sigmoid(to_f32(z[i])));
+    }
+}
+
+int sm_count()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+    return sms;
+}
+
+template <typename TO, typename TZ>
+int launch_gate_out(const void *o, const void *z, void *out, int out_dtype, long long n,
+                    dim3 grid, cudaStream_t stream)
+{
+    if (out_dtype == KDA_BF16)
+        output_gate_kernel<TO, TZ, __nv_bfloat16><<<grid, 256, 0, stream>>>(
+            static_cast<const TO *>(o), static_cast<const TZ *>(z), static_cast<__nv_bfloat16 *>(out), n);
+    else
+        output_gate_kernel<TO, TZ, float><<<grid, 256, 0, stream>>>(
+            static_cast<const TO *>(o), static_cast<const TZ *>(z), static_cast<float *>(out), n);
+    return KDA_OK;
+}
+
+}  // namespace
+
+int launch_premix(const void *xq, const void *xk, const void *xv, const void *a, const void *b,
+                  const float *w, const void *hist, const int32_t *cu_seqlens, int n_seqs,
+                  long long total_tokens, int n_heads, int d, float eps, int dtype, void *q,
+                  void *k, void *v, void *g, void *beta, cudaStream_t stream)
+{
+    if (total_tokens == 0) return KDA_OK;
+    PremixArgs p;
+    p.x[0] = xq; p.x[1] = xk; p.x[2] = xv;
+    p.a = a; p.b = b; p.w = w; p.hist = hist;
+    p.cu = n_seqs == 1 ? nullptr : cu_seqlens;
+    p.n_seqs = n_seqs;
+    p.T = total_tokens;
+    p.H = n_heads; p.d = d; p.eps = eps;
+    p.y[0] = q; p.y[1] = k; p.y[2] = v;
+    p.g = g; p.beta = beta;
+    const long long HD = (long long)n_heads * d;
+    const dim3 grid_qk((unsigned)((total_tokens + kMixTokens - 1) / kMixTokens),
+                       (unsigned)((HD / 8 + kMixThreads - 1) / kMixThreads), 2);
+    const dim3 grid_v(grid_qk.x, grid_qk.y, 1);
+    if (dtype == KDA_BF16) {
+        premix_kernel<__nv_bfloat16, false><<<grid_qk, kMixThreads, 0, stream>>>(p);
+        premix_kernel<__nv_bfloat16, true><<<grid_v, kMixThreads, 0, stream>>>(p);
+    } else {
+        premix_kernel<float, false><<<grid_qk, kMixThreads, 0, stream>>>(p);
+        premix_kernel<float, true><<<grid_v, kMixThreads, 0, stream>>>(p);
+    }
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int launch_output_gate(const void *o, int o_dtype, const void *z, int z_dtype, void *out,
+                       int out_dtype, long long n, cudaStream_t stream)
+{
+    if (n == 0) return KDA_OK;
+    // enough 256-thread blocks for 8 resident per SM, fewer when n is small
+    const long long want = (n / 8 + 255) / 256;
+    const long long cap = 8ll * sm_count();
+    const dim3 grid((unsigned)(want < 1 ? 1 : (want < cap ? want : cap)));
+    if (o_dtype == KDA_BF16 && z_dtype == KDA_BF16)
+        launch_gate_out<__nv_bfloat16, __nv_bfloat16>(o, z, out, out_dtype, n, grid, stream);
+    else if (o_dtype == KDA_BF16)
+        launch_gate_out<__nv_bfloat16, float>(o, z, out, out_dtype, n, grid, stream);
+    else if (z_dtype == KDA_BF16)
+        launch_gate_out<float, __nv_bfloat16>(o, z, out, out_dtype, n, grid, stream);
+    else
+        launch_gate_out<float, float>(o, z, out, out_dtype, n, grid, stream);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace kda

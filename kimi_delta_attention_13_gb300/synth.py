@@ -123,3 +123,36 @@ def make_workload_inputs(w: Workload, device="cpu", decay_scale: float = 1.0) ->
         return make_decode_inputs(w.n_seqs, w.heads, w.d_k, w.d_v, w.dtype, w.seed, device)
     return make_inputs(w.lengths, w.heads, w.d_k, w.d_v, w.dtype, w.seed, device, w.init_state,
                        decay_scale)
+
+
+def make_premix_inputs(lengths: List[int], heads: int = HEADS, d: int = HEAD_DIM,
+                       dtype: str = "bf16", seed: int = 0, device="cpu", hist: bool = False) -> dict:
+    """Inputs of the pre-mixer: projection rows xq, xk, xv and the decay pre-activation a, all
+    N(0,1) [T,H,d]; the write-gate pre-activation b ~ N(0,1) [T,H]; taps w ~ 0.5 N(0,1) fp32
+    [3, H*d, 4]; conv history ~ N(0,1) [N,3,3,H*d] (or None); cu_seqlens int32 [N+1].
+    Draw order from one generator: xq, xk, xv, a, b, w, hist.  (The model's projections and
+    filter weights are trained; these stand-ins only give the kernels the same shapes.)"""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    T, N = int(sum(lengths)), len(lengths)
+    dt = torch_dtype(dtype)
+    kw = dict(generator=gen, device=device, dtype=torch.float32)
+    xq, xk, xv, a = (torch.randn(T, heads, d, **kw).to(dt) for _ in range(4))
+    b = torch.randn(T, heads, **kw).to(dt)
+    w = 0.5 * torch.randn(3, heads * d, 4, **kw)
+    hs = torch.randn(N, 3, 3, heads * d, **kw).to(dt) if hist else None
+    cu = torch.zeros(N + 1, dtype=torch.int64)
+    if N:
+        cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0)
+    return dict(xq=xq, xk=xk, xv=xv, a=a, b=b, w=w, hist=hs,
+                cu_seqlens=cu.to(device=device, dtype=torch.int32), lengths=list(lengths))
+
+
+def make_gate_inputs(shape, o_dtype: str = "f32", z_dtype: str = "bf16", seed: int = 0,
+                     device="cpu") -> dict:
+    """Output-gate inputs: o ~ N(0,1) (the mixer's output) and its gate pre-activation
+    z ~ N(0,1), both of `shape`.  Draw order: o, z."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    kw = dict(generator=gen, device=device, dtype=torch.float32)
+    o = torch.randn(*shape, **kw).to(torch_dtype(o_dtype))
+    z = torch.randn(*shape, **kw).to(torch_dtype(z_dtype))
+    return dict(o=o, z=z)

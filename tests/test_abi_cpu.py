@@ -122,3 +122,36 @@ def test_binding_refuses_cpu_tensors():
 def test_diag_timeout_rejects_out_of_range_cycles(lib):
     assert lib.kda_diag_device_timeout(0, None) == 1              # KDA_ERR_INVALID_ARG
     assert lib.kda_diag_device_timeout(4_000_000_001, None) == 1
+
+
+def _premix(lib, **over):
+    args = dict(xq=A, xk=A + 16, xv=A + 32, a=A + 48, b=A + 64, w=A + 80, hist=None, cu=None, n=1,
+                T=16, H=2, d=128, eps=1e-6, dtype=0, q=A + 4096, k=A + 4112, v=A + 4128,
+                g=A + 4144, beta=A + 4160, stream=None)
+    args.update(over)
+    return lib.kda_premix(*[args[k] for k in ("xq", "xk", "xv", "a", "b", "w", "hist", "cu", "n",
+                                               "T", "H", "d", "eps", "dtype", "q", "k", "v", "g",
+                                               "beta", "stream")])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(d=24), 2), (dict(d=4), 2), (dict(d=512), 2),   # d: a power of two in 8 .. 256
+    (dict(eps=0.0), 1), (dict(eps=-1.0), 1), (dict(dtype=2), 1), (dict(H=0), 1), (dict(T=-1), 1),
+    (dict(w=None), 1), (dict(beta=None), 1),
+    (dict(n=2), 1),                                      # two sequences need cu_seqlens
+    (dict(n=0), 1),                                      # tokens without a sequence
+    (dict(q=A), 1), (dict(g=A + 48), 1), (dict(v=A + 64), 1),   # outputs alias inputs
+    (dict(xq=A + 8), 3), (dict(hist=A + 4), 3), (dict(beta=A + 4162), 3), (dict(cu=A + 2), 3),
+])
+def test_premix_rejects(lib, over, code):
+    assert _premix(lib, **over) == code
+
+
+def test_output_gate_rejects(lib):
+    f = lib.kda_output_gate
+    assert f(A, 1, A + 16, 0, A + 32, 0, -1, None) == 1           # negative count
+    assert f(A, 3, A + 16, 0, A + 32, 0, 8, None) == 1            # bad dtype
+    assert f(A, 1, A + 16, 0, A + 16, 0, 8, None) == 1            # out aliases z
+    assert f(A, 1, A + 16, 0, A, 0, 8, None) == 1                 # in place with another dtype
+    assert f(None, 1, A + 16, 0, A + 32, 0, 8, None) == 1
+    assert f(A + 4, 1, A + 16, 0, A + 32, 0, 8, None) == 3
