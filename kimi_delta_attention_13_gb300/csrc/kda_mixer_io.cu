@@ -13,9 +13,9 @@
 //
 // Both kernels stream HBM once (the roofline is bytes / bandwidth): 16-byte vector loads and
 // stores of 8 channels per thread, fp32 arithmetic.  The pre-mixer walks a 32-token chunk per
-// thread with a 3-token register window and keeps the next 4 tokens' loads in flight; the chunk's
-// first tokens read their 3-token halo, which the neighbouring chunk (scheduled next to it: token
-// chunks are the fastest grid dimension) has just brought into L2.
+// thread with a 3-token register window and keeps the next 8 (bf16) or 4 (fp32) tokens' loads in
+// flight; the chunk's first tokens read their 3-token halo, which the neighbouring chunk
+// (scheduled next to it: token chunks are the fastest grid dimension) has just brought into L2.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -23,7 +23,9 @@ namespace {
 
 constexpr int kMixThreads = 128;   // 8 channels per thread: 1024 channels per block
 constexpr int kMixTokens = 32;     // tokens per pre-mixer block
-constexpr int kMixDepth = 4;       // tokens each pre-mixer thread keeps in flight
+// tokens each pre-mixer thread keeps in flight: 8 of bf16 (16 B each), 4 of fp32 (32 B each)
+template <typename T>
+constexpr int mix_depth() { return sizeof(T) == 2 ? 8 : 4; }
 
 // 8 consecutive elements <-> 8 floats (16-byte bf16 vector, or two 16-byte fp32 vectors)
 __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8])
@@ -88,12 +90,16 @@ struct Raw8<float> {
     }
 };
 
-__device__ __forceinline__ float sigmoid(float x) { return 1.0f / (1.0f + expf(-x)); }
+// The gates use the hardware exponential and logarithm (CUDA's __expf / __logf intrinsics):
+// a few ulps of relative error (at worst 2^-21 absolute for the logarithm near 1), far inside a
+// bf16 rounding and inside the fp32 outputs' bound; libm-accurate expf / log1pf per element made
+// the pre-mixer issue-bound.
+__device__ __forceinline__ float sigmoid(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 // clamp(-softplus(a), -5, 0): softplus(a) >= 5 for a >= 4.9933, so larger a need no evaluation
 __device__ __forceinline__ float decay_gate(float a)
 {
-    return a >= 5.0f ? -5.0f : fmaxf(-log1pf(expf(a)), -5.0f);
+    return a >= 5.0f ? -5.0f : fmaxf(-__logf(1.0f + __expf(a)), -5.0f);
 }
 
 struct PremixArgs {
@@ -117,6 +123,7 @@ struct PremixArgs {
 template <typename T, bool kV>
 __global__ void __launch_bounds__(kMixThreads) premix_kernel(const PremixArgs p)
 {
+    constexpr int kMixDepth = mix_depth<T>();
     const int xi = kV ? 2 : blockIdx.z;
     const long long HD = (long long)p.H * p.d;
     const long long col = 8ll * ((long long)blockIdx.y * kMixThreads + threadIdx.x);
@@ -218,7 +225,7 @@ __global__ void __launch_bounds__(kMixThreads) premix_kernel(const PremixArgs p)
             if (!kV) {
                 // per-head sum of squares over the head's `group` threads (aligned lane groups)
                 for (int m = group >> 1; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-                const float inv = 1.0f / fmaxf(sqrtf(ss), p.eps);
+                const float inv = rsqrtf(fmaxf(ss, p.eps * p.eps));   // 1 / max(||y||, eps)
 #pragma unroll
                 for (int c = 0; c < 8; ++c) o[c] *= inv;
             }
