@@ -59,21 +59,19 @@ __device__ __forceinline__ void store8(float *p, const float (&v)[8])
     *reinterpret_cast<float4 *>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
 }
 
-// 8 elements as loaded (packed bf16 stays packed until used): the prefetch ring's entries
+// 8 elements as loaded (packed bf16 stays packed until used): the prefetch ring's entries,
+// unpacked as 4 channel pairs
 template <typename T>
 struct Raw8;
 template <>
 struct Raw8<__nv_bfloat16> {
     uint4 u;
     __device__ __forceinline__ void load(const __nv_bfloat16 *p) { u = *reinterpret_cast<const uint4 *>(p); }
-    __device__ __forceinline__ void unpack(float (&v)[8]) const
+    __device__ __forceinline__ void unpack(float2 (&v)[4]) const
     {
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            v[2 * i] = __uint_as_float(w[i] << 16);
-            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
+        for (int i = 0; i < 4; ++i) v[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
     }
 };
 template <>
@@ -84,16 +82,51 @@ struct Raw8<float> {
         a = *reinterpret_cast<const float4 *>(p);
         b = *reinterpret_cast<const float4 *>(p + 4);
     }
-    __device__ __forceinline__ void unpack(float (&v)[8]) const
+    __device__ __forceinline__ void unpack(float2 (&v)[4]) const
     {
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        v[0] = make_float2(a.x, a.y); v[1] = make_float2(a.z, a.w);
+        v[2] = make_float2(b.x, b.y); v[3] = make_float2(b.z, b.w);
     }
 };
 
-// The gates use the hardware exponential and logarithm (CUDA's __expf / __logf intrinsics):
-// a few ulps of relative error (at worst 2^-21 absolute for the logarithm near 1), far inside a
-// bf16 rounding and inside the fp32 outputs' bound; libm-accurate expf / log1pf per element made
-// the pre-mixer issue-bound.
+// packed fp32 pairs (one f32x2 instruction per pair)
+__device__ __forceinline__ float2 pair_fma(float2 a, float2 b, float2 c)
+{
+    unsigned long long r, pa, pb, pc;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(pa) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(pb) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(pc) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pa), "l"(pb), "l"(pc));
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+__device__ __forceinline__ float2 pair_mul(float2 a, float2 b)
+{
+    unsigned long long r, pa, pb;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(pa) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(pb) : "f"(b.x), "f"(b.y));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pa), "l"(pb));
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16 *p, const float2 (&v)[4])
+{
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[i].x, v[i].y);
+        w[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ void store8(float *p, const float2 (&v)[4])
+{
+    *reinterpret_cast<float4 *>(p) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+    *reinterpret_cast<float4 *>(p + 4) = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
+}
+
 __device__ __forceinline__ float sigmoid(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 // clamp(-softplus(a), -5, 0): softplus(a) >= 5 for a >= 4.9933, so larger a need no evaluation
@@ -147,35 +180,60 @@ __global__ void __launch_bounds__(kMixThreads) premix_kernel(const PremixArgs p)
         next = p.cu[n + 1];
     }
 
-    float wt[8][4];
+    // taps as channel pairs: wt[k][i] = (w[c][k], w[c+1][k]) for channels c = col + 2i
+    float2 wt[4][4];
     if (active) {
         const float4 *wp = reinterpret_cast<const float4 *>(p.w + ((long long)xi * HD + col) * 4);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const float4 q4 = wp[c];
-            wt[c][0] = q4.x; wt[c][1] = q4.y; wt[c][2] = q4.z; wt[c][3] = q4.w;
+        for (int i = 0; i < 4; ++i) {
+            const float4 e = wp[2 * i], o = wp[2 * i + 1];
+            wt[0][i] = make_float2(e.x, o.x); wt[1][i] = make_float2(e.y, o.y);
+            wt[2][i] = make_float2(e.z, o.z); wt[3][i] = make_float2(e.w, o.w);
         }
     }
     // history row r (0, 1, 2 = the 3rd, 2nd, 1st token before the start) of sequence `seq`
-    auto hist_row = [&](int seq, int r, float (&v)[8]) {
+    auto hist_row = [&](int seq, int r, float2 (&v)[4]) {
+        Raw8<T> raw;
         if (active && p.hist) {
-            load8(static_cast<const T *>(p.hist) + (((long long)seq * 3 + xi) * 3 + r) * HD + col, v);
+            raw.load(static_cast<const T *>(p.hist) + (((long long)seq * 3 + xi) * 3 + r) * HD + col);
+            raw.unpack(v);
         } else {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) v[c] = 0.f;
+            for (int i = 0; i < 4; ++i) v[i] = make_float2(0.f, 0.f);
         }
     };
-    auto input = [&](long long t, float (&v)[8]) {   // t in [start - 3, t0)
+    auto input = [&](long long t, float2 (&v)[4]) {   // t in [start - 3, t0)
         if (t >= start) {
-            if (active) load8(x + t * HD + col, v);
+            Raw8<T> raw;
+            if (active) {
+                raw.load(x + t * HD + col);
+                raw.unpack(v);
+            }
         } else {
             hist_row(n, 3 - (int)(start - t), v);
         }
     };
-    float w3[8] = {}, w2[8] = {}, w1[8] = {};
+    float2 w3[4] = {}, w2[4] = {}, w1[4] = {};
     input(t0 - 3, w3);
     input(t0 - 2, w2);
     input(t0 - 1, w1);
+
+    // write-gate pre-activations of this chunk's tokens and this block's heads, staged once
+    const long long cb = (long long)blockIdx.y * kMixThreads * 8;
+    const int hpb = (int)(min(HD - cb, (long long)kMixThreads * 8) / p.d);   // heads in the block
+    const long long h_first = cb / p.d;
+    float *s_b = nullptr;
+    if constexpr (kV) {
+        __shared__ float s_b_buf[kMixTokens * kMixThreads];   // tokens x heads (<= 128 heads of d = 8)
+        s_b = s_b_buf;
+        const int cnt = (int)(t1 - t0) * hpb;
+        for (int i = threadIdx.x; i < cnt; i += kMixThreads) {
+            const int tt = i / hpb, hh = i - tt * hpb;
+            s_b[i] = to_f32(static_cast<const T *>(p.b)[(t0 + tt) * p.H + h_first + hh]);
+        }
+        __syncthreads();
+    }
+
     // the next kMixDepth tokens' x (and a) are in flight while one token is computed
     const T *av_base = static_cast<const T *>(p.a);
     Raw8<T> ring[kMixDepth], aring[kMixDepth];
@@ -194,7 +252,7 @@ __global__ void __launch_bounds__(kMixThreads) premix_kernel(const PremixArgs p)
         for (int j = 0; j < kMixDepth; ++j) {
             const long long t = tb + j;
             if (t >= t1) break;
-            float cur[8], av[8];
+            float2 cur[4], av[4];
             ring[j].unpack(cur);
             if (kV) aring[j].unpack(av);
             if (active && t + kMixDepth < t1) {
@@ -212,32 +270,34 @@ __global__ void __launch_bounds__(kMixThreads) premix_kernel(const PremixArgs p)
                 hist_row(n, 1, w2);
                 hist_row(n, 2, w1);
             }
-            float o[8];
-            float ss = 0.f;
+            float2 o[4];
+            float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                o[c] = fmaf(wt[c][3], cur[c], fmaf(wt[c][2], w1[c], fmaf(wt[c][1], w2[c], wt[c][0] * w3[c])));
-                ss = fmaf(o[c], o[c], ss);
-                w3[c] = w2[c];
-                w2[c] = w1[c];
-                w1[c] = cur[c];
+            for (int i = 0; i < 4; ++i) {
+                o[i] = pair_fma(wt[3][i], cur[i], pair_fma(wt[2][i], w1[i], pair_fma(wt[1][i], w2[i], pair_mul(wt[0][i], w3[i]))));
+                ss2 = pair_fma(o[i], o[i], ss2);
+                w3[i] = w2[i];
+                w2[i] = w1[i];
+                w1[i] = cur[i];
             }
             if (!kV) {
                 // per-head sum of squares over the head's `group` threads (aligned lane groups)
+                float ss = ss2.x + ss2.y;
                 for (int m = group >> 1; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
                 const float inv = rsqrtf(fmaxf(ss, p.eps * p.eps));   // 1 / max(||y||, eps)
 #pragma unroll
-                for (int c = 0; c < 8; ++c) o[c] *= inv;
+                for (int i = 0; i < 4; ++i) o[i] = pair_mul(o[i], make_float2(inv, inv));
             }
             if (!active) continue;
             store8(y + t * HD + col, o);
             if (kV) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) av[c] = decay_gate(av[c]);
+                for (int i = 0; i < 4; ++i) av[i] = make_float2(decay_gate(av[i].x), decay_gate(av[i].y));
                 store8(static_cast<T *>(p.g) + t * HD + col, av);
                 if (col % p.d == 0) {
-                    const long long hb = t * p.H + col / p.d;
-                    store_as(static_cast<T *>(p.beta) + hb, sigmoid(to_f32(static_cast<const T *>(p.b)[hb])));
+                    const long long hh = col / p.d;
+                    store_as(static_cast<T *>(p.beta) + t * p.H + hh,
+                             sigmoid(s_b[(int)(t - t0) * hpb + (int)(hh - h_first)]));
                 }
             }
         }
