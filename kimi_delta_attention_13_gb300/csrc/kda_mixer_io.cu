@@ -11,11 +11,13 @@
 //   g = clamp(-softplus(a), -5, 0),  beta = 1 / (1 + exp(-b))
 //   out = o / (1 + exp(-z))
 //
-// Both kernels stream HBM once (the roofline is bytes / bandwidth): 16-byte vector loads and
-// stores of 8 channels per thread, fp32 arithmetic.  The pre-mixer walks a 32-token chunk per
-// thread with a 3-token register window and keeps the next 8 (bf16) or 4 (fp32) tokens' loads in
-// flight; the chunk's first tokens read their 3-token halo, which the neighbouring chunk
-// (scheduled next to it: token chunks are the fastest grid dimension) has just brought into L2.
+// Every kernel here streams HBM once (the roofline is bytes / bandwidth): 16-byte vector loads
+// and stores of 8 channels per thread, fp32 arithmetic.  The pre-mixer is two launches: the
+// convolution of q, k and v, whose threads walk a 32-token chunk with a 3-token register window
+// and keep the next 8 (bf16) or 4 (fp32) tokens' loads in flight (the chunk's first tokens read a
+// 3-token halo that the neighbouring chunk, scheduled next to it, has just brought into L2); and
+// the gates, elementwise at full occupancy (their exp/log chains kept the convolution's warps
+// waiting when both shared a kernel).
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -151,13 +153,15 @@ struct PremixArgs {
     void *beta;            // [T, H]
 };
 
-// blockIdx.x: 32-token chunk, blockIdx.y: 1024-channel block; kV = false: blockIdx.z = 0 (q) or
-// 1 (k), normalised; kV = true: v with the gates.  Thread: 8 channels [col, col + 8) of one head.
-template <typename T, bool kV>
-__global__ void __launch_bounds__(kMixThreads) premix_kernel(const PremixArgs p)
+// The short convolution.  blockIdx.x: 32-token chunk, blockIdx.y: 1024-channel block,
+// blockIdx.z: 0 = q, 1 = k (both normalised), 2 = v.  Thread: 8 channels [col, col + 8) of one
+// head.
+template <typename T>
+__global__ void __launch_bounds__(kMixThreads) premix_conv_kernel(const PremixArgs p)
 {
     constexpr int kMixDepth = mix_depth<T>();
-    const int xi = kV ? 2 : blockIdx.z;
+    const int xi = blockIdx.z;
+    const bool norm = xi < 2;
     const long long HD = (long long)p.H * p.d;
     const long long col = 8ll * ((long long)blockIdx.y * kMixThreads + threadIdx.x);
     const bool active = col < HD;
@@ -218,32 +222,12 @@ __global__ void __launch_bounds__(kMixThreads) premix_kernel(const PremixArgs p)
     input(t0 - 2, w2);
     input(t0 - 1, w1);
 
-    // write-gate pre-activations of this chunk's tokens and this block's heads, staged once
-    const long long cb = (long long)blockIdx.y * kMixThreads * 8;
-    const int hpb = (int)(min(HD - cb, (long long)kMixThreads * 8) / p.d);   // heads in the block
-    const long long h_first = cb / p.d;
-    float *s_b = nullptr;
-    if constexpr (kV) {
-        __shared__ float s_b_buf[kMixTokens * kMixThreads];   // tokens x heads (<= 128 heads of d = 8)
-        s_b = s_b_buf;
-        const int cnt = (int)(t1 - t0) * hpb;
-        for (int i = threadIdx.x; i < cnt; i += kMixThreads) {
-            const int tt = i / hpb, hh = i - tt * hpb;
-            s_b[i] = to_f32(static_cast<const T *>(p.b)[(t0 + tt) * p.H + h_first + hh]);
-        }
-        __syncthreads();
-    }
-
-    // the next kMixDepth tokens' x (and a) are in flight while one token is computed
-    const T *av_base = static_cast<const T *>(p.a);
-    Raw8<T> ring[kMixDepth], aring[kMixDepth];
+    // the next kMixDepth tokens' x are in flight while one token is computed
+    Raw8<T> ring[kMixDepth];
 #pragma unroll
     for (int j = 0; j < kMixDepth; ++j) {
         const long long t = t0 + j;
-        if (active && t < t1) {
-            ring[j].load(x + t * HD + col);
-            if (kV) aring[j].load(av_base + t * HD + col);
-        }
+        if (active && t < t1) ring[j].load(x + t * HD + col);
     }
 
     const int group = p.d >> 3;   // threads per head (a power of two <= 32)
@@ -252,13 +236,9 @@ __global__ void __launch_bounds__(kMixThreads) premix_kernel(const PremixArgs p)
         for (int j = 0; j < kMixDepth; ++j) {
             const long long t = tb + j;
             if (t >= t1) break;
-            float2 cur[4], av[4];
+            float2 cur[4];
             ring[j].unpack(cur);
-            if (kV) aring[j].unpack(av);
-            if (active && t + kMixDepth < t1) {
-                ring[j].load(x + (t + kMixDepth) * HD + col);
-                if (kV) aring[j].load(av_base + (t + kMixDepth) * HD + col);
-            }
+            if (active && t + kMixDepth < t1) ring[j].load(x + (t + kMixDepth) * HD + col);
             if (t == next) {
                 // a new sequence starts at t: its window is its own history
                 do {
@@ -280,7 +260,7 @@ __global__ void __launch_bounds__(kMixThreads) premix_kernel(const PremixArgs p)
                 w2[i] = w1[i];
                 w1[i] = cur[i];
             }
-            if (!kV) {
+            if (norm) {
                 // per-head sum of squares over the head's `group` threads (aligned lane groups)
                 float ss = ss2.x + ss2.y;
                 for (int m = group >> 1; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
@@ -288,20 +268,29 @@ __global__ void __launch_bounds__(kMixThreads) premix_kernel(const PremixArgs p)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) o[i] = pair_mul(o[i], make_float2(inv, inv));
             }
-            if (!active) continue;
-            store8(y + t * HD + col, o);
-            if (kV) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) av[i] = make_float2(decay_gate(av[i].x), decay_gate(av[i].y));
-                store8(static_cast<T *>(p.g) + t * HD + col, av);
-                if (col % p.d == 0) {
-                    const long long hh = col / p.d;
-                    store_as(static_cast<T *>(p.beta) + t * p.H + hh,
-                             sigmoid(s_b[(int)(t - t0) * hpb + (int)(hh - h_first)]));
-                }
-            }
+            if (active) store8(y + t * HD + col, o);
         }
     }
+}
+
+// The gates: g = clamp(-softplus(a), -5, 0) over n8 groups of 8 elements, beta = sigmoid(b) over
+// nb elements (grid-stride loops)
+template <typename T>
+__global__ void __launch_bounds__(256) premix_gates_kernel(const T *a, const T *b, T *g, T *beta,
+                                                           long long n8, long long nb)
+{
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    for (long long i = i0; i < n8; i += stride) {
+        Raw8<T> raw;
+        raw.load(a + 8 * i);
+        float2 v[4];
+        raw.unpack(v);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[c] = make_float2(decay_gate(v[c].x), decay_gate(v[c].y));
+        store8(g + 8 * i, v);
+    }
+    for (long long i = i0; i < nb; i += stride) store_as(beta + i, sigmoid(to_f32(b[i])));
 }
 
 // out = o * sigmoid(z) over n elements; 8 per thread and step of a grid-stride loop
@@ -363,15 +352,21 @@ int launch_premix(const void *xq, const void *xk, const void *xv, const void *a,
     p.y[0] = q; p.y[1] = k; p.y[2] = v;
     p.g = g; p.beta = beta;
     const long long HD = (long long)n_heads * d;
-    const dim3 grid_qk((unsigned)((total_tokens + kMixTokens - 1) / kMixTokens),
-                       (unsigned)((HD / 8 + kMixThreads - 1) / kMixThreads), 2);
-    const dim3 grid_v(grid_qk.x, grid_qk.y, 1);
+    const dim3 grid((unsigned)((total_tokens + kMixTokens - 1) / kMixTokens),
+                    (unsigned)((HD / 8 + kMixThreads - 1) / kMixThreads), 3);
+    const long long n8 = total_tokens * HD / 8, nb = total_tokens * n_heads;
+    const long long want = (n8 + 255) / 256, cap = 8ll * sm_count();
+    const dim3 ggrid((unsigned)(want < cap ? want : cap));
     if (dtype == KDA_BF16) {
-        premix_kernel<__nv_bfloat16, false><<<grid_qk, kMixThreads, 0, stream>>>(p);
-        premix_kernel<__nv_bfloat16, true><<<grid_v, kMixThreads, 0, stream>>>(p);
+        premix_conv_kernel<__nv_bfloat16><<<grid, kMixThreads, 0, stream>>>(p);
+        premix_gates_kernel<__nv_bfloat16><<<ggrid, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(a), static_cast<const __nv_bfloat16 *>(b),
+            static_cast<__nv_bfloat16 *>(g), static_cast<__nv_bfloat16 *>(beta), n8, nb);
     } else {
-        premix_kernel<float, false><<<grid_qk, kMixThreads, 0, stream>>>(p);
-        premix_kernel<float, true><<<grid_v, kMixThreads, 0, stream>>>(p);
+        premix_conv_kernel<float><<<grid, kMixThreads, 0, stream>>>(p);
+        premix_gates_kernel<float><<<ggrid, 256, 0, stream>>>(
+            static_cast<const float *>(a), static_cast<const float *>(b), static_cast<float *>(g),
+            static_cast<float *>(beta), n8, nb);
     }
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
