@@ -68,7 +68,8 @@ def run_premix(orc, x, dtype, heads=None):
 @pytest.mark.parametrize("dtype,lengths,H,d,hist", [
     ("bf16", [100, 1, 37, 2, 64], 3, 128, False),
     ("bf16", [100, 1, 37, 2, 64], 3, 128, True),
-    ("bf16", [31, 32, 33], 4, 128, True),           # sequence edges next to chunk edges
+    ("bf16", [31, 32, 33], 4, 128, True),
+    ("bf16", [127, 1, 129, 3], 2, 128, True),       # sequence edges next to 128-token chunk edges
     ("bf16", [0, 5, 0, 40, 0], 2, 128, True),       # empty sequences
     ("f32", [45, 3, 70], 5, 64, True),              # 320 channels: a partial channel block
     ("f32", [9], 2, 8, False),
