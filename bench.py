@@ -419,6 +419,9 @@ def run_gb300(args):
     reuse = prefix_reuse_figure(dev, stream)
     assert kda.device_status() == 0
     torch.cuda.empty_cache()
+    cp = context_parallel_figure(dev, stream)
+    assert kda.device_status() == 0
+    torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
@@ -468,6 +471,7 @@ def run_gb300(args):
         "state_copy": {"workload": "64 states x 96 heads gathered by index (403 MB)",
                        "GB/s": cp_gbs, "frac": cp_gbs / hbm_peak, "ms": cp_ms},
         "prefix_reuse": reuse,
+        "context_parallel": cp,
         "gpu_launches": args.steps,
         "clocks": clk,
         "cpu_baseline": base,
@@ -529,6 +533,35 @@ def prefix_reuse_figure(dev, stream, n_req: int = 4, prefix: int = 16384, new_to
             "cache_hit_tokens_per_s": served / (hit_ms / 1e3),
             "new_tokens_per_s": n_req * new_tokens / (hit_ms / 1e3),
             "speedup": miss_ms / hit_ms, "restored_from_tokens": covered}
+
+
+def context_parallel_figure(dev, stream, T=262144, heads=8, seg_len=16384):
+    """One long sequence at a low head count: the plain prefill runs one CTA per head; the
+    context-parallel prefill cuts the sequence into segments that prefill side by side."""
+    import torch
+
+    import kimi_delta_attention_13_gb300 as kda
+    from kimi_delta_attention_13_gb300 import synth
+    from kimi_delta_attention_13_gb300.context_parallel import prefill_cp
+
+    x = synth.make_inputs([T], heads=heads, dtype="bf16", seed=9, device=dev)
+    args = [x[k_] for k_ in ("q", "k", "v", "g", "beta")]
+
+    def plain():
+        kda.prefill(*args, stream=stream)
+
+    def split():
+        prefill_cp(*args, seg_len=seg_len, lengths=[T], stream=stream)
+
+    plain()
+    split()
+    _, plain_ms = cuda_time_ms(plain, 2, stream)
+    _, cp_ms = cuda_time_ms(split, 3, stream)
+    del x, args
+    return {"workload": f"one sequence T={T} H={heads} d={D} bf16, fp32 out and final state; "
+                        f"segments of {seg_len} tokens",
+            "plain_ms": plain_ms, "cp_ms": cp_ms, "speedup": plain_ms / cp_ms,
+            "cp_tokens_per_s": T / (cp_ms / 1e3), "plain_tokens_per_s": T / (plain_ms / 1e3)}
 
 
 def kbuild_source_hash() -> str:

@@ -187,6 +187,32 @@ int kda_output_gate(const void *o, int32_t o_dtype, const void *z, int32_t z_dty
                     int32_t out_dtype, int64_t n, void *stream);
 
 /*
+ * kda_cp_combine -- the scan of a context-parallel prefill.
+ *
+ * The recurrence above is affine in the state: per token S_t = A_t S_(t-1) + beta_t k_t v_t^T with
+ * A_t = (I - beta_t k_t k_t^T) diag(exp(clamp(g_t, -5, 0))).  Over a segment of a sequence,
+ * S_end = M S_start + S_loc, where S_loc is the segment's final state from a zero initial state
+ * (a kda_prefill of the segment) and M = A_L ... A_1 is its final state when prefilled with v = 0
+ * from the identity (a kda_prefill with d_v = d_k).  Splitting a sequence into segments lets
+ * those two prefills run every segment side by side; this call turns their end states into each
+ * segment's true initial state, and one more kda_prefill of the segments from those states gives
+ * the sequence's outputs and final state.
+ *
+ * For every sequence n and head, over its segments j in [seq_seg[n], seq_seg[n+1]) (at least one;
+ * the first prefilled from the sequence's own initial state, so S_loc(first) is its true end state):
+ *     S_start(first + 1) = S_loc(first),   S_start(j + 1) = M(j) S_start(j) + S_loc(j).
+ *   s_loc, m       fp32 [n_seg, H, d, d]: the segments' final states of the two prefills (m of a
+ *                  sequence's first segment is not read).
+ *   seq_seg        device int32 [n_seqs + 1], non-decreasing segment ranges per sequence.
+ *   s_start        fp32 [n_seg, H, d, d]: written for every segment but the first of each sequence.
+ *   final_state    fp32 [n_seqs, H, d, d] (M(last) S_start(last) + S_loc(last)) or NULL.
+ *   d              128.  Outputs must not alias inputs.  Arithmetic is fp32.
+ * Errors: KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED_SHAPE, KDA_ERR_MISALIGNED, KDA_ERR_CUDA.
+ */
+int kda_cp_combine(const float *s_loc, const float *m, const int32_t *seq_seg, int32_t n_seqs,
+                   int32_t n_heads, int32_t d, float *s_start, float *final_state, void *stream);
+
+/*
  * kda_device_status -- synchronize `stream`, then read and clear the current device's sticky
  * error word (KDA_OK if no device-side error was recorded since the last read).  *status
  * receives the recorded kda_status.  Returns KDA_OK, or KDA_ERR_CUDA if the read failed.

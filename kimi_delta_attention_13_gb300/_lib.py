@@ -35,6 +35,7 @@ SIGNATURES = {
     "kda_premix": (ctypes.c_int, [_vp] * 7 + [_vp, _i32, _i64, _i32, _i32, ctypes.c_float, _i32]
                    + [_vp] * 5 + [_vp]),
     "kda_output_gate": (ctypes.c_int, [_vp, _i32, _vp, _i32, _vp, _i32, _i64, _vp]),
+    "kda_cp_combine": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
 }
 
 _LIB = None

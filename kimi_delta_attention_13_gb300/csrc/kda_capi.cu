@@ -176,6 +176,23 @@ int kda_output_gate(const void *o, int32_t o_dtype, const void *z, int32_t z_dty
     return launch_output_gate(o, o_dtype, z, z_dtype, out, out_dtype, n, (cudaStream_t)stream);
 }
 
+int kda_cp_combine(const float *s_loc, const float *m, const int32_t *seq_seg, int32_t n_seqs,
+                   int32_t n_heads, int32_t d, float *s_start, float *final_state, void *stream)
+{
+    if (n_seqs < 0 || n_heads < 1 || d < 1) return KDA_ERR_INVALID_ARG;
+    if (d != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (n_seqs > 0 && (!s_loc || !m || !seq_seg || !s_start)) return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {s_loc, m, s_start, final_state};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(seq_seg) & 3u) != 0) return KDA_ERR_MISALIGNED;
+    if (s_start && (s_start == s_loc || s_start == m)) return KDA_ERR_INVALID_ARG;
+    if (final_state && (final_state == s_loc || final_state == m || final_state == s_start))
+        return KDA_ERR_INVALID_ARG;
+    return launch_cp_combine(s_loc, m, seq_seg, n_seqs, n_heads, s_start, final_state,
+                             (cudaStream_t)stream);
+}
+
 int kda_diag_device_timeout(int64_t timeout_cycles, void *stream)
 {
     if (timeout_cycles < 1 || timeout_cycles > 4000000000LL) return KDA_ERR_INVALID_ARG;

@@ -47,6 +47,8 @@ int launch_premix(const void *xq, const void *xk, const void *xv, const void *a,
                   void *k, void *v, void *g, void *beta, cudaStream_t stream);
 int launch_output_gate(const void *o, int o_dtype, const void *z, int z_dtype, void *out,
                        int out_dtype, long long n, cudaStream_t stream);
+int launch_cp_combine(const float *s_loc, const float *m, const int32_t *seq_seg, int n_seqs, int H,
+                      float *s_start, float *final_state, cudaStream_t stream);
 int launch_prefill_tc(const void *q, const void *k, const void *v, const void *g,
                       const void *beta, const int32_t *cu_seqlens, int n_seqs,
                       int64_t total_tokens, int n_heads, int out_dtype, const float *init_state,

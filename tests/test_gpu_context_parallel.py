@@ -1,0 +1,66 @@
+"""Context-parallel prefill on the GPU against the fp64 oracle's plain (token by token) prefill:
+segments prefilled side by side and joined by kda_cp_combine's scan must give the outputs and
+final states of the whole sequences (bf16 inputs: 2e-2 x RMS on outputs, 1e-2 on states)."""
+import pytest
+import torch
+
+import kimi_delta_attention_13_gb300 as kda
+import oracle
+from kimi_delta_attention_13_gb300 import synth
+from kimi_delta_attention_13_gb300.context_parallel import prefill_cp
+from parity import TOL, assert_close, head_slice
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    yield
+    torch.cuda.empty_cache()
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.default()
+
+
+def check(orc, lengths, heads, seg_len, init, seed, oracle_heads=None):
+    x = synth.make_inputs(lengths, heads=heads, dtype="bf16", seed=seed, device=DEV, init_state=init)
+    out, fin = prefill_cp(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], x["state"],
+                          seg_len=seg_len, lengths=lengths)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    hs = list(range(heads)) if oracle_heads is None else oracle_heads
+    c = head_slice(x, hs)
+    init_c = None if x["state"] is None else x["state"][:, hs].cpu()
+    ro, rf, _ = orc.prefill(c["q"], c["k"], c["v"], c["g"], c["beta"], x["cu_seqlens"].cpu().long(), init_c)
+    idx = torch.tensor(hs, device=DEV)
+    assert_close("out", out.index_select(1, idx), ro, TOL["bf16"]["out"])
+    assert_close("final_state", fin.index_select(1, idx), rf, TOL["bf16"]["state"])
+    return x, out, fin
+
+
+@pytest.mark.parametrize("lengths,heads,seg_len,init", [
+    ([300, 5, 700], 2, 128, True),      # ragged segments, a sequence shorter than a segment
+    ([1000], 3, 64, False),             # many segments
+    ([0, 257, 0, 64], 2, 64, True),     # empty sequences, a sequence of exactly one segment
+    ([4096], 2, 1000, True),            # segment length not a multiple of the tile
+])
+def test_cp_matches_oracle(orc, lengths, heads, seg_len, init):
+    check(orc, lengths, heads, seg_len, init, seed=sum(lengths) + seg_len)
+
+
+def test_cp_without_a_split_is_the_plain_prefill(orc):
+    x, out, fin = check(orc, [200, 31], 2, 4096, True, seed=71)
+    o2, f2, _ = kda.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], x["state"])
+    torch.cuda.synchronize()
+    assert torch.equal(out, o2) and torch.equal(fin, f2)
+
+
+def test_cp_long_sequence(orc):
+    # 65,536 tokens of 4 heads in 8 segments of 8,192: 32 + 32 CTAs instead of 4
+    check(orc, [65536], 4, 8192, True, seed=72)
