@@ -535,14 +535,16 @@ def prefix_reuse_figure(dev, stream, n_req: int = 4, prefix: int = 16384, new_to
             "speedup": miss_ms / hit_ms, "restored_from_tokens": covered}
 
 
-def context_parallel_figure(dev, stream, T=262144, heads=8, seg_len=16384):
+def context_parallel_figure(dev, stream, T=262144, heads=8):
     """One long sequence at a low head count: the plain prefill runs one CTA per head; the
     context-parallel prefill cuts the sequence into segments that prefill side by side."""
     import torch
 
     import kimi_delta_attention_13_gb300 as kda
     from kimi_delta_attention_13_gb300 import synth
-    from kimi_delta_attention_13_gb300.context_parallel import prefill_cp
+    from kimi_delta_attention_13_gb300.context_parallel import auto_seg_len, prefill_cp
+
+    seg_len = auto_seg_len(T, heads, torch.cuda.get_device_properties(dev).multi_processor_count)
 
     x = synth.make_inputs([T], heads=heads, dtype="bf16", seed=9, device=dev)
     args = [x[k_] for k_ in ("q", "k", "v", "g", "beta")]

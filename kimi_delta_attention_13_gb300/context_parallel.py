@@ -41,6 +41,14 @@ def segments(lengths: Sequence[int], seg_len: int) -> Tuple[List[Tuple[int, int]
     return bounds, seq_seg
 
 
+def auto_seg_len(total_tokens: int, heads: int, sms: int) -> int:
+    """A segment length that fills the GPU in one wave: about sms / heads segments per sequence
+    of `total_tokens`, rounded up to a multiple of the 32-token chain step."""
+    per_seq = max(1, sms // max(1, heads))
+    per = -(-int(total_tokens) // per_seq)
+    return max(32, -(-per // 32) * 32)
+
+
 def prefill_cp(q, k, v, g, beta, cu_seqlens=None, init_state=None, *, seg_len: int,
                lengths: Optional[Sequence[int]] = None, out=None, final_state=True, stream=None):
     """Varlen KDA prefill with every sequence cut into segments of `seg_len` tokens that prefill

@@ -23,3 +23,13 @@ def test_bad_arguments():
         segments([10], 0)
     with pytest.raises(ValueError):
         segments([-1], 8)
+
+
+def test_auto_seg_len_fills_one_wave():
+    from kimi_delta_attention_13_gb300.context_parallel import auto_seg_len
+
+    L = auto_seg_len(262144, 8, 152)
+    assert L % 32 == 0
+    n_seg = -(-262144 // L)
+    assert n_seg * 8 <= 152 and (n_seg + 1) * 8 > 152 - 8
+    assert auto_seg_len(100, 200, 152) >= 100     # more heads than SMs: no split
