@@ -25,11 +25,11 @@ def test_bad_arguments():
         segments([-1], 8)
 
 
-def test_auto_seg_len_fills_one_wave():
+def test_auto_seg_len_is_one_wave():
     from kimi_delta_attention_13_gb300.context_parallel import auto_seg_len
 
     L = auto_seg_len(262144, 8, 152)
     assert L % 32 == 0
     n_seg = -(-262144 // L)
-    assert n_seg * 8 <= 152 and (n_seg + 1) * 8 > 152 - 8
+    assert n_seg == 16                            # 16 x 8 = 128 CTAs: 7/8 of 152 SMs
     assert auto_seg_len(100, 200, 152) >= 100     # more heads than SMs: no split
