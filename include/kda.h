@@ -187,6 +187,43 @@ int kda_output_gate(const void *o, int32_t o_dtype, const void *z, int32_t z_dty
                     int32_t out_dtype, int64_t n, void *stream);
 
 /*
+ * kda_prefill_staged -- kda_prefill from pinned host memory, with the copies overlapped.
+ *
+ * The same operation as kda_prefill (d_k = d_v = 128, no checkpoints) for inputs and outputs in
+ * host memory.  The packed tokens are cut into chunks of `chunk_tokens`: chunk c's inputs are
+ * copied host -> device on one internal stream, prefilled on `stream` (every sequence resumes
+ * from its running state in final_state, as the recurrence hands the state on from token to
+ * token), and its outputs copied device -> host on a second internal stream, so uploads,
+ * prefills and downloads of neighbouring chunks overlap.  When the call returns, all of it is
+ * enqueued and `stream` is ordered after the last download.
+ *
+ *   h_q, h_k, h_v, h_g, h_beta   pinned host inputs, layouts and `dtype` as for kda_prefill.
+ *   h_cu_seqlens     HOST int32 [n_seqs + 1] (checked here: 0, non-decreasing, total_tokens),
+ *                    or NULL when n_seqs == 1.
+ *   init_state       device fp32 [n_seqs, H, 128, 128] or NULL (zeros); may alias final_state.
+ *   d_q .. d_beta, d_out   device buffers of the inputs' / outputs' full size (staging).
+ *   h_out            pinned host [total_tokens, H, 128] outputs (`out_dtype`).
+ *   final_state      device fp32 [n_seqs, H, 128, 128] (required: it carries the states).
+ *   d_scratch        device int32 [scratch_ints] for the chunks' sequence tables, at least
+ *                    kda_prefill_staged_scratch(...) entries (0 for a single sequence).
+ *   chunk_tokens     >= 1 (a multiple of 32 keeps a single sequence's arithmetic identical to
+ *                    kda_prefill's).
+ * Errors: those of kda_prefill, KDA_ERR_INVALID_ARG (a bad host table, too little scratch),
+ * KDA_ERR_CUDA (stream or event creation, copies).
+ */
+int kda_prefill_staged(const void *h_q, const void *h_k, const void *h_v, const void *h_g,
+                       const void *h_beta, const int32_t *h_cu_seqlens, int32_t n_seqs,
+                       int64_t total_tokens, int32_t n_heads, int32_t dtype, int32_t out_dtype,
+                       const float *init_state, void *d_q, void *d_k, void *d_v, void *d_g,
+                       void *d_beta, void *d_out, void *h_out, float *final_state,
+                       int32_t *d_scratch, int64_t scratch_ints, int64_t chunk_tokens, void *stream);
+
+/* Scratch entries (int32) kda_prefill_staged needs for these sequences and chunk size, or -1 for
+ * invalid arguments.  Host-only. */
+int64_t kda_prefill_staged_scratch(const int32_t *h_cu_seqlens, int32_t n_seqs, int64_t total_tokens,
+                                   int64_t chunk_tokens);
+
+/*
  * kda_cp_combine -- the scan of a context-parallel prefill.
  *
  * The recurrence above is affine in the state: per token S_t = A_t S_(t-1) + beta_t k_t v_t^T with

@@ -21,7 +21,8 @@ from . import _lib
 from ._lib import KDAError
 
 __all__ = ["prefill", "prefill_recurrent", "decode", "state_copy", "device_status", "prefill_path",
-           "num_checkpoints", "KDAError", "load", "diag_device_timeout", "premix", "output_gate"]
+           "num_checkpoints", "KDAError", "load", "diag_device_timeout", "premix", "output_gate",
+           "prefill_staged"]
 
 _DTYPES = {torch.bfloat16: _lib.KDA_BF16, torch.float32: _lib.KDA_F32}
 
@@ -216,6 +217,66 @@ def output_gate(o, z, *, out=None, out_dtype=None, stream=None):
                              _DTYPES[out.dtype], o.numel(), _stream(dev, stream))
     _lib.check(rc, "kda_output_gate")
     return out
+
+
+def prefill_staged(h_q, h_k, h_v, h_g, h_beta, h_cu_seqlens=None, init_state=None, *,
+                   device=None, chunk_tokens: int = 1024, buffers=None, h_out=None,
+                   final_state=None, out_dtype=torch.float32, stream=None):
+    """kda_prefill from pinned host memory with the copies overlapped (kda_prefill_staged).
+
+    h_q, h_k, h_v, h_g: pinned CPU [T, H, 128]; h_beta: pinned CPU [T, H] (one dtype, bf16 or
+    fp32); h_cu_seqlens: CPU int32 [N+1] (or a list) or None for one sequence; init_state: device
+    fp32 [N, H, 128, 128] or None.  `buffers` (device staging, returned, reusable across calls),
+    `h_out` (pinned CPU [T, H, 128]) and `final_state` are allocated when not passed.  The work is
+    enqueued on `stream`; synchronise it before reading h_out.  Returns (h_out, final_state,
+    buffers)."""
+    import numpy as np
+
+    lib = _lib.load()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    dtype = h_q.dtype
+    if dtype not in _DTYPES or out_dtype not in _DTYPES:
+        raise ValueError("inputs and outputs must be bfloat16 or float32")
+    T, H, D = h_q.shape
+    if D != 128:
+        raise ValueError("the staged prefill takes d_k = d_v = 128")
+    for t, name, shp in ((h_q, "h_q", (T, H, D)), (h_k, "h_k", (T, H, D)), (h_v, "h_v", (T, H, D)),
+                         (h_g, "h_g", (T, H, D)), (h_beta, "h_beta", (T, H))):
+        if t.device.type != "cpu" or not t.is_pinned() or not t.is_contiguous() or t.dtype != dtype \
+                or tuple(t.shape) != shp:
+            raise ValueError(f"{name} must be a pinned, contiguous CPU tensor {shp} of {dtype}")
+    cu = None
+    if h_cu_seqlens is not None:
+        cu = np.ascontiguousarray(np.asarray(h_cu_seqlens.tolist() if hasattr(h_cu_seqlens, "tolist")
+                                             else h_cu_seqlens, dtype=np.int32))
+    n = 1 if cu is None else cu.shape[0] - 1
+    cu_ptr = None if cu is None else cu.ctypes.data
+    if init_state is not None:
+        _require(init_state, "init_state", dev, torch.float32, (n, H, D, D))
+    if final_state is None:
+        final_state = torch.empty((n, H, D, D), device=dev, dtype=torch.float32)
+    _require(final_state, "final_state", dev, torch.float32, (n, H, D, D))
+    if h_out is None:
+        h_out = torch.empty((T, H, D), dtype=out_dtype).pin_memory()
+    if h_out.device.type != "cpu" or not h_out.is_pinned() or h_out.dtype != out_dtype or \
+            tuple(h_out.shape) != (T, H, D):
+        raise ValueError("h_out must be a pinned CPU tensor [T, H, 128] of out_dtype")
+    need = int(lib.kda_prefill_staged_scratch(cu_ptr, n, T, int(chunk_tokens)))
+    if need < 0:
+        raise ValueError("invalid sequences or chunk size")
+    if buffers is None:
+        buffers = {k: torch.empty_like(t, device=dev) for k, t in
+                   (("q", h_q), ("k", h_k), ("v", h_v), ("g", h_g), ("beta", h_beta))}
+        buffers["out"] = torch.empty((T, H, D), device=dev, dtype=out_dtype)
+    if "scratch" not in buffers or buffers["scratch"].numel() < need:
+        buffers["scratch"] = torch.empty(max(need, 1), device=dev, dtype=torch.int32)
+    rc = lib.kda_prefill_staged(
+        _ptr(h_q), _ptr(h_k), _ptr(h_v), _ptr(h_g), _ptr(h_beta), cu_ptr, n, T, H, _DTYPES[dtype],
+        _DTYPES[out_dtype], _ptr(init_state), *[_ptr(buffers[k]) for k in ("q", "k", "v", "g", "beta", "out")],
+        _ptr(h_out), _ptr(final_state), _ptr(buffers["scratch"]), buffers["scratch"].numel(),
+        int(chunk_tokens), _stream(dev, stream))
+    _lib.check(rc, "kda_prefill_staged")
+    return h_out, final_state, buffers
 
 
 def state_copy(dst, src, dst_idx=None, src_idx=None, n: Optional[int] = None, stream=None):

@@ -139,8 +139,6 @@ __device__ __forceinline__ float decay_gate(float a)
 
 struct PremixArgs {
     const void *x[3];      // xq, xk, xv  [T, H, d]
-    const void *a;         // [T, H, d]
-    const void *b;         // [T, H]
     const float *w;        // [3, H*d, 4]
     const void *hist;      // [N, 3, 3, H*d] or null
     const int32_t *cu;     // [N+1] or null (one sequence)
@@ -149,8 +147,6 @@ struct PremixArgs {
     int H, d;
     float eps;
     void *y[3];            // q, k, v  [T, H, d]
-    void *g;               // [T, H, d]
-    void *beta;            // [T, H]
 };
 
 // The short convolution.  blockIdx.x: kMixTokens-token chunk, blockIdx.y: 1024-channel block,
@@ -344,13 +340,12 @@ int launch_premix(const void *xq, const void *xk, const void *xv, const void *a,
     if (total_tokens == 0) return KDA_OK;
     PremixArgs p;
     p.x[0] = xq; p.x[1] = xk; p.x[2] = xv;
-    p.a = a; p.b = b; p.w = w; p.hist = hist;
+    p.w = w; p.hist = hist;
     p.cu = n_seqs == 1 ? nullptr : cu_seqlens;
     p.n_seqs = n_seqs;
     p.T = total_tokens;
     p.H = n_heads; p.d = d; p.eps = eps;
     p.y[0] = q; p.y[1] = k; p.y[2] = v;
-    p.g = g; p.beta = beta;
     const long long HD = (long long)n_heads * d;
     const dim3 grid((unsigned)((total_tokens + kMixTokens - 1) / kMixTokens),
                     (unsigned)((HD / 8 + kMixThreads - 1) / kMixThreads), 3);

@@ -1,0 +1,141 @@
+// kda_staged.cu -- prefill from pinned host memory with the copies overlapped with the compute.
+//
+// The packed tokens are cut into chunks.  Chunk c's inputs go host -> device on one internal
+// stream, its prefill runs on the caller's stream once they have landed (every sequence resumes
+// from its running state, kept in final_state: the recurrence hands the state from token to token,
+// "Kimi K3 im Detail", section "Sequenz-Mixing: KDA-Zustand und globale MLA"), and its outputs go
+// device -> host on a second internal stream.  Chunk c+1's upload therefore overlaps chunk c's
+// prefill and chunk c-1's download, and both copy directions run at once.
+#include <vector>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+struct Chunk {
+    long long t0, t1;   // token range
+    int n_a, n_b;       // sequences n_a .. n_b (inclusive) intersect it
+    int cu_off;         // its sub-batch cu table in the scratch (-1: one sequence, no table)
+};
+
+// The chunks of `chunk_tokens` tokens and their sub-batch cu tables (appended to `tab`)
+std::vector<Chunk> plan(const int32_t *cu, int n_seqs, long long T, long long chunk_tokens,
+                        std::vector<int32_t> &tab)
+{
+    std::vector<Chunk> out;
+    int n = 0;
+    for (long long t0 = 0; t0 < T; t0 += chunk_tokens) {
+        const long long t1 = t0 + chunk_tokens < T ? t0 + chunk_tokens : T;
+        while (n + 1 < n_seqs && cu[n + 1] <= t0) ++n;   // first sequence holding t0
+        int m = n;
+        while (m + 1 < n_seqs && cu[m + 1] < t1) ++m;    // last sequence holding a token < t1
+        Chunk c{t0, t1, n, m, -1};
+        if (m > n) {
+            c.cu_off = (int)tab.size();
+            tab.push_back(0);
+            for (int s = n + 1; s <= m; ++s) tab.push_back((int32_t)(cu[s] - t0));
+            tab.push_back((int32_t)(t1 - t0));
+        }
+        out.push_back(c);
+    }
+    return out;
+}
+
+}  // namespace
+
+int64_t staged_scratch_ints(const int32_t *h_cu, int n_seqs, long long T, long long chunk_tokens)
+{
+    if (n_seqs <= 1 || T == 0) return 0;
+    std::vector<int32_t> tab;
+    plan(h_cu, n_seqs, T, chunk_tokens, tab);
+    return (int64_t)tab.size();
+}
+
+int run_prefill_staged(const void *const h_in[5], const int32_t *h_cu, int n_seqs, long long T,
+                       int H, int dtype, int out_dtype, const float *init_state, void *const d_in[5],
+                       void *d_out, void *h_out, float *final_state, int32_t *d_scratch,
+                       long long chunk_tokens, cudaStream_t stream)
+{
+    const size_t esz = dtype == KDA_BF16 ? 2 : 4, osz = out_dtype == KDA_BF16 ? 2 : 4;
+    const size_t row = (size_t)H * 128;                       // elements of a token's q/k/v/g row
+    const size_t blk = (size_t)H * 128 * 128 * sizeof(float);   // one sequence's states
+    // running states: the initial ones (or zeros), overwritten chunk by chunk
+    cudaError_t e = cudaSuccess;
+    if (!init_state)
+        e = cudaMemsetAsync(final_state, 0, blk * n_seqs, stream);
+    else if (init_state != final_state)
+        e = cudaMemcpyAsync(final_state, init_state, blk * n_seqs, cudaMemcpyDeviceToDevice, stream);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    if (T == 0) return KDA_OK;
+    std::vector<int32_t> tab;
+    const std::vector<Chunk> chunks = plan(h_cu, n_seqs, T, chunk_tokens, tab);
+    if (!tab.empty() &&   // pageable source: the call returns once the table has been taken
+        cudaMemcpyAsync(d_scratch, tab.data(), tab.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
+                        stream) != cudaSuccess)
+        return KDA_ERR_CUDA;
+
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    int rc = KDA_OK;
+    auto ok = [&](cudaError_t x) {
+        if (x != cudaSuccess && rc == KDA_OK) rc = KDA_ERR_CUDA;
+        return rc == KDA_OK;
+    };
+    if (!ok(cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking)) ||
+        !ok(cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking)) ||
+        !ok(cudaEventCreateWithFlags(&start, cudaEventDisableTiming)) ||
+        !ok(cudaEventCreateWithFlags(&done, cudaEventDisableTiming)) ||
+        !ok(cudaEventRecord(start, stream)) || !ok(cudaStreamWaitEvent(s_in, start, 0)) ||
+        !ok(cudaStreamWaitEvent(s_out, start, 0))) {
+        // fall through to the clean-up below
+    }
+    for (size_t i = 0; rc == KDA_OK && i < chunks.size(); ++i) {
+        const Chunk &c = chunks[i];
+        const size_t rows = (size_t)(c.t1 - c.t0);
+        cudaEvent_t landed = nullptr, computed = nullptr;
+        if (!ok(cudaEventCreateWithFlags(&landed, cudaEventDisableTiming)) ||
+            !ok(cudaEventCreateWithFlags(&computed, cudaEventDisableTiming)))
+            break;
+        // inputs of the chunk: q, k, v, g rows, then beta
+        for (int x = 0; x < 5 && rc == KDA_OK; ++x) {
+            const size_t w = (x < 4 ? row : (size_t)H) * esz;
+            ok(cudaMemcpyAsync(static_cast<char *>(d_in[x]) + c.t0 * w, static_cast<const char *>(h_in[x]) + c.t0 * w,
+                               rows * w, cudaMemcpyHostToDevice, s_in));
+        }
+        ok(cudaEventRecord(landed, s_in));
+        ok(cudaStreamWaitEvent(stream, landed, 0));
+        if (rc == KDA_OK) {
+            const int n_sub = c.n_b - c.n_a + 1;
+            void *p[5];
+            for (int x = 0; x < 5; ++x)
+                p[x] = static_cast<char *>(d_in[x]) + c.t0 * (x < 4 ? row : (size_t)H) * esz;
+            float *st = final_state + (size_t)c.n_a * H * 128 * 128;
+            const int r = kda_prefill(p[0], p[1], p[2], p[3], p[4],
+                                      c.cu_off < 0 ? nullptr : d_scratch + c.cu_off, n_sub,
+                                      (int64_t)rows, H, 128, 128, dtype, out_dtype, st,
+                                      static_cast<char *>(d_out) + c.t0 * row * osz, st, 0, nullptr,
+                                      stream);
+            if (r != KDA_OK) rc = r;
+        }
+        ok(cudaEventRecord(computed, stream));
+        ok(cudaStreamWaitEvent(s_out, computed, 0));
+        ok(cudaMemcpyAsync(static_cast<char *>(h_out) + c.t0 * row * osz,
+                           static_cast<const char *>(d_out) + c.t0 * row * osz, rows * row * osz,
+                           cudaMemcpyDeviceToHost, s_out));
+        cudaEventDestroy(landed);     // released once recorded work completes
+        cudaEventDestroy(computed);
+    }
+    // the caller's stream continues after the last download
+    if (done && s_out) {
+        ok(cudaEventRecord(done, s_out));
+        ok(cudaStreamWaitEvent(stream, done, 0));
+    }
+    if (start) cudaEventDestroy(start);
+    if (done) cudaEventDestroy(done);
+    if (s_in) cudaStreamDestroy(s_in);   // destroyed once their queued work completes
+    if (s_out) cudaStreamDestroy(s_out);
+    return rc;
+}
+
+}  // namespace kda

@@ -155,3 +155,41 @@ def test_output_gate_rejects(lib):
     assert f(A, 1, A + 16, 0, A, 0, 8, None) == 1                 # in place with another dtype
     assert f(None, 1, A + 16, 0, A + 32, 0, 8, None) == 1
     assert f(A + 4, 1, A + 16, 0, A + 32, 0, 8, None) == 3
+
+
+def test_staged_scratch_sizes(lib):
+    import numpy as np
+
+    cu = np.array([0, 300, 301, 301, 1001, 1051], dtype=np.int32)
+    # chunks of 128: [256, 384) holds sequences 0..3 (5 entries), [896, 1024) sequences 3..4 (3)
+    assert lib.kda_prefill_staged_scratch(cu.ctypes.data, 5, 1051, 128) == 8
+    assert lib.kda_prefill_staged_scratch(None, 1, 1051, 128) == 0
+    assert lib.kda_prefill_staged_scratch(None, 2, 10, 128) == -1      # two sequences need a table
+    assert lib.kda_prefill_staged_scratch(cu.ctypes.data, 5, 1051, 0) == -1
+
+
+def _staged(lib, cu=None, n=1, T=64, scratch=None, scratch_ints=0, **over):
+    args = dict(init=None, fin=A + 8192, dtype=0, odt=1, chunk=32)
+    args.update(over)
+    h = [A + 16 * i for i in range(5)]
+    d = [A + 4096 + 16 * i for i in range(6)]
+    return lib.kda_prefill_staged(*h, cu, n, T, 2, args["dtype"], args["odt"], args["init"], *d,
+                                  A + 2048, args["fin"], scratch, scratch_ints, args["chunk"], None)
+
+
+def test_staged_rejects(lib):
+    import numpy as np
+
+    bad0 = np.array([1, 10, 64], dtype=np.int32)          # does not start at 0
+    down = np.array([0, 40, 30, 64], dtype=np.int32)      # decreasing
+    short = np.array([0, 10, 60], dtype=np.int32)         # does not end at T
+    assert _staged(lib, bad0.ctypes.data, 2) == 1
+    assert _staged(lib, down.ctypes.data, 3) == 1
+    assert _staged(lib, short.ctypes.data, 2) == 1
+    assert _staged(lib, None, 2) == 1                      # two sequences need the host table
+    ok = np.array([0, 10, 64], dtype=np.int32)
+    assert _staged(lib, ok.ctypes.data, 2, scratch=None) == 1          # scratch needed
+    assert _staged(lib, ok.ctypes.data, 2, scratch=A + 8192 * 4, scratch_ints=1) == 1   # too little
+    assert _staged(lib, fin=None) == 1                     # final_state carries the states
+    assert _staged(lib, chunk=0) == 1
+    assert _staged(lib, fin=A + 8196) == 3
