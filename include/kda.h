@@ -224,6 +224,22 @@ int64_t kda_prefill_staged_scratch(const int32_t *h_cu_seqlens, int32_t n_seqs, 
                                    int64_t chunk_tokens);
 
 /*
+ * kda_prefill_staged_static -- kda_prefill_staged without caller scratch: the chunks' sequence
+ * tables go to a fixed device array of the library (2^20 int32 entries per device, a file-scope
+ * __device__ array), so the caller provides no scratch and the library allocates nothing.  Calls
+ * share that array: each call's `stream` first waits for the previous call's last prefill, so
+ * calls from several streams or threads are safe and run one after another on the device.
+ * Arguments and errors as for kda_prefill_staged; KDA_ERR_INVALID_ARG also when the tables need
+ * more than 2^20 entries (kda_prefill_staged_scratch tells).
+ */
+int kda_prefill_staged_static(const void *h_q, const void *h_k, const void *h_v, const void *h_g,
+                              const void *h_beta, const int32_t *h_cu_seqlens, int32_t n_seqs,
+                              int64_t total_tokens, int32_t n_heads, int32_t dtype, int32_t out_dtype,
+                              const float *init_state, void *d_q, void *d_k, void *d_v, void *d_g,
+                              void *d_beta, void *d_out, void *h_out, float *final_state,
+                              int64_t chunk_tokens, void *stream);
+
+/*
  * kda_cp_combine -- the scan of a context-parallel prefill.
  *
  * The recurrence above is affine in the state: per token S_t = A_t S_(t-1) + beta_t k_t v_t^T with

@@ -221,15 +221,15 @@ def output_gate(o, z, *, out=None, out_dtype=None, stream=None):
 
 def prefill_staged(h_q, h_k, h_v, h_g, h_beta, h_cu_seqlens=None, init_state=None, *,
                    device=None, chunk_tokens: int = 1024, buffers=None, h_out=None,
-                   final_state=None, out_dtype=torch.float32, stream=None):
+                   final_state=None, out_dtype=torch.float32, stream=None, static_tables=False):
     """kda_prefill from pinned host memory with the copies overlapped (kda_prefill_staged).
 
     h_q, h_k, h_v, h_g: pinned CPU [T, H, 128]; h_beta: pinned CPU [T, H] (one dtype, bf16 or
     fp32); h_cu_seqlens: CPU int32 [N+1] (or a list) or None for one sequence; init_state: device
     fp32 [N, H, 128, 128] or None.  `buffers` (device staging, returned, reusable across calls),
     `h_out` (pinned CPU [T, H, 128]) and `final_state` are allocated when not passed.  The work is
-    enqueued on `stream`; synchronise it before reading h_out.  Returns (h_out, final_state,
-    buffers)."""
+    enqueued on `stream`; synchronise it before reading h_out.  static_tables=True takes
+    kda_prefill_staged_static (no caller scratch).  Returns (h_out, final_state, buffers)."""
     import numpy as np
 
     lib = _lib.load()
@@ -268,13 +268,17 @@ def prefill_staged(h_q, h_k, h_v, h_g, h_beta, h_cu_seqlens=None, init_state=Non
         buffers = {k: torch.empty_like(t, device=dev) for k, t in
                    (("q", h_q), ("k", h_k), ("v", h_v), ("g", h_g), ("beta", h_beta))}
         buffers["out"] = torch.empty((T, H, D), device=dev, dtype=out_dtype)
+    head = [_ptr(h_q), _ptr(h_k), _ptr(h_v), _ptr(h_g), _ptr(h_beta), cu_ptr, n, T, H, _DTYPES[dtype],
+            _DTYPES[out_dtype], _ptr(init_state)] + \
+        [_ptr(buffers[k]) for k in ("q", "k", "v", "g", "beta", "out")] + [_ptr(h_out), _ptr(final_state)]
+    if static_tables:   # the library's own table array: no scratch from the caller
+        rc = lib.kda_prefill_staged_static(*head, int(chunk_tokens), _stream(dev, stream))
+        _lib.check(rc, "kda_prefill_staged_static")
+        return h_out, final_state, buffers
     if "scratch" not in buffers or buffers["scratch"].numel() < need:
         buffers["scratch"] = torch.empty(max(need, 1), device=dev, dtype=torch.int32)
-    rc = lib.kda_prefill_staged(
-        _ptr(h_q), _ptr(h_k), _ptr(h_v), _ptr(h_g), _ptr(h_beta), cu_ptr, n, T, H, _DTYPES[dtype],
-        _DTYPES[out_dtype], _ptr(init_state), *[_ptr(buffers[k]) for k in ("q", "k", "v", "g", "beta", "out")],
-        _ptr(h_out), _ptr(final_state), _ptr(buffers["scratch"]), buffers["scratch"].numel(),
-        int(chunk_tokens), _stream(dev, stream))
+    rc = lib.kda_prefill_staged(*head, _ptr(buffers["scratch"]), buffers["scratch"].numel(),
+                                int(chunk_tokens), _stream(dev, stream))
     _lib.check(rc, "kda_prefill_staged")
     return h_out, final_state, buffers
 

@@ -39,6 +39,8 @@ SIGNATURES = {
     "kda_prefill_staged": (ctypes.c_int, [_vp] * 6 + [_i32, _i64, _i32, _i32, _i32, _vp] + [_vp] * 9
                            + [_i64, _i64, _vp]),
     "kda_prefill_staged_scratch": (ctypes.c_int64, [_vp, _i32, _i64, _i64]),
+    "kda_prefill_staged_static": (ctypes.c_int, [_vp] * 6 + [_i32, _i64, _i32, _i32, _i32, _vp]
+                                  + [_vp] * 8 + [_i64, _vp]),
 }
 
 _LIB = None

@@ -40,6 +40,34 @@ int check_prefill(const void *q, const void *k, const void *v, const void *g, co
     return KDA_OK;
 }
 
+// Validation shared by the two staged entry points (everything but the scratch).
+int check_staged(const void *h_q, const void *h_k, const void *h_v, const void *h_g, const void *h_beta,
+                 const int32_t *h_cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t n_heads,
+                 int32_t dtype, int32_t out_dtype, const float *init_state, void *d_q, void *d_k,
+                 void *d_v, void *d_g, void *d_beta, void *d_out, void *h_out, float *final_state,
+                 int64_t chunk_tokens)
+{
+    if (n_seqs < 0 || total_tokens < 0 || n_heads < 1 || chunk_tokens < 1 || bad_dtype(dtype) ||
+        bad_dtype(out_dtype) || total_tokens > 0x7fffffffLL)
+        return KDA_ERR_INVALID_ARG;
+    if ((total_tokens > 0 && n_seqs == 0) || (n_seqs > 0 && !final_state) || (n_seqs > 1 && !h_cu_seqlens))
+        return KDA_ERR_INVALID_ARG;
+    const void *host_in[] = {h_q, h_k, h_v, h_g, h_beta, h_out};
+    const void *dev_buf[] = {d_q, d_k, d_v, d_g, d_beta, d_out};
+    for (int i = 0; i < 6; ++i)
+        if (total_tokens > 0 && (!host_in[i] || !dev_buf[i])) return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {h_q, h_k, h_v, h_g, h_beta, h_out, d_q, d_k, d_v, d_g, d_beta, d_out,
+                          init_state, final_state};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+    if (n_seqs > 1) {   // the host table is checked in full here
+        if (h_cu_seqlens[0] != 0 || h_cu_seqlens[n_seqs] != total_tokens) return KDA_ERR_INVALID_ARG;
+        for (int n = 0; n < n_seqs; ++n)
+            if (h_cu_seqlens[n + 1] < h_cu_seqlens[n]) return KDA_ERR_INVALID_ARG;
+    }
+    return KDA_OK;
+}
+
 bool tc_supported(int32_t d_k, int32_t d_v, int32_t dtype)
 {
     return dtype == KDA_BF16 && d_k == 128 && d_v == 128;
@@ -207,24 +235,11 @@ int kda_prefill_staged(const void *h_q, const void *h_k, const void *h_v, const 
                        void *d_beta, void *d_out, void *h_out, float *final_state,
                        int32_t *d_scratch, int64_t scratch_ints, int64_t chunk_tokens, void *stream)
 {
-    if (n_seqs < 0 || total_tokens < 0 || n_heads < 1 || chunk_tokens < 1 || bad_dtype(dtype) ||
-        bad_dtype(out_dtype) || total_tokens > 0x7fffffffLL)
-        return KDA_ERR_INVALID_ARG;
-    if ((total_tokens > 0 && n_seqs == 0) || (n_seqs > 0 && !final_state) || (n_seqs > 1 && !h_cu_seqlens))
-        return KDA_ERR_INVALID_ARG;
-    const void *host_in[] = {h_q, h_k, h_v, h_g, h_beta, h_out};
-    const void *dev_buf[] = {d_q, d_k, d_v, d_g, d_beta, d_out};
-    for (int i = 0; i < 6; ++i)
-        if (total_tokens > 0 && (!host_in[i] || !dev_buf[i])) return KDA_ERR_INVALID_ARG;
-    const void *ptrs[] = {h_q, h_k, h_v, h_g, h_beta, h_out, d_q, d_k, d_v, d_g, d_beta, d_out,
-                          init_state, final_state, d_scratch};
-    for (const void *p : ptrs)
-        if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
-    if (n_seqs > 1) {   // the host table is checked in full here
-        if (h_cu_seqlens[0] != 0 || h_cu_seqlens[n_seqs] != total_tokens) return KDA_ERR_INVALID_ARG;
-        for (int n = 0; n < n_seqs; ++n)
-            if (h_cu_seqlens[n + 1] < h_cu_seqlens[n]) return KDA_ERR_INVALID_ARG;
-    }
+    int rc = check_staged(h_q, h_k, h_v, h_g, h_beta, h_cu_seqlens, n_seqs, total_tokens, n_heads,
+                          dtype, out_dtype, init_state, d_q, d_k, d_v, d_g, d_beta, d_out, h_out,
+                          final_state, chunk_tokens);
+    if (rc != KDA_OK) return rc;
+    if (d_scratch && !aligned16(d_scratch)) return KDA_ERR_MISALIGNED;
     const int64_t need = staged_scratch_ints(h_cu_seqlens, n_seqs, total_tokens, chunk_tokens);
     if (need > 0 && (!d_scratch || scratch_ints < need)) return KDA_ERR_INVALID_ARG;
     const void *h_in[5] = {h_q, h_k, h_v, h_g, h_beta};
@@ -232,6 +247,24 @@ int kda_prefill_staged(const void *h_q, const void *h_k, const void *h_v, const 
     return run_prefill_staged(h_in, h_cu_seqlens, n_seqs, total_tokens, n_heads, dtype, out_dtype,
                               init_state, d_in, d_out, h_out, final_state, d_scratch, chunk_tokens,
                               (cudaStream_t)stream);
+}
+
+int kda_prefill_staged_static(const void *h_q, const void *h_k, const void *h_v, const void *h_g,
+                              const void *h_beta, const int32_t *h_cu_seqlens, int32_t n_seqs,
+                              int64_t total_tokens, int32_t n_heads, int32_t dtype, int32_t out_dtype,
+                              const float *init_state, void *d_q, void *d_k, void *d_v, void *d_g,
+                              void *d_beta, void *d_out, void *h_out, float *final_state,
+                              int64_t chunk_tokens, void *stream)
+{
+    int rc = check_staged(h_q, h_k, h_v, h_g, h_beta, h_cu_seqlens, n_seqs, total_tokens, n_heads,
+                          dtype, out_dtype, init_state, d_q, d_k, d_v, d_g, d_beta, d_out, h_out,
+                          final_state, chunk_tokens);
+    if (rc != KDA_OK) return rc;
+    const void *h_in[5] = {h_q, h_k, h_v, h_g, h_beta};
+    void *d_in[5] = {d_q, d_k, d_v, d_g, d_beta};
+    return run_prefill_staged_static(h_in, h_cu_seqlens, n_seqs, total_tokens, n_heads, dtype,
+                                     out_dtype, init_state, d_in, d_out, h_out, final_state,
+                                     chunk_tokens, (cudaStream_t)stream);
 }
 
 int kda_diag_device_timeout(int64_t timeout_cycles, void *stream)

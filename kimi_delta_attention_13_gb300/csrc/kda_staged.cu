@@ -6,12 +6,20 @@
 // "Kimi K3 im Detail", section "Sequenz-Mixing: KDA-Zustand und globale MLA"), and its outputs go
 // device -> host on a second internal stream.  Chunk c+1's upload therefore overlaps chunk c's
 // prefill and chunk c-1's download, and both copy directions run at once.
+#include <mutex>
 #include <vector>
 
 #include "kda_internal.cuh"
 
 namespace kda {
 namespace {
+
+// Sequence tables of kda_prefill_staged_static: a fixed device array instead of caller scratch.
+// Calls share it, so each call's stream first waits for the previous call's last read of it.
+constexpr int64_t kStaticTableInts = 1 << 20;
+static __device__ __align__(256) int32_t g_staged_tables[kStaticTableInts];
+std::mutex g_tables_mu;
+cudaEvent_t g_tables_free[64] = {};   // per device: recorded after the last call that read the table
 
 struct Chunk {
     long long t0, t1;   // token range
@@ -135,6 +143,34 @@ int run_prefill_staged(const void *const h_in[5], const int32_t *h_cu, int n_seq
     if (done) cudaEventDestroy(done);
     if (s_in) cudaStreamDestroy(s_in);   // destroyed once their queued work completes
     if (s_out) cudaStreamDestroy(s_out);
+    return rc;
+}
+
+int run_prefill_staged_static(const void *const h_in[5], const int32_t *h_cu, int n_seqs, long long T,
+                              int H, int dtype, int out_dtype, const float *init_state,
+                              void *const d_in[5], void *d_out, void *h_out, float *final_state,
+                              long long chunk_tokens, cudaStream_t stream)
+{
+    if (staged_scratch_ints(h_cu, n_seqs, T, chunk_tokens) > kStaticTableInts) return KDA_ERR_INVALID_ARG;
+    int dev = 0;
+    void *tables = nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 ||
+        cudaGetSymbolAddress(&tables, g_staged_tables) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_tables_mu);
+    cudaEvent_t &free_ev = g_tables_free[dev];
+    if (!free_ev && cudaEventCreateWithFlags(&free_ev, cudaEventDisableTiming) != cudaSuccess) {
+        free_ev = nullptr;
+        return KDA_ERR_CUDA;
+    }
+    // the table upload below is ordered after the previous call's prefills (a fresh event counts
+    // as complete)
+    if (cudaStreamWaitEvent(stream, free_ev, 0) != cudaSuccess) return KDA_ERR_CUDA;
+    const int rc = run_prefill_staged(h_in, h_cu, n_seqs, T, H, dtype, out_dtype, init_state, d_in,
+                                      d_out, h_out, final_state, static_cast<int32_t *>(tables),
+                                      chunk_tokens, stream);
+    // `stream` is ordered after this call's last prefill (and download)
+    if (cudaEventRecord(free_ev, stream) != cudaSuccess && rc == KDA_OK) return KDA_ERR_CUDA;
     return rc;
 }
 
