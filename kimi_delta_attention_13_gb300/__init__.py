@@ -242,8 +242,8 @@ def prefill_staged(h_q, h_k, h_v, h_g, h_beta, h_cu_seqlens=None, init_state=Non
         raise ValueError("the staged prefill takes d_k = d_v = 128")
     for t, name, shp in ((h_q, "h_q", (T, H, D)), (h_k, "h_k", (T, H, D)), (h_v, "h_v", (T, H, D)),
                          (h_g, "h_g", (T, H, D)), (h_beta, "h_beta", (T, H))):
-        if t.device.type != "cpu" or not t.is_pinned() or not t.is_contiguous() or t.dtype != dtype \
-                or tuple(t.shape) != shp:
+        if t.device.type != "cpu" or (t.numel() and not t.is_pinned()) or not t.is_contiguous() \
+                or t.dtype != dtype or tuple(t.shape) != shp:
             raise ValueError(f"{name} must be a pinned, contiguous CPU tensor {shp} of {dtype}")
     cu = None
     if h_cu_seqlens is not None:
@@ -258,8 +258,8 @@ def prefill_staged(h_q, h_k, h_v, h_g, h_beta, h_cu_seqlens=None, init_state=Non
     _require(final_state, "final_state", dev, torch.float32, (n, H, D, D))
     if h_out is None:
         h_out = torch.empty((T, H, D), dtype=out_dtype).pin_memory()
-    if h_out.device.type != "cpu" or not h_out.is_pinned() or h_out.dtype != out_dtype or \
-            tuple(h_out.shape) != (T, H, D):
+    if h_out.device.type != "cpu" or (h_out.numel() and not h_out.is_pinned()) or \
+            h_out.dtype != out_dtype or tuple(h_out.shape) != (T, H, D):
         raise ValueError("h_out must be a pinned CPU tensor [T, H, 128] of out_dtype")
     need = int(lib.kda_prefill_staged_scratch(cu_ptr, n, T, int(chunk_tokens)))
     if need < 0:

@@ -64,3 +64,13 @@ def test_cp_without_a_split_is_the_plain_prefill(orc):
 def test_cp_long_sequence(orc):
     # 65,536 tokens of 4 heads in 8 segments of 8,192: 32 + 32 CTAs instead of 4
     check(orc, [65536], 4, 8192, True, seed=72)
+
+
+def test_cp_edge_cases(orc):
+    # a single-token sequence next to a long one, and a batch without tokens
+    check(orc, [1, 600], 2, 128, True, seed=73)
+    e = synth.make_inputs([0, 0], heads=2, dtype="bf16", seed=74, device=DEV, init_state=True)
+    out, fin = prefill_cp(e["q"], e["k"], e["v"], e["g"], e["beta"], e["cu_seqlens"], e["state"],
+                          seg_len=64, lengths=[0, 0])
+    torch.cuda.synchronize()
+    assert out.numel() == 0 and torch.equal(fin, e["state"])

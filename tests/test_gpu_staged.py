@@ -59,3 +59,26 @@ def test_varlen_against_oracle(lengths, chunk, out_dtype):
     tol_out = TOL["bf16"]["out"] if out_dtype == torch.float32 else 4e-2
     assert_close("out", out, ro, tol_out)
     assert_close("final_state", fin, rf, TOL["bf16"]["state"])
+
+
+def test_edge_cases():
+    orc = oracle.default()
+    # empty leading and trailing sequences, one chunk larger than all tokens
+    lengths = [0, 37, 0, 90, 0]
+    x = synth.make_inputs(lengths, heads=2, dtype="bf16", seed=85, device=DEV, init_state=True)
+    h = host(x)
+    out, fin, _ = kda.prefill_staged(h["q"], h["k"], h["v"], h["g"], h["beta"], x["cu_seqlens"].cpu(),
+                                     x["state"], chunk_tokens=4096)
+    torch.cuda.synchronize()
+    ro, rf, _ = orc.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"].cpu().long(), x["state"])
+    assert_close("out", out, ro, TOL["bf16"]["out"])
+    assert_close("final_state", fin, rf, TOL["bf16"]["state"])
+    assert torch.equal(fin[0], x["state"][0]) and torch.equal(fin[4], x["state"][4])   # empty: init kept
+    # no tokens at all: the final states are the initial ones
+    e = synth.make_inputs([0, 0], heads=2, dtype="bf16", seed=86, device=DEV, init_state=True)
+    he = host(e)
+    out, fin, _ = kda.prefill_staged(he["q"], he["k"], he["v"], he["g"], he["beta"], e["cu_seqlens"].cpu(),
+                                     e["state"], chunk_tokens=64)
+    torch.cuda.synchronize()
+    assert out.numel() == 0 and torch.equal(fin, e["state"])
+    assert kda.device_status() == 0
