@@ -276,12 +276,14 @@ int kda_diag_device_timeout(int64_t timeout_cycles, void *stream)
 int kda_device_status(int32_t *status, void *stream)
 {
     if (!status) return KDA_ERR_INVALID_ARG;
-    int32_t a = 0, b = 0;
+    int32_t a = 0, b = 0, c = 0;
     int rc = read_and_clear_status_state_copy((cudaStream_t)stream, &a);
     if (rc != KDA_OK) return rc;
     rc = read_and_clear_status_prefill_tc((cudaStream_t)stream, &b);
     if (rc != KDA_OK) return rc;
-    *status = b != KDA_OK ? b : a;
+    rc = read_and_clear_status_decode((cudaStream_t)stream, &c);
+    if (rc != KDA_OK) return rc;
+    *status = b != KDA_OK ? b : (c != KDA_OK ? c : a);
     return KDA_OK;
 }
 

@@ -14,6 +14,7 @@
 // Column sums over i: per-thread partials over its 16 rows, then a cross-warp pass in
 // shared memory.
 #include "kda_internal.cuh"
+#include "sm100_ptx.cuh"
 
 namespace kda {
 namespace {
@@ -124,7 +125,132 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     }
 }
 
+// d_k = d_v = 128: the 64 KB state of a head is one contiguous block, so it moves by one bulk
+// copy each way and is worked on in shared memory.  Registers stay few, three blocks share an SM
+// and up to three states per SM are in flight.
+constexpr uint32_t kStateBytes = 128 * 128 * 4;
+constexpr long long kDecodeTimeout = 2000000000ll;   // SM cycles (~1 s): bounded waits
+
+__device__ int g_decode_error;   // sticky device error word of this translation unit
+
+template <typename T, typename TO>
+__global__ void __launch_bounds__(kThreads)
+decode_bulk_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+                   const T *__restrict__ g, const T *__restrict__ beta, float *__restrict__ state,
+                   TO *__restrict__ out)
+{
+    using namespace ptx;
+    extern __shared__ __align__(128) float sS[];   // S[i][j], 128 x 128, row = key channel
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ float s_k[kMaxDk], s_q[kMaxDk], s_a[kMaxDk], s_v[kMaxDv];
+    __shared__ float s_part[kWarps][kMaxDv];   // one sum's per-warp partials at a time (3 blocks/SM)
+    __shared__ float s_r[2][kMaxDv];
+    __shared__ float s_kq;
+    __shared__ int s_zero;   // the abort flag of the waits: never set, they end by timeout only
+    const int64_t nh = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float *S = state + nh * (int64_t)kMaxDk * kMaxDv;
+    if (tid == 0) {
+        s_zero = 0;
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (tid == 0) {   // the state goes out first: it is the bytes this kernel exists to move
+        mbar_arrive_expect_tx(&bar, kStateBytes);
+        bulk_load_1d(sS, S, kStateBytes, &bar);
+    }
+    if (tid < kMaxDk) {
+        s_k[tid] = to_f32(k[nh * kMaxDk + tid]);
+        s_q[tid] = to_f32(q[nh * kMaxDk + tid]);
+        s_a[tid] = retention(to_f32(g[nh * kMaxDk + tid]));
+        s_v[tid] = to_f32(v[nh * kMaxDv + tid]);
+    }
+    const float b = to_f32(beta[nh]);
+    __syncthreads();
+    if (warp == 0) {  // k . q, needed only for the output
+        float acc = 0.f;
+        for (int i = lane; i < kMaxDk; i += 32) acc += s_k[i] * s_q[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) s_kq = acc;
+    }
+    const bool landed = mbar_wait(&bar, 0, &s_zero, kDecodeTimeout);
+    if (!__syncthreads_and(landed)) {
+        if (tid == 0) {
+            atomicExch(&g_decode_error, KDA_ERR_DEVICE_TIMEOUT);
+            mbar_wait(&bar, 0, &s_zero, kDecodeTimeout);   // no copy left in flight at exit
+        }
+        return;
+    }
+    // decay, then the two column sums S'^T k and S'^T q over this thread's rows i = warp + 8m
+    const float4 *S4 = reinterpret_cast<const float4 *>(sS);
+    float rk[4] = {0.f, 0.f, 0.f, 0.f}, rq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int m = 0; m < kRowsPerWarp; ++m) {
+        const int i = warp + kWarps * m;
+        const float a = s_a[i], ki = s_k[i] * a, qi = s_q[i] * a;
+        const float4 s = S4[i * 32 + lane];
+        rk[0] += s.x * ki; rk[1] += s.y * ki; rk[2] += s.z * ki; rk[3] += s.w * ki;
+        rq[0] += s.x * qi; rq[1] += s.y * qi; rq[2] += s.z * qi; rq[3] += s.w * qi;
+    }
+    // cross-warp sums through one 4 KB buffer: first S'^T k, then S'^T q
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s_part[warp][4 * lane + c] = which ? rq[c] : rk[c];
+        __syncthreads();
+        if (tid < kMaxDv) {
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) acc += s_part[w][tid];
+            s_r[which][tid] = acc;
+        }
+        __syncthreads();
+    }
+    float u[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) u[c] = b * (s_v[4 * lane + c] - s_r[0][4 * lane + c]);
+    if (warp == 0) {
+        const float kq = s_kq;
+        TO *o = out + nh * kMaxDv + 4 * lane;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) store_as(o + c, s_r[1][4 * lane + c] + kq * u[c]);
+    }
+    // S = S' + k u^T in place, then one bulk store back
+    float4 *W4 = reinterpret_cast<float4 *>(sS);
+#pragma unroll 4
+    for (int m = 0; m < kRowsPerWarp; ++m) {
+        const int i = warp + kWarps * m;
+        const float a = s_a[i], ki = s_k[i];
+        float4 s = W4[i * 32 + lane];
+        s.x = fmaf(s.x, a, ki * u[0]); s.y = fmaf(s.y, a, ki * u[1]);
+        s.z = fmaf(s.z, a, ki * u[2]); s.w = fmaf(s.w, a, ki * u[3]);
+        W4[i * 32 + lane] = s;
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        bulk_store_1d(S, sS, kStateBytes);
+        bulk_commit();
+        bulk_wait_read_all();   // the shared-memory source stays until the copy has read it
+    }
+}
+
 }  // namespace
+
+int read_and_clear_status_decode(cudaStream_t s, int32_t *status)
+{
+    int host = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&host, g_decode_error, sizeof(int), 0, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_decode_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    *status = host;
+    return KDA_OK;
+}
 
 int launch_decode(const void *q, const void *k, const void *v, const void *g, const void *beta,
                   float *state, void *out, int n_seqs, int n_heads, int d_k, int d_v, int dtype,
@@ -135,19 +261,31 @@ int launch_decode(const void *q, const void *k, const void *v, const void *g, co
     const int64_t blocks = (int64_t)n_seqs * n_heads;
     if (blocks == 0) return KDA_OK;
     if (blocks > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    const bool bulk = d_k == kMaxDk && d_v == kMaxDv;
+    bool attr_ok = true;
     auto go = [&](auto in_tag, auto out_tag) {
         using T = decltype(in_tag);
         using TO = decltype(out_tag);
-        decode_kernel<T, TO><<<(unsigned)blocks, kThreads, 0, stream>>>(
-            (const T *)q, (const T *)k, (const T *)v, (const T *)g, (const T *)beta, state,
-            (TO *)out, d_k, d_v);
+        if (bulk) {
+            attr_ok = cudaFuncSetAttribute(decode_bulk_kernel<T, TO>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kStateBytes) == cudaSuccess;
+            if (attr_ok)
+                decode_bulk_kernel<T, TO><<<(unsigned)blocks, kThreads, kStateBytes, stream>>>(
+                    (const T *)q, (const T *)k, (const T *)v, (const T *)g, (const T *)beta, state,
+                    (TO *)out);
+        } else {
+            decode_kernel<T, TO><<<(unsigned)blocks, kThreads, 0, stream>>>(
+                (const T *)q, (const T *)k, (const T *)v, (const T *)g, (const T *)beta, state,
+                (TO *)out, d_k, d_v);
+        }
     };
     if (dtype == KDA_BF16) {
         if (out_dtype == KDA_BF16) go(__nv_bfloat16{}, __nv_bfloat16{}); else go(__nv_bfloat16{}, float{});
     } else {
         if (out_dtype == KDA_BF16) go(float{}, __nv_bfloat16{}); else go(float{}, float{});
     }
-    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return (attr_ok && cudaGetLastError() == cudaSuccess) ? KDA_OK : KDA_ERR_CUDA;
 }
 
 }  // namespace kda

@@ -26,6 +26,7 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Per-translation-unit readers of the sticky device error words (see kda_device_status).
 int read_and_clear_status_state_copy(cudaStream_t s, int32_t *status);
 int read_and_clear_status_prefill_tc(cudaStream_t s, int32_t *status);
+int read_and_clear_status_decode(cudaStream_t s, int32_t *status);
 // Launch the one-CTA probe whose bounded device wait expires after `cycles` SM cycles.
 int launch_wait_timeout_probe(long long cycles, cudaStream_t stream);
 

@@ -112,6 +112,24 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// 1-D bulk copy global -> shared of `bytes` (both addresses 16-byte aligned, a multiple of 16
+// bytes), completing that many transaction bytes on `bar`
+__device__ __forceinline__ void bulk_load_1d(void *smem_dst, const void *gmem_src, uint32_t bytes,
+                                             uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(smem_dst)), "l"(__cvta_generic_to_global(gmem_src)), "r"(bytes),
+                   "r"(smem_u32(bar))
+                 : "memory");
+}
+// 1-D bulk copy shared -> global of `bytes` (same alignment rules), in this thread's bulk group
+__device__ __forceinline__ void bulk_store_1d(void *gmem_dst, const void *smem_src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(__cvta_generic_to_global(gmem_dst)), "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+}
 // wait until every committed bulk store of this thread has read its shared-memory source
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // wait until every committed bulk store of this thread has completed
