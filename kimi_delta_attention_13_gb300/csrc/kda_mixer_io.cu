@@ -163,8 +163,9 @@ __global__ void __launch_bounds__(kMixThreads) premix_conv_kernel(const PremixAr
     const bool active = col < HD;
     const long long t0 = (long long)blockIdx.x * kMixTokens;
     const long long t1 = min(t0 + kMixTokens, p.T);
-    const T *x = static_cast<const T *>(p.x[xi]);
-    T *y = static_cast<T *>(p.y[xi]);
+    // pointers picked without indexing the parameter arrays (which would copy them to local memory)
+    const T *x = static_cast<const T *>(xi == 0 ? p.x[0] : xi == 1 ? p.x[1] : p.x[2]);
+    T *y = static_cast<T *>(xi == 0 ? p.y[0] : xi == 1 ? p.y[1] : p.y[2]);
 
     // the sequence holding t0: the last n with cu[n] <= t0 (then cu[n+1] > t0)
     int n = 0;
