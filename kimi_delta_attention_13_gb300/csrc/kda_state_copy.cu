@@ -4,10 +4,13 @@
 // restarts a sequence from a stored KDA state at the same token boundary as the global
 // attention cache; this kernel moves such states between slot arrays:
 //     dst[dst_idx[i]] = src[src_idx[i]],  one slot = H * d_k * d_v fp32.
-// Pure HBM copy: 128-bit streaming loads and stores, four loads in flight per thread ahead of
-// their stores; gridDim.y walks the slots, gridDim.x x blockDim.x threads stride through one slot.  Indices outside their slot range skip the copy and set
-// this unit's sticky error word.
+// Pure HBM copy.  When a slot is a whole number of 16-byte units (always for d_k = d_v = 128), each
+// block moves one 64 KB chunk of a slot by a 1-D bulk copy into shared memory and a bulk store out
+// (three blocks per SM, so up to three chunks per SM in flight).  Otherwise 128-bit or scalar
+// streaming loads and stores, four loads in flight per thread ahead of their stores.  Indices
+// outside their slot range skip the copy and set this unit's sticky error word.
 #include "kda_internal.cuh"
+#include "sm100_ptx.cuh"
 
 namespace kda {
 namespace {
@@ -43,6 +46,44 @@ state_copy_kernel(V *__restrict__ dst, const int64_t *__restrict__ dst_idx, int6
     }
 }
 
+constexpr uint32_t kChunkBytes = 65536;
+constexpr long long kCopyTimeout = 2000000000ll;   // SM cycles (~1 s): bounded waits
+
+// block b copies chunk b % chunks of slot pair b / chunks; lane 0 of the one warp does the work
+__global__ void __launch_bounds__(32)
+state_copy_bulk_kernel(char *__restrict__ dst, const int64_t *__restrict__ dst_idx, int64_t n_dst,
+                       const char *__restrict__ src, const int64_t *__restrict__ src_idx,
+                       int64_t n_src, int64_t unit_bytes, int64_t chunks)
+{
+    using namespace ptx;
+    extern __shared__ __align__(128) uint8_t buf[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int s_zero;   // the abort flag of the waits: never set, they end by timeout only
+    if (threadIdx.x != 0) return;
+    const int64_t i = (int64_t)blockIdx.x / chunks, c = (int64_t)blockIdx.x % chunks;
+    const int64_t d = dst_idx ? dst_idx[i] : i;
+    const int64_t s = src_idx ? src_idx[i] : i;
+    if (d < 0 || d >= n_dst || s < 0 || s >= n_src) {
+        if (c == 0) atomicExch(&g_state_copy_error, KDA_ERR_INDEX_RANGE);
+        return;
+    }
+    const int64_t off = c * kChunkBytes;
+    const uint32_t bytes = (uint32_t)(unit_bytes - off < kChunkBytes ? unit_bytes - off : kChunkBytes);
+    s_zero = 0;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(&bar, bytes);
+    bulk_load_1d(buf, src + s * unit_bytes + off, bytes, &bar);
+    if (!mbar_wait(&bar, 0, &s_zero, kCopyTimeout)) {
+        atomicExch(&g_state_copy_error, KDA_ERR_DEVICE_TIMEOUT);
+        mbar_wait(&bar, 0, &s_zero, kCopyTimeout);   // no copy left in flight at exit
+        return;
+    }
+    bulk_store_1d(dst + d * unit_bytes + off, buf, bytes);
+    bulk_commit();
+    bulk_wait_read_all();   // the shared-memory source stays until the copy has read it
+}
+
 }  // namespace
 
 int read_and_clear_status_state_copy(cudaStream_t s, int32_t *status)
@@ -68,7 +109,15 @@ int launch_state_copy(float *dst, const int64_t *dst_idx, int64_t n_dst, const f
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const unsigned ys = (unsigned)(n < 65535 ? n : 65535);
-    if (unit_floats % 4 == 0) {
+    const int64_t unit_bytes = unit_floats * 4, chunks = (unit_bytes + kChunkBytes - 1) / kChunkBytes;
+    if (unit_floats % 4 == 0 && n * chunks <= 0x7fffffffLL) {
+        if (cudaFuncSetAttribute(state_copy_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kChunkBytes) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        state_copy_bulk_kernel<<<(unsigned)(n * chunks), 32, kChunkBytes, stream>>>(
+            reinterpret_cast<char *>(dst), dst_idx, n_dst, reinterpret_cast<const char *>(src), src_idx,
+            n_src, unit_bytes, chunks);
+    } else if (unit_floats % 4 == 0) {
         const int64_t vecs = unit_floats / 4;
         // enough blocks per slot that every SM is fully occupied (8 blocks of 256 threads)
         int64_t bx = (8LL * sms + ys - 1) / ys;
