@@ -40,7 +40,7 @@ BYTES_PER_TOKEN_HEAD = 4 * D * 2 + 2 + D * 4        # q, k, v, g bf16 + beta bf1
 STATE_BYTES = D * D * 4                             # 65,536 per (sequence, head)
 DECODE_BYTES_PER_SEQ_HEAD = 2 * STATE_BYTES + 4 * D * 2 + 2 + D * 4   # 132,610
 PREMIX_BYTES_PER_TOKEN_HEAD = 2 * (4 * D * 2 + 2)    # xq, xk, xv, a, b in; q, k, v, g, beta out: 2,052
-E2E_CHUNK = 512                # tokens per chunk of the staged (copy-overlapped) end-to-end prefill
+E2E_CHUNK = 1024               # tokens per chunk of the staged (copy-overlapped) end-to-end prefill
 
 
 def set_heads(heads: int) -> None:

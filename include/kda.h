@@ -193,16 +193,21 @@ int kda_output_gate(const void *o, int32_t o_dtype, const void *z, int32_t z_dty
  * host memory.  The packed tokens are cut into chunks of `chunk_tokens`: chunk c's inputs are
  * copied host -> device on one internal stream, prefilled on `stream` (every sequence resumes
  * from its running state in final_state, as the recurrence hands the state on from token to
- * token), and its outputs copied device -> host on a second internal stream, so uploads,
- * prefills and downloads of neighbouring chunks overlap.  When the call returns, all of it is
- * enqueued and `stream` is ordered after the last download.
+ * token), and its outputs moved device -> host on a second internal stream, so uploads,
+ * prefills and downloads of neighbouring chunks overlap.  When chunk_tokens is a multiple of 32,
+ * the last chunk is cut in halves (multiples of 32 tokens) down to at most 128 tokens, which
+ * shortens the work left after the last upload.  Downloads into pinned host memory are SM
+ * stores through its device mapping (a 64-block kernel beside the prefill); into other
+ * host memory they are copies.  When the call returns, all of it is enqueued and `stream` is
+ * ordered after the last download.
  *
  *   h_q, h_k, h_v, h_g, h_beta   pinned host inputs, layouts and `dtype` as for kda_prefill.
  *   h_cu_seqlens     HOST int32 [n_seqs + 1] (checked here: 0, non-decreasing, total_tokens),
  *                    or NULL when n_seqs == 1.
  *   init_state       device fp32 [n_seqs, H, 128, 128] or NULL (zeros); may alias final_state.
  *   d_q .. d_beta, d_out   device buffers of the inputs' / outputs' full size (staging).
- *   h_out            pinned host [total_tokens, H, 128] outputs (`out_dtype`).
+ *   h_out            host [total_tokens, H, 128] outputs (`out_dtype`), pinned for speed
+ *                    (pageable memory works, with copy-engine downloads).
  *   final_state      device fp32 [n_seqs, H, 128, 128] (required: it carries the states).
  *   d_scratch        device int32 [scratch_ints] for the chunks' sequence tables, at least
  *                    kda_prefill_staged_scratch(...) entries (0 for a single sequence).

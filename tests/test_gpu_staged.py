@@ -82,3 +82,29 @@ def test_edge_cases():
     torch.cuda.synchronize()
     assert out.numel() == 0 and torch.equal(fin, e["state"])
     assert kda.device_status() == 0
+
+
+def test_tail_split_and_pageable_output():
+    # 1000 tokens in chunks of 512: the last 488 are cut into 256 + 128 + 104; outputs are
+    # downloaded by SM stores into the pinned buffer, and by copies into a pageable one.
+    x = synth.make_inputs([1000], heads=3, dtype="bf16", seed=87, device=DEV, init_state=True)
+    ref_o, ref_f, _ = kda.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], None, x["state"])
+    h = host(x)
+    out, fin, bufs = kda.prefill_staged(h["q"], h["k"], h["v"], h["g"], h["beta"], None, x["state"],
+                                        chunk_tokens=512)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_o.cpu()) and torch.equal(fin, ref_f)
+
+    lib = kda._lib.load()
+    pageable = torch.full((1000, 3, 128), float("nan"))
+    assert not pageable.is_pinned()
+    fin2 = torch.empty_like(ref_f)
+    rc = lib.kda_prefill_staged(
+        kda._ptr(h["q"]), kda._ptr(h["k"]), kda._ptr(h["v"]), kda._ptr(h["g"]), kda._ptr(h["beta"]),
+        None, 1, 1000, 3, kda._DTYPES[torch.bfloat16], kda._DTYPES[torch.float32], kda._ptr(x["state"]),
+        *[kda._ptr(bufs[k]) for k in ("q", "k", "v", "g", "beta", "out")], kda._ptr(pageable),
+        kda._ptr(fin2), None, 0, 512, kda._stream(DEV, None))
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert torch.equal(pageable, ref_o.cpu()) and torch.equal(fin2, ref_f)
+    assert kda.device_status() == 0
