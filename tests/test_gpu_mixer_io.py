@@ -76,6 +76,13 @@ def run_premix(orc, x, dtype, heads=None):
     ("f32", [33], 1, 16, True),
     ("f32", [40, 40], 3, 32, True),
     ("f32", [17, 2], 9, 256, True),                 # 2304 channels: three channel blocks
+    # bf16 with H*d a multiple of 1024: the bulk-staged convolution
+    ("bf16", [100, 1, 37, 2, 64], 8, 128, False),
+    ("bf16", [127, 1, 129, 3], 8, 128, True),       # sequence edges next to chunk and stage edges
+    ("bf16", [0, 5, 0, 40, 0], 16, 64, True),       # empty sequences
+    ("bf16", [300], 4, 256, True),                  # last chunk of 44 tokens: a partial stage
+    ("bf16", [77, 200], 32, 64, False),             # two channel blocks
+    ("bf16", [20, 13], 128, 8, True),               # one thread per head
 ])
 def test_premix_parity(orc, dtype, lengths, H, d, hist):
     x = synth.make_premix_inputs(lengths, heads=H, d=d, dtype=dtype, seed=sum(lengths) + H + d,
