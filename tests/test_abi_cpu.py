@@ -166,6 +166,13 @@ def test_staged_scratch_sizes(lib):
     assert lib.kda_prefill_staged_scratch(None, 1, 1051, 128) == 0
     assert lib.kda_prefill_staged_scratch(None, 2, 10, 128) == -1      # two sequences need a table
     assert lib.kda_prefill_staged_scratch(cu.ctypes.data, 5, 1051, 0) == -1
+    # the last chunk is cut in halves down to 128 tokens: T = 1000 in chunks of 512 becomes
+    # [0, 512) [512, 768) [768, 896) [896, 1000); with sequences [0, 700) [700, 800) [800, 1000)
+    # the 2nd and 3rd chunks each hold two sequences (3 entries each), against one 4-entry table
+    # for an unsplit [512, 1000)
+    cu3 = np.array([0, 700, 800, 1000], dtype=np.int32)
+    assert lib.kda_prefill_staged_scratch(cu3.ctypes.data, 3, 1000, 512) == 6
+    assert lib.kda_prefill_staged_scratch(cu3.ctypes.data, 3, 1000, 500) == 4   # not a multiple of 32
 
 
 def _staged(lib, cu=None, n=1, T=64, scratch=None, scratch_ints=0, **over):
