@@ -43,8 +43,11 @@ class CheckpointStore:
         slot = self._next
         self._next = (self._next + 1) % self.n_slots
         old = self._owner[slot]
-        if old is not None:
+        if old is not None and self._index.get(old) == slot:
             del self._index[old]
+        prev = self._index.get(entry)
+        if prev is not None:   # the same checkpoint stored again: its older slot is superseded
+            self._owner[prev] = None
         self._owner[slot] = entry
         self._index[entry] = slot
         return slot
