@@ -98,11 +98,18 @@ def _prefill(fn_name, q, k, v, g, beta, cu_seqlens, init_state, out, final_state
         final_state = None
     else:
         _require(final_state, "final_state", dev, torch.float32, (n, H, dk, dv))
-    if ckpt_stride and ckpts is None:
+    if lengths is not None and (len(lengths) != n or sum(int(L) for L in lengths) != T):
+        raise ValueError(f"lengths must hold {n} sequence lengths adding up to {T}")
+    if ckpt_stride:
         if lengths is None:  # host read of the lengths (synchronizes); pass `lengths` to avoid it
             lengths = [T] if cu_seqlens is None else torch.diff(cu_seqlens).tolist()
         slots = num_checkpoints(lengths, ckpt_stride)
-        ckpts = torch.empty((slots, H, dk, dv), device=dev, dtype=torch.float32)
+        if ckpts is None:
+            ckpts = torch.empty((slots, H, dk, dv), device=dev, dtype=torch.float32)
+        else:   # the kernel writes every slot the sequences reach: a smaller buffer would overflow
+            _require(ckpts, "ckpts", dev, torch.float32)
+            if ckpts.dim() != 4 or tuple(ckpts.shape[1:]) != (H, dk, dv) or ckpts.shape[0] < slots:
+                raise ValueError(f"ckpts must be [>= {slots}, {H}, {dk}, {dv}] (got {tuple(ckpts.shape)})")
     elif ckpts is not None:
         _require(ckpts, "ckpts", dev, torch.float32)
     if ckpts is not None and ckpts.numel() == 0:

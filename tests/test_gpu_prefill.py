@@ -153,6 +153,32 @@ def test_empty_batches():
     assert torch.count_nonzero(fin) == 0
 
 
+def test_checkpoint_buffer_and_lengths_are_checked(orc):
+    # the kernel writes every checkpoint slot the sequences reach, so the binding refuses a
+    # smaller buffer, and lengths that do not describe cu_seqlens, before anything is enqueued
+    x = synth.make_inputs([100, 200], heads=2, dtype="bf16", seed=27, device=DEV)
+    args = (x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"])
+    small = torch.full((2, 2, 128, 128), float("nan"), device=DEV)   # 1 + 3 slots needed
+    with pytest.raises(ValueError):
+        kda.prefill(*args, ckpt_stride=64, ckpts=small)
+    with pytest.raises(ValueError):
+        kda.prefill(*args, ckpt_stride=64, ckpts=torch.empty(4, 2, 128, 64, device=DEV))
+    with pytest.raises(ValueError):
+        kda.prefill(*args, ckpt_stride=64, lengths=[100, 100])
+    with pytest.raises(ValueError):
+        kda.prefill(*args, lengths=[300])
+    torch.cuda.synchronize()
+    assert torch.isnan(small).all()
+    # a larger buffer is fine: the slots past the last checkpoint stay untouched
+    big = torch.full((6, 2, 128, 128), float("nan"), device=DEV)
+    _, _, ck = kda.prefill(*args, ckpt_stride=64, ckpts=big, lengths=[100, 200])
+    torch.cuda.synchronize()
+    assert ck is big and not torch.isnan(big[:4]).any() and torch.isnan(big[4:]).all()
+    _, _, rc = orc.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"].cpu(), None,
+                           ckpt_stride=64)
+    assert_close("ckpts", big[:4], rc, TOL["bf16"]["state"])
+
+
 # --- full-size workloads, in the benchmark's launch configuration ---------------------------------
 
 def test_workload_prefill_T8192_all_heads(orc):
