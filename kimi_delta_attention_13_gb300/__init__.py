@@ -275,6 +275,13 @@ def prefill_staged(h_q, h_k, h_v, h_g, h_beta, h_cu_seqlens=None, init_state=Non
         buffers = {k: torch.empty_like(t, device=dev) for k, t in
                    (("q", h_q), ("k", h_k), ("v", h_v), ("g", h_g), ("beta", h_beta))}
         buffers["out"] = torch.empty((T, H, D), device=dev, dtype=out_dtype)
+    else:   # staging buffers of an earlier call: they must hold this call's tokens
+        for key, ref, dt in (("q", h_q, dtype), ("k", h_k, dtype), ("v", h_v, dtype),
+                             ("g", h_g, dtype), ("beta", h_beta, dtype), ("out", h_out, out_dtype)):
+            buf = buffers.get(key)
+            _require(buf, f"buffers[{key!r}]", dev, dt)
+            if buf.numel() < ref.numel():
+                raise ValueError(f"buffers[{key!r}] holds {buf.numel()} elements, {ref.numel()} needed")
     head = [_ptr(h_q), _ptr(h_k), _ptr(h_v), _ptr(h_g), _ptr(h_beta), cu_ptr, n, T, H, _DTYPES[dtype],
             _DTYPES[out_dtype], _ptr(init_state)] + \
         [_ptr(buffers[k]) for k in ("q", "k", "v", "g", "beta", "out")] + [_ptr(h_out), _ptr(final_state)]
@@ -305,6 +312,10 @@ def state_copy(dst, src, dst_idx=None, src_idx=None, n: Optional[int] = None, st
     if n is None:
         n = (dst_idx.numel() if dst_idx is not None else
              src_idx.numel() if src_idx is not None else min(dst.shape[0], src.shape[0]))
+    # the kernel reads n entries of each index array (whose length the C call does not take)
+    for t, name in ((dst_idx, "dst_idx"), (src_idx, "src_idx")):
+        if t is not None and int(n) > t.numel():
+            raise ValueError(f"n = {n} exceeds the {t.numel()} entries of {name}")
     _, H, dk, dv = dst.shape
     rc = lib.kda_state_copy(_ptr(dst), _ptr(dst_idx), dst.shape[0], _ptr(src), _ptr(src_idx),
                             src.shape[0], int(n), H, dk, dv, _stream(dev, stream))

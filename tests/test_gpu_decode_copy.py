@@ -104,6 +104,19 @@ def test_state_copy_gather_scatter():
     assert kda.device_status() == 0
 
 
+def test_state_copy_count_is_checked_against_the_indices():
+    src = torch.randn(4, 2, 128, 128, device=DEV)
+    dst = torch.zeros_like(src)
+    idx = torch.tensor([2, 0], device=DEV)
+    with pytest.raises(ValueError):
+        kda.state_copy(dst, src, idx, idx, n=3)   # 3 entries read from 2-entry index arrays
+    torch.cuda.synchronize()
+    assert not dst.any()
+    kda.state_copy(dst, src, idx, idx, n=1)
+    torch.cuda.synchronize()
+    assert torch.equal(dst[2], src[2]) and not dst[0].any()
+
+
 def test_state_copy_identity_and_odd_unit():
     src = torch.randn(3, 1, 3, 5, device=DEV)   # 15 floats per slot: scalar path
     dst = torch.zeros(3, 1, 3, 5, device=DEV)

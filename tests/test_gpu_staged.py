@@ -108,3 +108,15 @@ def test_tail_split_and_pageable_output():
     torch.cuda.synchronize()
     assert torch.equal(pageable, ref_o.cpu()) and torch.equal(fin2, ref_f)
     assert kda.device_status() == 0
+
+
+def test_reused_buffers_must_hold_the_tokens():
+    short = synth.make_inputs([64], heads=2, dtype="bf16", seed=88, device=DEV)
+    hs = host(short)
+    _, _, bufs = kda.prefill_staged(hs["q"], hs["k"], hs["v"], hs["g"], hs["beta"], chunk_tokens=32)
+    x = synth.make_inputs([96], heads=2, dtype="bf16", seed=89, device=DEV)
+    h = host(x)
+    with pytest.raises(ValueError):
+        kda.prefill_staged(h["q"], h["k"], h["v"], h["g"], h["beta"], chunk_tokens=32, buffers=bufs)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
