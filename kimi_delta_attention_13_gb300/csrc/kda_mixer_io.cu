@@ -17,7 +17,7 @@
 // and keep the next 8 (bf16) or 4 (fp32) tokens' loads in flight (the chunk's first tokens read a
 // 3-token halo that the neighbouring chunk, scheduled next to it, has just brought into L2); and
 // the gates, elementwise at full occupancy (their exp/log chains kept the convolution's warps
-// waiting when both shared a kernel).
+// waiting when both shared a kernel), launched as a programmatic dependent of the convolution.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -155,6 +155,9 @@ struct PremixArgs {
 template <typename T>
 __global__ void __launch_bounds__(kMixThreads) premix_conv_kernel(const PremixArgs p)
 {
+    // the gates kernel launched after this one reads none of its outputs: it may start as soon
+    // as every block of this grid has started
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int kMixDepth = mix_depth<T>();
     const int xi = blockIdx.z;
     const bool norm = xi < 2;
@@ -318,6 +321,27 @@ int sm_count()
     return sms;
 }
 
+// The gates after the convolution, as a programmatic dependent launch: their blocks fill the SMs
+// that the convolution's last wave leaves idle.  Work later in the stream still waits for both.
+template <typename T>
+cudaError_t launch_gates(const void *a, const void *b, void *g, void *beta, long long n8, long long nb,
+                         dim3 grid, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, premix_gates_kernel<T>, static_cast<const T *>(a),
+                              static_cast<const T *>(b), static_cast<T *>(g), static_cast<T *>(beta),
+                              n8, nb);
+}
+
 template <typename TO, typename TZ>
 int launch_gate_out(const void *o, const void *z, void *out, int out_dtype, long long n,
                     dim3 grid, cudaStream_t stream)
@@ -355,16 +379,16 @@ int launch_premix(const void *xq, const void *xk, const void *xv, const void *a,
     const dim3 ggrid((unsigned)(want < cap ? want : cap));
     if (dtype == KDA_BF16) {
         premix_conv_kernel<__nv_bfloat16><<<grid, kMixThreads, 0, stream>>>(p);
-        premix_gates_kernel<__nv_bfloat16><<<ggrid, 256, 0, stream>>>(
-            static_cast<const __nv_bfloat16 *>(a), static_cast<const __nv_bfloat16 *>(b),
-            static_cast<__nv_bfloat16 *>(g), static_cast<__nv_bfloat16 *>(beta), n8, nb);
+        if (cudaGetLastError() != cudaSuccess ||
+            launch_gates<__nv_bfloat16>(a, b, g, beta, n8, nb, ggrid, stream) != cudaSuccess)
+            return KDA_ERR_CUDA;
     } else {
         premix_conv_kernel<float><<<grid, kMixThreads, 0, stream>>>(p);
-        premix_gates_kernel<float><<<ggrid, 256, 0, stream>>>(
-            static_cast<const float *>(a), static_cast<const float *>(b), static_cast<float *>(g),
-            static_cast<float *>(beta), n8, nb);
+        if (cudaGetLastError() != cudaSuccess ||
+            launch_gates<float>(a, b, g, beta, n8, nb, ggrid, stream) != cudaSuccess)
+            return KDA_ERR_CUDA;
     }
-    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return KDA_OK;
 }
 
 int launch_output_gate(const void *o, int o_dtype, const void *z, int z_dtype, void *out,
