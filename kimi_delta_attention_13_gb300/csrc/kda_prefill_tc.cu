@@ -1203,13 +1203,10 @@ int launch_typed(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap
                  const CUtensorMap &mv, const CUtensorMap &mo, const Params &p, int blocks,
                  cudaStream_t stream)
 {
-    static std::once_flag once;
-    static cudaError_t attr_rc = cudaSuccess;
-    std::call_once(once, [] {
-        attr_rc = cudaFuncSetAttribute(prefill_tc_kernel<TO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SMEM_ALLOC);
-    });
-    if (attr_rc != cudaSuccess) return KDA_ERR_CUDA;
+    // a function attribute belongs to the current device: set it on every launch
+    if (cudaFuncSetAttribute(prefill_tc_kernel<TO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_ALLOC) != cudaSuccess)
+        return KDA_ERR_CUDA;
     prefill_tc_kernel<TO><<<blocks, kThreads, SMEM_ALLOC, stream>>>(mq, mk, mg, mv, mo, p);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
