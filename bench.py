@@ -40,6 +40,7 @@ BYTES_PER_TOKEN_HEAD = 4 * D * 2 + 2 + D * 4        # q, k, v, g bf16 + beta bf1
 STATE_BYTES = D * D * 4                             # 65,536 per (sequence, head)
 DECODE_BYTES_PER_SEQ_HEAD = 2 * STATE_BYTES + 4 * D * 2 + 2 + D * 4   # 132,610
 PREMIX_BYTES_PER_TOKEN_HEAD = 2 * (4 * D * 2 + 2)    # xq, xk, xv, a, b in; q, k, v, g, beta out: 2,052
+TOL_OUT, TOL_STATE = 2e-2, 1e-2   # bf16-input bounds: max|err| / RMS on outputs and on states
 E2E_CHUNK = 1024               # tokens per chunk of the staged (copy-overlapped) end-to-end prefill
 
 
@@ -239,15 +240,47 @@ def oracle_sample(tokens: int, heads: int, seed: int = 1, threads=None):
     return time.perf_counter() - t0, min(nthreads, heads)
 
 
-def cpu_baseline(target_s: float = 10.0):
-    """The oracle timed on a bounded sample of the T=8192, H=96 workload, scaled to tokens/s of
-    the full 96-head width."""
-    t_small, _ = oracle_sample(64, H)
+def rel_err(got, ref) -> float:
+    """max |got - ref| / RMS(ref) over a tensor."""
+    import numpy as np
+
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    if ref.size == 0:
+        return 0.0
+    return float(np.max(np.abs(got - ref)) / rms) if rms > 0 else float(np.max(np.abs(got)))
+
+
+def cpu_baseline(step, target_s: float = 10.0):
+    """The oracle timed on a bounded sample of the timed step's own inputs (its first tokens, all
+    96 heads), scaled to tokens/s; the step's GPU results on the same tokens are compared with the
+    oracle's (outputs, and the final state when the sample is the whole sequence)."""
+    import oracle
+
+    orc = oracle.default()
+    cores = int(os.cpu_count() or 1)
+    x = step["inputs"]
+
+    def run(tokens):
+        sl = [x[k][:tokens] for k in ("q", "k", "v", "g", "beta")]
+        t0 = time.perf_counter()
+        o, f, _ = orc.prefill(*sl, threads=cores)
+        return time.perf_counter() - t0, o, f
+
+    t_small, _, _ = run(64)
     tokens = int(max(64, min(T1, 64 * target_s / max(t_small, 1e-3))))
-    secs, cores = oracle_sample(tokens, H)
-    return {"value": tokens / secs, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"fp64 oracle, first {tokens} tokens x all {H} heads of the T=8192 workload "
-                      f"({secs:.1f} s)"}
+    secs, o, f = run(tokens)
+    base = {"value": tokens / secs, "unit": "tokens/s", "cores": min(cores, H), "kind": "oracle",
+            "sample": f"fp64 oracle on the timed step's inputs: first {tokens} tokens x all {H} heads "
+                      f"of the T=8192 workload ({secs:.1f} s)"}
+    out_err = rel_err(step["out"][:tokens].numpy(), o)
+    fin_err = rel_err(step["final"].numpy(), f) if tokens == T1 else None
+    ok = out_err <= TOL_OUT and (fin_err is None or fin_err <= TOL_STATE)
+    parity = {"vs": "fp64 oracle, same inputs", "tokens": tokens, "heads": H,
+              "metric": "max|gpu - oracle| / RMS(oracle)", "out": out_err, "final_state": fin_err,
+              "tolerance": {"out": TOL_OUT, "final_state": TOL_STATE}, "pass": ok}
+    return base, parity
 
 
 def run_reference(args):
@@ -341,8 +374,11 @@ def run_gb300(args):
     h_out = torch.empty(T1, H, D, dtype=torch.float32).pin_memory()
     h_fin = torch.empty(1, H, D, D, dtype=torch.float32).pin_memory()
     del x
+    # the timed step's inputs and results, for the oracle comparison of the CPU-baseline leg
+    with_base = rank == 0 and world == 1 and not args.no_cpu_baseline
+    step = {"inputs": hx, "out": out.cpu(), "final": fin.cpu()} if with_base else None
 
-    # the staged prefill: 512-token chunks whose uploads, prefills and downloads overlap; device
+    # the staged prefill: chunks whose uploads, prefills and downloads overlap; device
     # staging buffers are allocated once, as a serving loop would
     fin_d = torch.empty(1, H, D, D, device=dev, dtype=torch.float32)
     staged = {"buffers": None}
@@ -363,7 +399,8 @@ def run_gb300(args):
         e2e_per = max_over_ranks(e2e_per, dev)
     h2d = sum(v.numel() * v.element_size() for v in hx.values())
     d2h = h_out.numel() * 4 + h_fin.numel() * 4
-    del hx, h_out, h_fin, staged, fin_d
+    del h_out, h_fin, staged, fin_d
+    hx = None
     torch.cuda.empty_cache()
 
     # ---- decode workload: 256 x 96 states (1.6 GB fp32), updated in place -----------------
@@ -436,7 +473,7 @@ def run_gb300(args):
             torch.distributed.destroy_process_group()
         return 0
 
-    base = cpu_baseline() if (world == 1 and not args.no_cpu_baseline) else None
+    base, parity = cpu_baseline(step) if with_base else (None, None)
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "prefill_traffic.json")
     if os.path.exists(tpath):
@@ -485,6 +522,7 @@ def run_gb300(args):
         "gpu_launches": args.steps,
         "clocks": clk,
         "cpu_baseline": base,
+        "parity": parity,
         "published": PUBLISHED,
     }
     print(json.dumps(line), flush=True)
