@@ -71,7 +71,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
             if log:
                 print(log)
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [cc, "-shared", "-o", tmp] + [o for o, _ in results] + ARCH_FLAGS
+    # -ldl: the NVTX ranges of the C ABI look up a profiler's injection library at run time
+    cmd = [cc, "-shared", "-o", tmp] + [o for o, _ in results] + ARCH_FLAGS + ["-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -2,11 +2,22 @@
 // Declarations, argument meaning, layouts and error behaviour: include/kda.h.
 #include <cstdio>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kda_internal.cuh"
 
 using namespace kda;
 
 namespace {
+
+// An NVTX range over one C-ABI call, so that profiler captures can be scoped to a call.  Without
+// a tool attached the push and pop do nothing.
+struct CallRange {
+    explicit CallRange(const char *name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange &) = delete;
+    CallRange &operator=(const CallRange &) = delete;
+};
 
 bool bad_dtype(int32_t dtype) { return dtype != KDA_BF16 && dtype != KDA_F32; }
 
@@ -106,6 +117,7 @@ int kda_prefill(const void *q, const void *k, const void *v, const void *g, cons
                 int32_t d_k, int32_t d_v, int32_t dtype, int32_t out_dtype, const float *init_state,
                 void *out, float *final_state, int32_t ckpt_stride, float *ckpts, void *stream)
 {
+    const CallRange range("kda_prefill");
     int rc = check_prefill(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, n_heads, d_k, d_v,
                            dtype, out_dtype, init_state, out, final_state, ckpt_stride, ckpts);
     if (rc != KDA_OK) return rc;
@@ -124,6 +136,7 @@ int kda_prefill_recurrent(const void *q, const void *k, const void *v, const voi
                           int32_t dtype, int32_t out_dtype, const float *init_state, void *out,
                           float *final_state, int32_t ckpt_stride, float *ckpts, void *stream)
 {
+    const CallRange range("kda_prefill_recurrent");
     int rc = check_prefill(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, n_heads, d_k, d_v,
                            dtype, out_dtype, init_state, out, final_state, ckpt_stride, ckpts);
     if (rc != KDA_OK) return rc;
@@ -136,6 +149,7 @@ int kda_decode(const void *q, const void *k, const void *v, const void *g, const
                float *state, void *out, int32_t n_seqs, int32_t n_heads, int32_t d_k, int32_t d_v,
                int32_t dtype, int32_t out_dtype, void *stream)
 {
+    const CallRange range("kda_decode");
     if (n_seqs < 0 || n_heads < 1 || d_k < 1 || d_v < 1 || bad_dtype(dtype) || bad_dtype(out_dtype))
         return KDA_ERR_INVALID_ARG;
     if (n_seqs > 0 && (!q || !k || !v || !g || !beta || !state || !out)) return KDA_ERR_INVALID_ARG;
@@ -152,6 +166,7 @@ int kda_state_copy(float *dst, const int64_t *dst_idx, int64_t n_dst_slots, cons
                    const int64_t *src_idx, int64_t n_src_slots, int64_t n, int32_t n_heads,
                    int32_t d_k, int32_t d_v, void *stream)
 {
+    const CallRange range("kda_state_copy");
     if (n < 0 || n_dst_slots < 0 || n_src_slots < 0 || n_heads < 1 || d_k < 1 || d_v < 1)
         return KDA_ERR_INVALID_ARG;
     if (n > 0 && (!dst || !src)) return KDA_ERR_INVALID_ARG;
@@ -169,6 +184,7 @@ int kda_premix(const void *xq, const void *xk, const void *xv, const void *a, co
                int64_t total_tokens, int32_t n_heads, int32_t d, float eps, int32_t dtype, void *q,
                void *k, void *v, void *g, void *beta, void *stream)
 {
+    const CallRange range("kda_premix");
     if (n_seqs < 0 || total_tokens < 0 || n_heads < 1 || d < 1 || bad_dtype(dtype) || !(eps > 0.f))
         return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0 && n_seqs == 0) return KDA_ERR_INVALID_ARG;
@@ -193,6 +209,7 @@ int kda_premix(const void *xq, const void *xk, const void *xv, const void *a, co
 int kda_output_gate(const void *o, int32_t o_dtype, const void *z, int32_t z_dtype, void *out,
                     int32_t out_dtype, int64_t n, void *stream)
 {
+    const CallRange range("kda_output_gate");
     if (n < 0 || bad_dtype(o_dtype) || bad_dtype(z_dtype) || bad_dtype(out_dtype))
         return KDA_ERR_INVALID_ARG;
     if (n > 0 && (!o || !z || !out)) return KDA_ERR_INVALID_ARG;
@@ -207,6 +224,7 @@ int kda_output_gate(const void *o, int32_t o_dtype, const void *z, int32_t z_dty
 int kda_cp_combine(const float *s_loc, const float *m, const int32_t *seq_seg, int32_t n_seqs,
                    int32_t n_heads, int32_t d, float *s_start, float *final_state, void *stream)
 {
+    const CallRange range("kda_cp_combine");
     if (n_seqs < 0 || n_heads < 1 || d < 1) return KDA_ERR_INVALID_ARG;
     if (d != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
     if (n_seqs > 0 && (!s_loc || !m || !seq_seg || !s_start)) return KDA_ERR_INVALID_ARG;
@@ -235,6 +253,7 @@ int kda_prefill_staged(const void *h_q, const void *h_k, const void *h_v, const 
                        void *d_beta, void *d_out, void *h_out, float *final_state,
                        int32_t *d_scratch, int64_t scratch_ints, int64_t chunk_tokens, void *stream)
 {
+    const CallRange range("kda_prefill_staged");
     int rc = check_staged(h_q, h_k, h_v, h_g, h_beta, h_cu_seqlens, n_seqs, total_tokens, n_heads,
                           dtype, out_dtype, init_state, d_q, d_k, d_v, d_g, d_beta, d_out, h_out,
                           final_state, chunk_tokens);
@@ -256,6 +275,7 @@ int kda_prefill_staged_static(const void *h_q, const void *h_k, const void *h_v,
                               void *d_beta, void *d_out, void *h_out, float *final_state,
                               int64_t chunk_tokens, void *stream)
 {
+    const CallRange range("kda_prefill_staged_static");
     int rc = check_staged(h_q, h_k, h_v, h_g, h_beta, h_cu_seqlens, n_seqs, total_tokens, n_heads,
                           dtype, out_dtype, init_state, d_q, d_k, d_v, d_g, d_beta, d_out, h_out,
                           final_state, chunk_tokens);
