@@ -77,7 +77,8 @@ const char *kda_status_string(int status);
  *                     May alias final_state (in-place resume).
  *   out               [total_tokens, H, d_v] outputs o_t, `out_dtype`.  Must not alias an input.
  *   final_state       fp32 [n_seqs, H, d_k, d_v] state after each sequence, or NULL.
- *   ckpt_stride       0 (no checkpoints) or a positive multiple of 64.  Sequence n of length
+ *   ckpt_stride       0 (no checkpoints) or a positive multiple of 32 (the tensor-core kernel
+ *                     advances the state 32 tokens a step).  Sequence n of length
  *                     L_n emits floor(L_n / ckpt_stride) checkpoints: the state after its first
  *                     m*ckpt_stride tokens, m = 1..floor(L_n / ckpt_stride).
  *   ckpts             fp32 [sum_n floor(L_n / ckpt_stride), H, d_k, d_v]; slots are ordered by
@@ -88,6 +89,15 @@ const char *kda_status_string(int status);
  * inputs, and for bf16 inputs with other sizes, 1 <= d_k <= 128 and d_v a multiple of 32 up to 256 (per-token
  * CUDA-core kernel).  Errors: KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED_SHAPE,
  * KDA_ERR_MISALIGNED, KDA_ERR_CUDA.
+ *
+ * Value range of the tensor-core kernel: the state stays fp32, but the state products take the
+ * new values V - K~S0 and a copy of the state as fp16 operands (full precision from 6.1e-5 to
+ * 65504).  With q and k of unit norm and beta in [0, 1], v and init_state scaled by powers of two
+ * from 2^-12 to 2^13 of unit variance (|v| up to about 4e4) keep the bf16-input bounds (outputs
+ * 2e-2, states 1e-2 of RMS); at 2^14 (|v| ~ 8e4) the fp16 operands overflow and the outputs are not
+ * finite, and at 2^-16 the fp16 subnormal range costs accuracy (outputs ~4e-2 of RMS).  Scale v
+ * into that range (the recurrence is linear in v and the state) or use kda_prefill_recurrent,
+ * which keeps every product in fp32.
  */
 int kda_prefill(const void *q, const void *k, const void *v, const void *g, const void *beta,
                 const int32_t *cu_seqlens, int32_t n_seqs, int64_t total_tokens, int32_t n_heads,
@@ -109,6 +119,7 @@ int kda_prefill_recurrent(const void *q, const void *k, const void *v, const voi
 /* Which kernel kda_prefill runs for these sizes: 1 = tensor-core chunked, 0 = per-token
  * CUDA-core, negative = a kda_status (unsupported / invalid). */
 int kda_prefill_path(int32_t d_k, int32_t d_v, int32_t dtype);
+
 
 /*
  * kda_decode -- one new token per sequence, state updated in place.
@@ -212,9 +223,16 @@ int kda_output_gate(const void *o, int32_t o_dtype, const void *z, int32_t z_dty
  *   d_scratch        device int32 [scratch_ints] for the chunks' sequence tables, at least
  *                    kda_prefill_staged_scratch(...) entries (0 for a single sequence).
  *   chunk_tokens     >= 1 (a multiple of 32 keeps a single sequence's arithmetic identical to
- *                    kda_prefill's).
- * Errors: those of kda_prefill, KDA_ERR_INVALID_ARG (a bad host table, too little scratch),
- * KDA_ERR_CUDA (stream or event creation, copies).
+ *                    kda_prefill's).  When the tokens span more than one chunk, chunk_tokens x
+ *                    n_heads x (2 for bf16, 4 for fp32) must be a multiple of 16, so that every
+ *                    chunk's beta rows start 16-byte aligned (bf16: chunk_tokens x n_heads a
+ *                    multiple of 8); otherwise KDA_ERR_INVALID_ARG and nothing is enqueued.
+ *   stream           a stream of the current device (KDA_ERR_INVALID_ARG for another device's).
+ * The first call on a device creates two non-blocking streams (uploads, downloads) and four
+ * events, which later calls on that device reuse and which live until the process exits; calls
+ * from several host threads take turns at enqueueing on them.
+ * Errors: those of kda_prefill, KDA_ERR_INVALID_ARG (a bad host table, too little scratch, an
+ * unaligned chunk size, another device's stream), KDA_ERR_CUDA (stream or event creation, copies).
  */
 int kda_prefill_staged(const void *h_q, const void *h_k, const void *h_v, const void *h_g,
                        const void *h_beta, const int32_t *h_cu_seqlens, int32_t n_seqs,

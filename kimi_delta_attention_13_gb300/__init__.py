@@ -130,7 +130,7 @@ def prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, *, out=None, fin
     q, k, g: [T, H, d_k]; v: [T, H, d_v]; beta: [T, H] (bf16 or fp32, contiguous, CUDA);
     cu_seqlens: int32 [N+1] on the device or None for one sequence; init_state: fp32
     [N, H, d_k, d_v] or None (zeros).  final_state: True to allocate, a tensor to fill, or
-    None/False.  ckpt_stride: 0 or a multiple of 64.  out_dtype: float32 (default, the
+    None/False.  ckpt_stride: 0 or a multiple of 32.  out_dtype: float32 (default, the
     accumulation precision) or bfloat16.  Returns (out, final_state, ckpts).
     """
     return _prefill("kda_prefill", q, k, v, g, beta, cu_seqlens, init_state, out, final_state,

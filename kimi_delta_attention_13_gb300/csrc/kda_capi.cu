@@ -35,7 +35,8 @@ int check_prefill(const void *q, const void *k, const void *v, const void *g, co
     if (total_tokens > 0 && n_seqs == 0) return KDA_ERR_INVALID_ARG;
     if (!cu_seqlens && n_seqs > 1) return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;  // cu_seqlens are int32
-    if (ckpt_stride < 0 || ckpt_stride % 64 != 0) return KDA_ERR_INVALID_ARG;
+    // a checkpoint falls on a boundary of the tensor-core kernel's 32-token steps
+    if (ckpt_stride < 0 || ckpt_stride % 32 != 0) return KDA_ERR_INVALID_ARG;
     if (ckpt_stride > 0 && !ckpts) return KDA_ERR_INVALID_ARG;
     const void *ptrs[] = {q, k, v, g, beta, init_state, out, final_state, ckpts};
     for (const void *p : ptrs)
@@ -71,6 +72,10 @@ int check_staged(const void *h_q, const void *h_k, const void *h_v, const void *
                           init_state, final_state};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+    // every chunk after the first starts at a multiple of chunk_tokens (or of 32 in the cut-up
+    // last chunk), and its beta rows must start 16-byte aligned like every pointer of a prefill
+    const int64_t esz = dtype == KDA_BF16 ? 2 : 4;
+    if (total_tokens > chunk_tokens && (chunk_tokens * n_heads * esz) % 16 != 0) return KDA_ERR_INVALID_ARG;
     if (n_seqs > 1) {   // the host table is checked in full here
         if (h_cu_seqlens[0] != 0 || h_cu_seqlens[n_seqs] != total_tokens) return KDA_ERR_INVALID_ARG;
         for (int n = 0; n < n_seqs; ++n)

@@ -25,7 +25,59 @@ namespace {
 constexpr int64_t kStaticTableInts = 1 << 20;
 static __device__ __align__(256) int32_t g_staged_tables[kStaticTableInts];
 std::mutex g_tables_mu;
-cudaEvent_t g_tables_free[64] = {};   // per device: recorded after the last call that read the table
+cudaEvent_t g_tables_free[64] = {};   // (indexed like g_resources)   // per device: recorded after the last call that read the table
+
+// Streams and events of the staged calls, created on a device's first call and kept until the
+// process exits: two non-blocking streams (uploads, downloads) and four events, reused by every
+// later call on that device.  A call holds `mu` while it enqueues, so calls from several host
+// threads take turns at enqueueing and share the two copy streams.
+struct Resources {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr, landed = nullptr, computed = nullptr;
+};
+constexpr int kMaxDevices = 64;
+Resources g_resources[kMaxDevices];
+std::mutex g_resources_mu;
+
+// The device that `stream` belongs to, which must be the current device (the kernels launch
+// there).  KDA_ERR_INVALID_ARG for another device's stream.
+int stream_device(cudaStream_t stream, int *dev)
+{
+    int cur = 0, sd = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess || cudaStreamGetDevice(stream, &sd) != cudaSuccess) return KDA_ERR_CUDA;
+    if (sd != cur) return KDA_ERR_INVALID_ARG;
+    if (cur < 0 || cur >= kMaxDevices) return KDA_ERR_CUDA;
+    *dev = cur;
+    return KDA_OK;
+}
+
+int device_resources(cudaStream_t stream, Resources **out)
+{
+    int dev = 0;
+    const int rc = stream_device(stream, &dev);
+    if (rc != KDA_OK) return rc;
+    std::lock_guard<std::mutex> lock(g_resources_mu);
+    Resources &r = g_resources[dev];
+    if (!r.ready) {   // a set left partial by a failed creation is completed by the next call
+        cudaStream_t *streams[2] = {&r.s_in, &r.s_out};
+        cudaEvent_t *events[4] = {&r.start, &r.done, &r.landed, &r.computed};
+        for (cudaStream_t *x : streams)
+            if (!*x && cudaStreamCreateWithFlags(x, cudaStreamNonBlocking) != cudaSuccess) {
+                *x = nullptr;
+                return KDA_ERR_CUDA;
+            }
+        for (cudaEvent_t *x : events)
+            if (!*x && cudaEventCreateWithFlags(x, cudaEventDisableTiming) != cudaSuccess) {
+                *x = nullptr;
+                return KDA_ERR_CUDA;
+            }
+        r.ready = true;
+    }
+    *out = &r;
+    return KDA_OK;
+}
 
 // SM-store downloads: a few blocks fill the host link and leave most SMs to the next chunk's
 // prefill (one whole SM per CTA).  On the T = 8192, H = 96 workload 64 blocks did slightly better
@@ -112,6 +164,11 @@ int run_prefill_staged(const void *const h_in[5], const int32_t *h_cu, int n_seq
     const size_t esz = dtype == KDA_BF16 ? 2 : 4, osz = out_dtype == KDA_BF16 ? 2 : 4;
     const size_t row = (size_t)H * 128;                       // elements of a token's q/k/v/g row
     const size_t blk = (size_t)H * 128 * 128 * sizeof(float);   // one sequence's states
+    // the call's streams and events are the device's cached set, held for the whole enqueue
+    Resources *res = nullptr;
+    const int rdev = device_resources(stream, &res);
+    if (rdev != KDA_OK) return rdev;
+    std::lock_guard<std::mutex> lock(res->mu);
     // running states: the initial ones (or zeros), overwritten chunk by chunk
     cudaError_t e = cudaSuccess;
     if (!init_state)
@@ -135,36 +192,26 @@ int run_prefill_staged(const void *const h_in[5], const int32_t *h_cu, int n_seq
         (void)cudaGetLastError();   // pageable or unregistered memory: not an error here
     }
 
-    cudaStream_t s_in = nullptr, s_out = nullptr;
-    cudaEvent_t start = nullptr, done = nullptr;
     int rc = KDA_OK;
     auto ok = [&](cudaError_t x) {
         if (x != cudaSuccess && rc == KDA_OK) rc = KDA_ERR_CUDA;
         return rc == KDA_OK;
     };
-    if (!ok(cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking)) ||
-        !ok(cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking)) ||
-        !ok(cudaEventCreateWithFlags(&start, cudaEventDisableTiming)) ||
-        !ok(cudaEventCreateWithFlags(&done, cudaEventDisableTiming)) ||
-        !ok(cudaEventRecord(start, stream)) || !ok(cudaStreamWaitEvent(s_in, start, 0)) ||
-        !ok(cudaStreamWaitEvent(s_out, start, 0))) {
-        // fall through to the clean-up below
-    }
+    ok(cudaEventRecord(res->start, stream));
+    ok(cudaStreamWaitEvent(res->s_in, res->start, 0));
+    ok(cudaStreamWaitEvent(res->s_out, res->start, 0));
     for (size_t i = 0; rc == KDA_OK && i < chunks.size(); ++i) {
         const Chunk &c = chunks[i];
         const size_t rows = (size_t)(c.t1 - c.t0);
-        cudaEvent_t landed = nullptr, computed = nullptr;
-        if (!ok(cudaEventCreateWithFlags(&landed, cudaEventDisableTiming)) ||
-            !ok(cudaEventCreateWithFlags(&computed, cudaEventDisableTiming)))
-            break;
         // inputs of the chunk: q, k, v, g rows, then beta
         for (int x = 0; x < 5 && rc == KDA_OK; ++x) {
             const size_t w = (x < 4 ? row : (size_t)H) * esz;
             ok(cudaMemcpyAsync(static_cast<char *>(d_in[x]) + c.t0 * w, static_cast<const char *>(h_in[x]) + c.t0 * w,
-                               rows * w, cudaMemcpyHostToDevice, s_in));
+                               rows * w, cudaMemcpyHostToDevice, res->s_in));
         }
-        ok(cudaEventRecord(landed, s_in));
-        ok(cudaStreamWaitEvent(stream, landed, 0));
+        // a wait takes the event as last recorded, so one event serves every chunk
+        ok(cudaEventRecord(res->landed, res->s_in));
+        ok(cudaStreamWaitEvent(stream, res->landed, 0));
         if (rc == KDA_OK) {
             const int n_sub = c.n_b - c.n_a + 1;
             void *p[5];
@@ -178,31 +225,24 @@ int run_prefill_staged(const void *const h_in[5], const int32_t *h_cu, int n_seq
                                       stream);
             if (r != KDA_OK) rc = r;
         }
-        ok(cudaEventRecord(computed, stream));
-        ok(cudaStreamWaitEvent(s_out, computed, 0));
+        ok(cudaEventRecord(res->computed, stream));
+        ok(cudaStreamWaitEvent(res->s_out, res->computed, 0));
         const size_t off = c.t0 * row * osz, bytes = rows * row * osz;   // multiples of 256 B
         if (h_out_dev) {
-            store_to_host_kernel<<<kStoreBlocks, kStoreThreads, 0, s_out>>>(
+            store_to_host_kernel<<<kStoreBlocks, kStoreThreads, 0, res->s_out>>>(
                 reinterpret_cast<int4 *>(h_out_dev + off),
                 reinterpret_cast<const int4 *>(static_cast<const char *>(d_out) + off),
                 (long long)(bytes / 16));
             ok(cudaGetLastError());
         } else {
             ok(cudaMemcpyAsync(static_cast<char *>(h_out) + off, static_cast<const char *>(d_out) + off,
-                               bytes, cudaMemcpyDeviceToHost, s_out));
+                               bytes, cudaMemcpyDeviceToHost, res->s_out));
         }
-        cudaEventDestroy(landed);     // released once recorded work completes
-        cudaEventDestroy(computed);
     }
-    // the caller's stream continues after the last download
-    if (done && s_out) {
-        ok(cudaEventRecord(done, s_out));
-        ok(cudaStreamWaitEvent(stream, done, 0));
-    }
-    if (start) cudaEventDestroy(start);
-    if (done) cudaEventDestroy(done);
-    if (s_in) cudaStreamDestroy(s_in);   // destroyed once their queued work completes
-    if (s_out) cudaStreamDestroy(s_out);
+    // the caller's stream continues after the last download (also after an error, so that no
+    // later work of the caller overtakes copies already queued)
+    cudaEventRecord(res->done, res->s_out);
+    cudaStreamWaitEvent(stream, res->done, 0);
     return rc;
 }
 
@@ -213,10 +253,10 @@ int run_prefill_staged_static(const void *const h_in[5], const int32_t *h_cu, in
 {
     if (staged_scratch_ints(h_cu, n_seqs, T, chunk_tokens) > kStaticTableInts) return KDA_ERR_INVALID_ARG;
     int dev = 0;
+    const int sd = stream_device(stream, &dev);   // the array and event of the stream's device
+    if (sd != KDA_OK) return sd;
     void *tables = nullptr;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 ||
-        cudaGetSymbolAddress(&tables, g_staged_tables) != cudaSuccess)
-        return KDA_ERR_CUDA;
+    if (cudaGetSymbolAddress(&tables, g_staged_tables) != cudaSuccess) return KDA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_tables_mu);
     cudaEvent_t &free_ev = g_tables_free[dev];
     if (!free_ev && cudaEventCreateWithFlags(&free_ev, cudaEventDisableTiming) != cudaSuccess) {

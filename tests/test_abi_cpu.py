@@ -75,7 +75,8 @@ def _prefill(lib, **over):
     (dict(H=0), 1), (dict(n=-1), 1), (dict(T=-5), 1), (dict(dtype=3), 1), (dict(q=None), 1),
     (dict(odt=2), 1),
     (dict(n=2), 1),                       # two sequences need cu_seqlens
-    (dict(stride=48), 1),                 # not a multiple of 64
+    (dict(stride=48), 1),                 # not a multiple of 32
+    (dict(stride=16), 1),
     (dict(stride=64), 1),                 # checkpoints requested without a buffer
     (dict(out=A), 1),                     # out aliases q
     (dict(q=A + 8), 3), (dict(fin=A + 100), 3), (dict(cu=A + 2), 3),
@@ -199,4 +200,9 @@ def test_staged_rejects(lib):
     assert _staged(lib, ok.ctypes.data, 2, scratch=A + 8192 * 4, scratch_ints=1) == 1   # too little
     assert _staged(lib, fin=None) == 1                     # final_state carries the states
     assert _staged(lib, chunk=0) == 1
+    # chunks of 3 tokens x 2 heads of bf16 beta: the second chunk's beta rows start at byte 12
+    assert _staged(lib, chunk=3) == 1
+    assert lib.kda_prefill_staged_static(*[A + 16 * i for i in range(5)], None, 1, 64, 2, 0, 1, None,
+                                         *[A + 4096 + 16 * i for i in range(6)], A + 2048, A + 8192,
+                                         3, None) == 1
     assert _staged(lib, fin=A + 8196) == 3

@@ -28,8 +28,9 @@ def orc():
     return oracle.default()
 
 
-def check(orc, lengths, heads, seg_len, init, seed, oracle_heads=None):
-    x = synth.make_inputs(lengths, heads=heads, dtype="bf16", seed=seed, device=DEV, init_state=init)
+def check(orc, lengths, heads, seg_len, init, seed, oracle_heads=None, decay_scale=1.0):
+    x = synth.make_inputs(lengths, heads=heads, dtype="bf16", seed=seed, device=DEV, init_state=init,
+                          decay_scale=decay_scale)
     out, fin = prefill_cp(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], x["state"],
                           seg_len=seg_len, lengths=lengths)
     torch.cuda.synchronize()
@@ -74,3 +75,20 @@ def test_cp_edge_cases(orc):
                           seg_len=64, lengths=[0, 0])
     torch.cuda.synchronize()
     assert out.numel() == 0 and torch.equal(fin, e["state"])
+
+
+def test_cp_bench_configuration(orc):
+    # the configuration of the benchmark's context-parallel figure: one sequence of 262,144 tokens,
+    # 8 heads, the benchmark's seed and segment length (16 segments of 16,384 on 152 SMs); the
+    # oracle checks two heads
+    from kimi_delta_attention_13_gb300.context_parallel import auto_seg_len
+
+    T, H = 262144, 8
+    seg = auto_seg_len(T, H, torch.cuda.get_device_properties(DEV).multi_processor_count)
+    check(orc, [T], H, seg, False, seed=9, oracle_heads=[2, 5])
+
+
+def test_cp_slow_decay(orc):
+    # g x 0.01: each segment's map M is far from zero, so the scan composes states that carry
+    # across segments (with the workloads' fast decay every M is ~0)
+    check(orc, [65536], 4, 8192, True, seed=75, decay_scale=0.01)

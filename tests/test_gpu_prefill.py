@@ -181,19 +181,42 @@ def test_checkpoint_buffer_and_lengths_are_checked(orc):
 
 # --- full-size workloads, in the benchmark's launch configuration ---------------------------------
 
-def test_workload_prefill_T8192_all_heads(orc):
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_workload_prefill_T8192_all_heads(orc, seed):
+    # seed 1 is the workload's own input; seeds 2 and 3 redraw it from the same distributions, so
+    # that the margin to the bound is not one draw's luck
     w = synth.workloads()[1]
-    x = synth.make_workload_inputs(w, DEV)
+    x = synth.make_inputs(w.lengths, w.heads, w.d_k, w.d_v, w.dtype, seed, DEV, w.init_state)
     errs, _ = run_and_check(orc, x)
-    print("T8192", errs)
+    print("T8192 seed", seed, errs)
 
 
-def test_workload_varlen8_sampled_heads(orc):
+def test_workload_varlen8_all_heads(orc):
     w = synth.workloads()[2]
     x = synth.make_workload_inputs(w, DEV)
-    heads = sorted(torch.randperm(96, generator=torch.Generator().manual_seed(202))[:6].tolist())
-    errs, _ = run_and_check(orc, x, heads=heads)
+    errs, _ = run_and_check(orc, x)
     print("varlen8", w.lengths, errs)
+
+
+@pytest.mark.parametrize("path", ["prefill", "recurrent"])
+def test_checkpoint_stride_32(orc, path):
+    # the finest stride: a checkpoint after every 32-token step of the tensor-core kernel
+    x = synth.make_inputs([5, 64, 0, 130, 1, 200, 96], heads=3, dtype="bf16", seed=33, device=DEV,
+                          init_state=True)
+    run_and_check(orc, x, path=path, ckpt_stride=32)
+
+
+@pytest.mark.parametrize("e", [-12, -6, 6, 13])
+def test_value_and_state_scale(orc, e):
+    """The recurrence is linear in (v, S0) (pinned in the oracle), so v and the initial state
+    scaled by 2^e scale outputs and states by 2^e; the tensor-core kernel rounds V - K~S0 and
+    its state copy to fp16 operands, whose range (6e-8 .. 65504) these scales exercise."""
+    x = synth.make_inputs([1000], heads=2, dtype="bf16", seed=34, device=DEV, init_state=True)
+    x["v"] = (x["v"].float() * 2.0 ** e).to(torch.bfloat16)      # exact: a power of two
+    x["state"] = x["state"] * 2.0 ** e
+    errs, (out, fin, _) = run_and_check(orc, x)
+    print("scale 2^%d" % e, errs, "max|v|", float(x["v"].float().abs().max()),
+          "max|S|", float(fin.abs().max()))
 
 
 def test_workload_long_context_checkpoints(orc):

@@ -120,3 +120,39 @@ def test_reused_buffers_must_hold_the_tokens():
         kda.prefill_staged(h["q"], h["k"], h["v"], h["g"], h["beta"], chunk_tokens=32, buffers=bufs)
     torch.cuda.synchronize()
     assert kda.device_status() == 0
+
+
+def test_unaligned_chunk_size_is_refused_before_any_work():
+    # H = 3 bf16 heads: chunks of 100 tokens would start the second chunk's beta rows at byte
+    # 600, off the 16-byte grid every prefill pointer keeps; the call refuses it up front
+    x = synth.make_inputs([250], heads=3, dtype="bf16", seed=90, device=DEV, init_state=True)
+    h = host(x)
+    fin = torch.full((1, 3, 128, 128), 7.0, device=DEV)
+    with pytest.raises(kda.KDAError, match="INVALID_ARG"):
+        kda.prefill_staged(h["q"], h["k"], h["v"], h["g"], h["beta"], None, x["state"], chunk_tokens=100,
+                           final_state=fin)
+    torch.cuda.synchronize()
+    assert bool((fin == 7.0).all())   # nothing was enqueued
+    # chunks of 96 tokens x 3 heads keep beta aligned: same call, against the oracle
+    out, fin, _ = kda.prefill_staged(h["q"], h["k"], h["v"], h["g"], h["beta"], None, x["state"], chunk_tokens=96)
+    torch.cuda.synchronize()
+    ro, rf, _ = oracle.default().prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], None, x["state"])
+    assert_close("out", out, ro, TOL["bf16"]["out"])
+    assert_close("final_state", fin, rf, TOL["bf16"]["state"])
+    assert kda.device_status() == 0
+
+
+def test_repeated_calls_reuse_the_device_streams():
+    # the staged call keeps two streams and four events per device after its first call; many
+    # calls in a row (and from a second stream) stay exact against one kda_prefill
+    x = synth.make_inputs([640], heads=2, dtype="bf16", seed=91, device=DEV, init_state=True)
+    ref_o, ref_f, _ = kda.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], None, x["state"])
+    h = host(x)
+    bufs = None
+    s2 = torch.cuda.Stream(device=DEV)
+    for i in range(20):
+        out, fin, bufs = kda.prefill_staged(h["q"], h["k"], h["v"], h["g"], h["beta"], None, x["state"],
+                                            chunk_tokens=128, buffers=bufs, stream=s2 if i % 2 else None)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_o.cpu()) and torch.equal(fin, ref_f)
+    assert kda.device_status() == 0
