@@ -48,7 +48,9 @@ typedef enum {
     KDA_ERR_MISALIGNED = 3,        /* a pointer not 16-byte aligned                           */
     KDA_ERR_CUDA = 4,              /* a CUDA runtime call or kernel launch failed             */
     KDA_ERR_DEVICE_TIMEOUT = 5,    /* a bounded device-side wait expired (device error word)  */
-    KDA_ERR_INDEX_RANGE = 6        /* kda_state_copy met an index outside its slot range      */
+    KDA_ERR_INDEX_RANGE = 6,       /* kda_state_copy met an index outside its slot range      */
+    KDA_ERR_DEVICE_BOUNDS = 7      /* a device-side bounds check failed (library built with
+                                      -DKDA_DEBUG, or kda_diag_bounds_check)                    */
 } kda_status;
 
 typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
@@ -306,6 +308,20 @@ int kda_device_status(int32_t *status, void *stream);
  * Errors: KDA_ERR_INVALID_ARG (cycles out of range), KDA_ERR_CUDA.
  */
 int kda_diag_device_timeout(int64_t timeout_cycles, void *stream);
+
+/*
+ * kda_diag_bounds_check -- the device-side bounds check of a debug build, shown to work.  A library
+ * compiled with -DKDA_DEBUG checks, inside the tensor-core prefill, every shared-memory pointer the
+ * kernel's accessors take against the CTA's shared-memory window and every TMEM address against
+ * the allocated columns and the lanes the executing warp may reach; a failed check skips the access
+ * and records KDA_ERR_DEVICE_BOUNDS in the device error word (read by kda_device_status) and the
+ * check's site number.  This call launches one thread that runs that check on an offset past its
+ * window, without any access, so the same recording happens in every build.  *site receives the
+ * site number of the first failed check since the last call (0 if none), after synchronizing
+ * `stream`, and is cleared.  The pages have no counterpart.  Errors: KDA_ERR_INVALID_ARG (site
+ * NULL), KDA_ERR_CUDA.
+ */
+int kda_diag_bounds_check(int32_t run_probe, int32_t *site, void *stream);
 
 #ifdef __cplusplus
 }

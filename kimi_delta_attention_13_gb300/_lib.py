@@ -14,7 +14,7 @@ KDA_BF16 = 0
 KDA_F32 = 1
 STATUS_NAMES = {
     0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED_SHAPE", 3: "KDA_ERR_MISALIGNED",
-    4: "KDA_ERR_CUDA", 5: "KDA_ERR_DEVICE_TIMEOUT", 6: "KDA_ERR_INDEX_RANGE",
+    4: "KDA_ERR_CUDA", 5: "KDA_ERR_DEVICE_TIMEOUT", 6: "KDA_ERR_INDEX_RANGE", 7: "KDA_ERR_DEVICE_BOUNDS",
 }
 
 # name -> (restype, argtypes); every function declared in include/kda.h
@@ -32,6 +32,7 @@ SIGNATURES = {
     "kda_state_copy": (ctypes.c_int, [_vp, _vp, _i64, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp]),
     "kda_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _vp]),
     "kda_diag_device_timeout": (ctypes.c_int, [_i64, _vp]),
+    "kda_diag_bounds_check": (ctypes.c_int, [_i32, ctypes.POINTER(ctypes.c_int32), _vp]),
     "kda_premix": (ctypes.c_int, [_vp] * 7 + [_vp, _i32, _i64, _i32, _i32, ctypes.c_float, _i32]
                    + [_vp] * 5 + [_vp]),
     "kda_output_gate": (ctypes.c_int, [_vp, _i32, _vp, _i32, _vp, _i32, _i64, _vp]),

@@ -39,25 +39,33 @@ def _deps():
     return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+# The debug variant (-DKDA_DEBUG: device-side bounds checks in the tensor-core prefill), built on
+# demand into a directory of its own; the release library is the one the package loads.
+DEBUG_BUILD_DIR = BUILD_DIR + "-debug"
+DEBUG_LIB_PATH = os.path.join(DEBUG_BUILD_DIR, "libkda_gb300_debug.so")
+
+
+def up_to_date(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile and link the library; returns its path."""
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=None, debug: bool = False) -> str:
+    """Compile and link the library (or, with debug=True, its bounds-checked variant); returns its
+    path."""
+    lib_path, build_dir = (DEBUG_LIB_PATH, DEBUG_BUILD_DIR) if debug else (LIB_PATH, BUILD_DIR)
+    if not force and up_to_date(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
-    flags = NVCC_FLAGS + ARCH_FLAGS + list(extra_flags or []) + ["-I", INCLUDE]
+    flags = NVCC_FLAGS + ARCH_FLAGS + list(extra_flags or []) + ["-I", INCLUDE] + (["-DKDA_DEBUG"] if debug else [])
     if verbose:
         flags = flags + ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, "-c", src, "-o", obj] + flags
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -70,14 +78,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
         for _, log in results:
             if log:
                 print(log)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     # -ldl: the NVTX ranges of the C ABI look up a profiler's injection library at run time
     cmd = [cc, "-shared", "-o", tmp] + [o for o, _ in results] + ARCH_FLAGS + ["-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

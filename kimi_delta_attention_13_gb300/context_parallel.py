@@ -110,3 +110,132 @@ def prefill_cp(q, k, v, g, beta, cu_seqlens=None, init_state=None, *, seg_len: i
         if final_state is not None and N > 0:
             state_copy(final_state, seg_final, seqs, last, stream=s)
         return out, final_state
+
+
+# --------------------------------------------------------------------------------------------
+# Across ranks: each rank owns a contiguous block of the segments.  Passes 1 and 2 run on a
+# rank's own segments; one all-gather hands every rank every segment's (M, S_loc); each rank
+# runs the (cheap) scan over all segments and pass 3 on its own.  The only data crossing ranks is
+# that exchange: 2 x H x d x d fp32 per segment.
+
+
+def assign_segments(n_seg: int, world_size: int) -> List[range]:
+    """Contiguous, balanced blocks of segment indices, one per rank (rank r owns owned[r])."""
+    if world_size < 1:
+        raise ValueError("world_size must be positive")
+    base, extra = divmod(int(n_seg), world_size)
+    out, lo = [], 0
+    for r in range(world_size):
+        hi = lo + base + (1 if r < extra else 0)
+        out.append(range(lo, hi))
+        lo = hi
+    return out
+
+
+def gather_segments(local: torch.Tensor, owned: List[range], group=None) -> torch.Tensor:
+    """All-gather of per-segment tensors: every rank passes its own block [len(owned[rank]), ...]
+    and gets [n_seg, ...] in segment order.  Blocks differ in size by at most one, so each is sent
+    padded to the largest and trimmed on arrival."""
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    width = max(len(r) for r in owned)
+    padded = torch.zeros((width,) + tuple(local.shape[1:]), dtype=local.dtype, device=local.device)
+    padded[: local.shape[0]] = local
+    bufs = [torch.empty_like(padded) for _ in range(world)]
+    dist.all_gather(bufs, padded, group=group)
+    return torch.cat([bufs[r][: len(owned[r])] for r in range(world)], 0)
+
+
+class _LibraryBackend:
+    """The library's calls on one device and stream: the compute of every pass."""
+
+    def __init__(self, device, stream):
+        self.device, self.stream = device, stream
+
+    def prefill(self, q, k, v, g, beta, cu, init):
+        out, fin, _ = prefill(q, k, v, g, beta, cu, init, final_state=True, stream=self.stream)
+        return out, fin
+
+    def scan(self, s_loc, m, seq_seg, s_start):
+        lib = _lib.load()
+        H, D = s_loc.shape[1], s_loc.shape[2]
+        seq_seg_t = torch.tensor(seq_seg, dtype=torch.int32, device=self.device)
+        rc = lib.kda_cp_combine(_ptr(s_loc), _ptr(m), _ptr(seq_seg_t), len(seq_seg) - 1, H, D,
+                                _ptr(s_start), None, _stream(self.device, self.stream))
+        _lib.check(rc, "kda_cp_combine")
+
+
+def _prefill_cp_ranks(q, k, v, g, beta, lengths, init_state, seg_len, backend, group=None):
+    """The rank-local part of a context-parallel prefill (see prefill_cp_distributed); `backend`
+    supplies the prefill of a varlen batch and the segment scan."""
+    import torch.distributed as dist
+
+    rank, world = dist.get_rank(group), dist.get_world_size(group)
+    T, H, D = q.shape
+    N = len(lengths)
+    bounds, seq_seg = segments(lengths, seg_len)
+    n_seg = len(bounds)
+    owned = assign_segments(n_seg, world)
+    mine = owned[rank]
+    # states in the initial states' precision (fp32 on the library's path)
+    dev, f32 = q.device, (init_state.dtype if init_state is not None else torch.float32)
+    # a sequence's first segment starts from the sequence's own initial state
+    first_of = {seq_seg[n]: n for n in range(N)}
+    tok_lo = bounds[mine.start][0] if len(mine) else 0
+    tok_hi = bounds[mine.stop - 1][1] if len(mine) else 0
+    if len(mine):
+        sl = slice(tok_lo, tok_hi)
+        xq, xk, xv, xg, xb = q[sl], k[sl], v[sl], g[sl], beta[sl]
+        cu = torch.tensor([bounds[j][0] - tok_lo for j in mine] + [tok_hi - tok_lo], dtype=torch.int32,
+                          device=dev)
+        init = torch.zeros((len(mine), H, D, D), device=dev, dtype=f32)
+        for j in mine:
+            if j in first_of and init_state is not None:
+                init[j - mine.start] = init_state[first_of[j]]
+        # 1. own segments from their local starts: S_loc;  2. with v = 0 from the identity: M
+        _, s_loc_mine = backend.prefill(xq, xk, xv, xg, xb, cu, init)
+        eye = torch.eye(D, device=dev, dtype=f32).expand(len(mine), H, D, D).contiguous()
+        _, m_mine = backend.prefill(xq, xk, torch.zeros_like(xv), xg, xb, cu, eye)
+    else:
+        s_loc_mine = torch.zeros((0, H, D, D), device=dev, dtype=f32)
+        m_mine = torch.zeros((0, H, D, D), device=dev, dtype=f32)
+    # the exchange: every segment's map and local end state on every rank
+    s_loc = gather_segments(s_loc_mine, owned, group)
+    m = gather_segments(m_mine, owned, group)
+    # 3. the scan over all segments: true start states (a first segment keeps its initial state)
+    s_start = torch.zeros((n_seg, H, D, D), device=dev, dtype=f32)
+    if init_state is not None:
+        for j, n in first_of.items():
+            s_start[j] = init_state[n]
+    backend.scan(s_loc, m, seq_seg, s_start)
+    # 4. own segments from their true starts: outputs of the own tokens, and the final state of
+    # every sequence whose last segment is here
+    out_mine, finals = None, {}
+    if len(mine):
+        out_mine, seg_final = backend.prefill(xq, xk, xv, xg, xb, cu, s_start[mine.start:mine.stop].contiguous())
+        for n in range(N):
+            last = seq_seg[n + 1] - 1
+            if last in mine:
+                finals[n] = seg_final[last - mine.start]
+    return out_mine, (tok_lo, tok_hi), finals
+
+
+def prefill_cp_distributed(q, k, v, g, beta, init_state=None, *, seg_len: int, lengths: Sequence[int],
+                           group=None, stream=None):
+    """Context-parallel prefill across the ranks of a torch.distributed group (one GPU each).
+
+    Every rank passes the same packed inputs (q, k, v, g, beta on its own device; init_state fp32
+    [N, H, 128, 128] or None) and the same `lengths` and `seg_len`.  The sequences are cut into
+    segments of `seg_len` tokens; rank r prefills the r-th contiguous block of them (passes 1 and
+    2), one all-gather shares every segment's (M, S_loc) (the only exchange, 2 x H x 128 x 128 fp32
+    per segment), and every rank runs the scan and the final pass over its own block.  Returns
+    (out, (t0, t1), finals): the outputs of the rank's tokens t0..t1-1 (fp32 [t1 - t0, H, 128]),
+    and {sequence index: final state [H, 128, 128]} for the sequences ending on this rank."""
+    dev = q.device
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    lengths = [int(L) for L in lengths]
+    if sum(lengths) != q.shape[0]:
+        raise ValueError("lengths do not add up to the token count")
+    with torch.cuda.stream(s):
+        return _prefill_cp_ranks(q, k, v, g, beta, lengths, init_state, seg_len, _LibraryBackend(dev, s), group)

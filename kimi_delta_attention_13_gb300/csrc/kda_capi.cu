@@ -105,6 +105,7 @@ const char *kda_status_string(int status)
     case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime call or launch failed";
     case KDA_ERR_DEVICE_TIMEOUT: return "KDA_ERR_DEVICE_TIMEOUT: bounded device wait expired";
     case KDA_ERR_INDEX_RANGE: return "KDA_ERR_INDEX_RANGE: state index out of range";
+    case KDA_ERR_DEVICE_BOUNDS: return "KDA_ERR_DEVICE_BOUNDS: device-side bounds check failed";
     default: return "KDA_ERR_UNKNOWN";
     }
 }
@@ -296,6 +297,13 @@ int kda_diag_device_timeout(int64_t timeout_cycles, void *stream)
 {
     if (timeout_cycles < 1 || timeout_cycles > 4000000000LL) return KDA_ERR_INVALID_ARG;
     return kda::launch_wait_timeout_probe((long long)timeout_cycles, (cudaStream_t)stream);
+}
+
+int kda_diag_bounds_check(int32_t run_probe, int32_t *site, void *stream)
+{
+    if (!site) return KDA_ERR_INVALID_ARG;
+    if (run_probe && kda::launch_bounds_check_probe((cudaStream_t)stream) != KDA_OK) return KDA_ERR_CUDA;
+    return kda::read_and_clear_debug_site((cudaStream_t)stream, site);
 }
 
 int kda_device_status(int32_t *status, void *stream)

@@ -29,6 +29,10 @@ int read_and_clear_status_prefill_tc(cudaStream_t s, int32_t *status);
 int read_and_clear_status_decode(cudaStream_t s, int32_t *status);
 // Launch the one-CTA probe whose bounded device wait expires after `cycles` SM cycles.
 int launch_wait_timeout_probe(long long cycles, cudaStream_t stream);
+// Launch the one-thread run of the shared-memory bounds check on an out-of-window offset; read
+// (and clear) the site number of the first failed bounds check.
+int launch_bounds_check_probe(cudaStream_t stream);
+int read_and_clear_debug_site(cudaStream_t s, int32_t *site);
 
 // Kernel launchers (host side, no validation: the C ABI validates first).
 int launch_decode(const void *q, const void *k, const void *v, const void *g, const void *beta,

@@ -169,6 +169,44 @@ struct Misc {
 };
 
 __device__ int g_prefill_tc_error;  // sticky device error word of this translation unit
+__device__ int g_prefill_tc_debug_site;   // the first failed bounds check (site number), 0 if none
+
+// ---- bounds checks.  A build with -DKDA_DEBUG checks every shared-memory pointer the kernel's
+// accessors take against the CTA's dynamic shared-memory window, and every TMEM address against
+// the 512 allocated columns and the lanes the executing warp may reach (its 32-lane sub-partition);
+// a failed check records KDA_ERR_DEVICE_BOUNDS and its site in device words and skips the access.
+// Release builds compile the checks out.
+extern __shared__ __align__(16) uint8_t kda_dyn_smem[];
+
+__device__ __noinline__ void bounds_failed(int site)
+{
+    atomicCAS(&g_prefill_tc_debug_site, 0, site);
+    atomicExch(&g_prefill_tc_error, KDA_ERR_DEVICE_BOUNDS);
+}
+
+__device__ __forceinline__ bool smem_in_window(const void *p, uint32_t bytes, int site)
+{
+    const uint32_t a = smem_u32(p), lo = smem_u32(kda_dyn_smem);
+    if (a >= lo && a + bytes <= lo + SMEM_ALLOC) return true;
+    bounds_failed(site);
+    return false;
+}
+
+__device__ __forceinline__ bool tmem_in_reach(uint32_t taddr, uint32_t ncols, int site)
+{
+    const uint32_t lane = taddr >> 16, col = taddr & 0xffffu;
+    if (lane == 32u * ((threadIdx.x >> 5) & 3u) && col + ncols <= 512u) return true;
+    bounds_failed(site);
+    return false;
+}
+
+#ifdef KDA_DEBUG
+#define KDA_SMEM_OK(p, n, site) smem_in_window((p), (n), (site))
+#define KDA_TMEM_OK(t, n, site) tmem_in_reach((t), (n), (site))
+#else
+#define KDA_SMEM_OK(p, n, site) true
+#define KDA_TMEM_OK(t, n, site) true
+#endif
 
 // Per-step timeline of the first CTA (SM clock stamps), compiled in only with -DKDA_TRACE.
 #ifdef KDA_TRACE
@@ -229,8 +267,14 @@ __device__ __forceinline__ void drain_mmas(uint64_t *bar, Misc *misc)
 
 __device__ __forceinline__ void st_shared_v4(uint8_t *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
-    *reinterpret_cast<uint4 *>(p) = make_uint4(a, b, c, d);
+    if (KDA_SMEM_OK(p, 16, 1)) *reinterpret_cast<uint4 *>(p) = make_uint4(a, b, c, d);
 }
+
+// TMEM loads and stores of this kernel (the warp-uniform address is checked in debug builds)
+__device__ __forceinline__ void tld32(uint32_t t, uint32_t (&r)[32]) { if (KDA_TMEM_OK(t, 32, 2)) tmem_ld32(t, r); }
+__device__ __forceinline__ void tld16(uint32_t t, uint32_t (&r)[16]) { if (KDA_TMEM_OK(t, 16, 3)) tmem_ld16(t, r); }
+__device__ __forceinline__ void tst32(uint32_t t, const uint32_t (&r)[32]) { if (KDA_TMEM_OK(t, 32, 4)) tmem_st32(t, r); }
+__device__ __forceinline__ void tst16(uint32_t t, const uint32_t (&r)[16]) { if (KDA_TMEM_OK(t, 16, 5)) tmem_st16(t, r); }
 
 // 8 consecutive fp16 values (one 16-byte chunk) from fp32
 __device__ __forceinline__ void store_chunk_f16(uint8_t *addr, const float *v)
@@ -399,10 +443,10 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(p.init ? p.init[sbase + (long long)(c0 + i) * D + j] : 0.f);
 #pragma unroll
         for (int i = 0; i < 16; ++i) rb[i] = pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-        tmem_st16(tb + TM_SBF + c0 / 2, rb);
+        tst16(tb + TM_SBF + c0 / 2, rb);
 #pragma unroll
         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * bc_all[c0 + i]);
-        tmem_st32(tb + TM_S32 + c0, r);
+        tst32(tb + TM_S32 + c0, r);
     }
     tmem_wait_st();
     tc_fence_before();
@@ -424,7 +468,7 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
         {
             uint32_t r[32];
             float t[8];
-            tmem_ld32(tb + TM_DR, r);
+            tld32(tb + TM_DR, r);
             tmem_wait_ld();
             uint8_t *kk = smem + kk_base(slot);
 #pragma unroll
@@ -434,7 +478,7 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
                 store_chunk_f16(kk + sw128(j, kk_half(slot) + 16 * m), t);   // R row = key channel j
             }
             if (wq == 0) {
-                tmem_ld32(tb + TM_DP, r);
+                tld32(tb + TM_DP, r);
                 tmem_wait_ld();
                 uint8_t *ab = smem + ab_off(slot);
 #pragma unroll
@@ -453,11 +497,11 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
         tc_fence_after();
         {
             uint32_t r[32], rb[16];
-            tmem_ld32(tb + TM_D1 + 64 * buf, r);
+            tld32(tb + TM_D1 + 64 * buf, r);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; ++i) rb[i] = pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-            tmem_st16(tb + TM_VBF, rb);
+            tst16(tb + TM_VBF, rb);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -485,11 +529,11 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t r[32], rb[16];
-            tmem_ld32(tb + TM_S32 + c0, r);
+            tld32(tb + TM_S32 + c0, r);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; ++i) rb[i] = pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-            tmem_st16(tb + TM_SBF + c0 / 2, rb);
+            tst16(tb + TM_SBF + c0 / 2, rb);
             if (ck) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) ck[(long long)(c0 + i) * D + j] = __uint_as_float(r[i]);
@@ -513,9 +557,9 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
         // directly.
         {
             uint32_t r[32];
-            tmem_ld32(tb + TM_D1 + 64 * buf + 32, r);
+            tld32(tb + TM_D1 + 64 * buf + 32, r);
             tmem_wait_ld();
-            if (valid == C) {
+            if (valid == C && KDA_SMEM_OK(reinterpret_cast<TO *>(smem + OFF_OSTAGE) + j, (31 * D + 1) * sizeof(TO), 17)) {
                 TO *st = reinterpret_cast<TO *>(smem + OFF_OSTAGE) + j;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) store_out<TO>(st + i * D, __uint_as_float(r[i]));
@@ -540,10 +584,11 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
         if (!last) {
             wait_bar(&bars[B_OPS_READY + nslot], ((s + 1) / kSlots) & 1, misc);   // b_C(s+1)
             const float *bcn = bc_all + nslot * D;
+            if (!KDA_SMEM_OK(bcn, D * 4, 18)) bcn = bc_all;   // (debug: record, read in range)
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t r[32];
-                tmem_ld32(tb + TM_S32 + c0, r);
+                tld32(tb + TM_S32 + c0, r);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
@@ -553,7 +598,7 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
                     r[i] = __float_as_uint(lo.x); r[i + 1] = __float_as_uint(lo.y);
                     r[i + 2] = __float_as_uint(hi.x); r[i + 3] = __float_as_uint(hi.y);
                 }
-                tmem_st32(tb + TM_S32 + c0, r);
+                tst32(tb + TM_S32 + c0, r);
             }
         }
         if (j == 0) KDA_TRACE_EVENT(17, s);
@@ -587,7 +632,7 @@ __device__ __forceinline__ float2 bf2x2(uint32_t w)
 // product ignores the low 13 bits), so the Gram sees round-to-nearest operands.
 __device__ __forceinline__ void store_tf32x2(uint8_t *addr, float2 v)
 {
-    *reinterpret_cast<unsigned long long *>(addr) = pk(v) + 0x0000100000001000ull;
+    if (KDA_SMEM_OK(addr, 8, 6)) *reinterpret_cast<unsigned long long *>(addr) = pk(v) + 0x0000100000001000ull;
 }
 
 // Decay factors and every scaled operand of step s.  Thread p owns the channel pair (2cp, 2cp+1)
@@ -609,7 +654,7 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
     for (int i = 0; i < 8; ++i) {
         const int r = 8 * qr + i;
         const uint32_t off = tile_off + sw128(r, cbyte);
-        const bool in = r < valid;
+        const bool in = r < valid && KDA_SMEM_OK(qkg + off, 2 * TILE_BYTES + 4, 7);
         const float2 g = in ? bf2x2(*reinterpret_cast<const uint32_t *>(qkg + 2 * TILE_BYTES + off)) : make_float2(0.f, 0.f);
         kv[i] = in ? bf2x2(*reinterpret_cast<const uint32_t *>(qkg + TILE_BYTES + off)) : make_float2(0.f, 0.f);
         qv[i] = in ? bf2x2(*reinterpret_cast<const uint32_t *>(qkg + off)) : make_float2(0.f, 0.f);
@@ -628,7 +673,7 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
 #pragma unroll
         for (int i = 1; i < 8; ++i) f[i] = mul2(f[i], f[i - 1]);
     }
-    tot[qr * 64 + cp] = f[7];
+    if (KDA_SMEM_OK(tot + qr * 64 + cp, 8, 8)) tot[qr * 64 + cp] = f[7];
     ok = gs.sync(misc) && ok;
     // the previous Gram has read its operands
     if (s >= 1) wait_bar(&bars[B_GRAM_DONE + ((s - 1) & 1)], ((s - 1) >> 1) & 1, misc);
@@ -638,7 +683,8 @@ __device__ __forceinline__ void prep_operands(uint8_t *smem, const uint8_t *qkg,
     const float2 one = make_float2(1.f, 1.f);
     const float2 pre = (qr & 1) ? (qr == 1 ? P0 : P2) : one;
     const float2 suf = (qr & 1) ? one : (qr == 0 ? P1 : P3);
-    if (qr == 0) reinterpret_cast<float2 *>(smem + OFF_BC + slot * D * 4)[cp] = mul2(B0, B1);
+    if (qr == 0 && KDA_SMEM_OK(smem + OFF_BC + slot * D * 4 + 8 * cp, 8, 9))
+        reinterpret_cast<float2 *>(smem + OFF_BC + slot * D * 4)[cp] = mul2(B0, B1);
     const float2 emul = tile ? mul2(pre, B0) : pre;      // E = f * emul
     const float2 xmul = tile ? suf : mul2(suf, B1);      // X = gl * xmul
     // 1/F = G / (tile total): F G is the tile's total retention for every token of the tile, so
@@ -724,6 +770,7 @@ static_assert(TB_BYTES == 2048, "shared-memory map reserves 2 KB per T-block buf
 __device__ __forceinline__ void solve_diag_blocks(const float *nA, int lane, float2 x2[8])
 {
     const int base = (lane >> 4) * 16, c = lane & 15;
+    if (!KDA_SMEM_OK(nA + base * 36 + base, (15 * 36 + 16) * 4, 12)) return;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const float *row = nA + (base + i) * 36 + base;
@@ -751,6 +798,7 @@ __device__ __forceinline__ void solve_offdiag(const float *nA, const float *tb, 
                                               float t10[4])
 {
     const int c = 8 * half + (lane & 7), rq = lane >> 3;
+    if (!KDA_SMEM_OK(tb, TB_BYTES, 13) || !KDA_SMEM_OK(nA + 16 * 36, 16 * 36 * 4, 14)) return;
     float2 tc[8];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
@@ -799,6 +847,7 @@ __device__ __forceinline__ void store_diag_blocks(float *tb, uint8_t *ab, int la
 {
     const int c = lane & 15;
     float t[8];
+    if (!KDA_SMEM_OK(tb, TB_BYTES, 15)) return;
     if (lane < 16) {
 #pragma unroll
         for (int g = 0; g < 4; ++g)
@@ -834,7 +883,8 @@ __device__ __forceinline__ void store_offdiag(uint8_t *ab, int half, int lane, c
 {
     const int c = 8 * half + (lane & 7), rq = lane >> 3;
     const uint32_t lo = pack_f16x2(bc * t10[0], bc * t10[1]), hi = pack_f16x2(bc * t10[2], bc * t10[3]);
-    *reinterpret_cast<uint2 *>(ab + sw128(c, 96 + 8 * rq)) = make_uint2(lo, hi);
+    if (KDA_SMEM_OK(ab + sw128(c, 96 + 8 * rq), 8, 16))
+        *reinterpret_cast<uint2 *>(ab + sw128(c, 96 + 8 * rq)) = make_uint2(lo, hi);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -846,8 +896,8 @@ struct GramRow {
     uint32_t r0[32], r1[16];
     __device__ __forceinline__ void load(uint32_t taddr)
     {
-        tmem_ld32(taddr, r0);
-        tmem_ld16(taddr + 32, r1);
+        tld32(taddr, r0);
+        tld16(taddr + 32, r1);
         tmem_wait_ld();
     }
     __device__ __forceinline__ float at(int r, int i) const
@@ -897,7 +947,9 @@ __device__ void a_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc *mis
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_EXTR_DONE + buf]);
         const int r = lane;   // token row
-        sbeta_all[buf * C + r] = br;
+        // (a failed debug check skips the stores; the warp stays on its path)
+        const bool st_ok = KDA_SMEM_OK(sA + r * 36, 128, 10) && KDA_SMEM_OK(sbeta_all + buf * C + r, 4, 11);
+        if (st_ok) sbeta_all[buf * C + r] = br;
         const float nbr = -br;           // sA holds -A
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
@@ -906,7 +958,7 @@ __device__ void a_role(const Params &p, uint8_t *smem, uint64_t *bars, Misc *mis
             v.y = (4 * m + 1 < r) ? nbr * g.at(r, 4 * m + 1) : 0.f;
             v.z = (4 * m + 2 < r) ? nbr * g.at(r, 4 * m + 2) : 0.f;
             v.w = (4 * m + 3 < r) ? nbr * g.at(r, 4 * m + 3) : 0.f;
-            *reinterpret_cast<float4 *>(sA + r * 36 + 4 * m) = v;
+            if (st_ok) *reinterpret_cast<float4 *>(sA + r * 36 + 4 * m) = v;
         }
         __syncwarp();
         if (lane == 0) {
@@ -1232,6 +1284,30 @@ __global__ void wait_timeout_probe_kernel(long long cycles)
 }
 
 }  // namespace
+
+// One thread runs the shared-memory bounds check on an offset past its CTA's window (nothing is
+// accessed): the check records KDA_ERR_DEVICE_BOUNDS, as a failed check in a debug build would.
+__global__ void bounds_check_probe_kernel()
+{
+    (void)smem_in_window(kda_dyn_smem + SMEM_ALLOC, 16, 99);
+}
+
+int launch_bounds_check_probe(cudaStream_t stream)
+{
+    bounds_check_probe_kernel<<<1, 1, 0, stream>>>();
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int read_and_clear_debug_site(cudaStream_t s, int32_t *site)
+{
+    int host = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&host, g_prefill_tc_debug_site, sizeof(int), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_prefill_tc_debug_site, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    *site = host;
+    return KDA_OK;
+}
 
 int launch_wait_timeout_probe(long long cycles, cudaStream_t stream)
 {

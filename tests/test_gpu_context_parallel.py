@@ -92,3 +92,34 @@ def test_cp_slow_decay(orc):
     # g x 0.01: each segment's map M is far from zero, so the scan composes states that carry
     # across segments (with the workloads' fast decay every M is ~0)
     check(orc, [65536], 4, 8192, True, seed=75, decay_scale=0.01)
+
+
+def test_cp_distributed_single_rank_equals_one_gpu(orc):
+    # the cross-rank call in a group of one (NCCL on this GPU): the same segments, scan and passes
+    # as the one-GPU call, so the results are bit-identical
+    import socket
+
+    import torch.distributed as dist
+
+    from kimi_delta_attention_13_gb300.context_parallel import prefill_cp_distributed
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                            device_id=DEV)
+    try:
+        lengths = [700, 0, 300]
+        x = synth.make_inputs(lengths, heads=2, dtype="bf16", seed=76, device=DEV, init_state=True)
+        out1, fin1 = prefill_cp(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], x["state"],
+                                seg_len=128, lengths=lengths)
+        out2, (t0, t1), finals = prefill_cp_distributed(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                                        x["state"], seg_len=128, lengths=lengths)
+        torch.cuda.synchronize()
+        assert (t0, t1) == (0, sum(lengths)) and sorted(finals) == [0, 1, 2]
+        assert torch.equal(out1, out2)
+        for n, f in finals.items():
+            assert torch.equal(f, fin1[n])
+        assert kda.device_status() == 0
+    finally:
+        dist.destroy_process_group()
