@@ -36,7 +36,8 @@ H, D = 96, 128
 T1 = 8192                      # prefill workload: one sequence of 8192 tokens
 N_DEC = 256                    # decode workload: 256 sequences
 FLOP_PER_TOKEN_HEAD = 6 * D * D + 8 * 16 * D        # 114,688 (chunk C = 16 accounting)
-BYTES_PER_TOKEN_HEAD = 4 * D * 2 + 2 + D * 4        # q, k, v, g bf16 + beta bf16 + o fp32 = 1,538
+BYTES_PER_TOKEN_HEAD = 4 * D * 2 + 2 + D * 2        # q, k, v, g, o bf16 + beta bf16 = 1,282
+BYTES_PER_TOKEN_HEAD_FP32_OUT = 4 * D * 2 + 2 + D * 4   # the same with o in fp32, as written = 1,538
 STATE_BYTES = D * D * 4                             # 65,536 per (sequence, head)
 DECODE_BYTES_PER_SEQ_HEAD = 2 * STATE_BYTES + 4 * D * 2 + 2 + D * 4   # 132,610
 PREMIX_BYTES_PER_TOKEN_HEAD = 2 * (4 * D * 2 + 2)    # xq, xk, xv, a, b in; q, k, v, g, beta out: 2,052
@@ -226,6 +227,26 @@ def cuda_time_ms(fn, steps, stream):
     return total, total / steps
 
 
+def cuda_time_ms_queued(fn, steps, stream, hold_cycles=4_000_000):
+    """As cuda_time_ms, for calls shorter than their host-side cost: a spin of `hold_cycles` GPU
+    cycles holds the stream while the calls are queued, so the events time the calls back to back
+    on the device rather than the rate at which the host submits them."""
+    import torch
+
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(hold_cycles)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    total = start.elapsed_time(stop)
+    return total, total / steps
+
+
 def oracle_sample(tokens: int, heads: int, seed: int = 1, threads=None):
     """Run the fp64 oracle on the first `tokens` tokens of `heads` heads of the prefill
     workload's distributions; returns (seconds, threads used)."""
@@ -361,7 +382,10 @@ def run_gb300(args):
         total_ms = max_over_ranks(total_ms, dev)
         per_ms = total_ms / args.steps
     tokens_per_s = replica_throughput(T1 * args.steps, total_ms, world)
+    # the roofline counts o in bf16 (the workload's byte budget); the kernel writes fp32 o, whose
+    # fraction, on the bytes actually written, is reported beside it
     bytes_alg = T1 * H * BYTES_PER_TOKEN_HEAD + H * STATE_BYTES
+    bytes_fp32_out = T1 * H * BYTES_PER_TOKEN_HEAD_FP32_OUT + H * STATE_BYTES
     flops_alg = T1 * H * FLOP_PER_TOKEN_HEAD
     achieved_gbs = bytes_alg / (per_ms / 1e3) / 1e9
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -495,6 +519,11 @@ def run_gb300(args):
                    "prefill_kernel": path},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved_gbs / hbm_peak, "traffic": traffic,
+                     "bytes_basis": "1,282 B per token-head: q, k, v, g, o in bf16, beta bf16; "
+                                    "+ the fp32 final state",
+                     "frac_fp32_out": bytes_fp32_out / (per_ms / 1e3) / 1e9 / hbm_peak,
+                     "frac_fp32_out_basis": "1,538 B per token-head: o counted in fp32, as the "
+                                            "kernel writes it",
                      "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "bytes_alg_per_launch": bytes_alg, "flops_alg_per_launch": flops_alg,
                      "t_bytes_us": t_bytes * 1e6, "t_flops_us": t_flops * 1e6,
@@ -590,7 +619,7 @@ def context_parallel_figure(dev, stream, T=262144, heads=8):
 
     import kimi_delta_attention_13_gb300 as kda
     from kimi_delta_attention_13_gb300 import synth
-    from kimi_delta_attention_13_gb300.context_parallel import auto_seg_len, prefill_cp
+    from kimi_delta_attention_13_gb300.context_parallel import auto_seg_len, cp_combine, prefill_cp
 
     seg_len = auto_seg_len(T, heads, torch.cuda.get_device_properties(dev).multi_processor_count)
 
@@ -608,9 +637,25 @@ def context_parallel_figure(dev, stream, T=262144, heads=8):
     _, plain_ms = cuda_time_ms(plain, 2, stream)
     _, cp_ms = cuda_time_ms(split, 3, stream)
     del x, args
+    # the scan alone, on states of the same shape (its time does not depend on the values)
+    n_seg = -(-T // seg_len)
+    gen = torch.Generator(device=dev).manual_seed(10)
+    s_loc = torch.randn(n_seg, heads, D, D, device=dev, generator=gen)
+    m = torch.randn(n_seg, heads, D, D, device=dev, generator=gen) / D ** 0.5
+    s_start = torch.empty_like(s_loc)
+    seq_seg = torch.tensor([0, n_seg], dtype=torch.int32, device=dev)
+
+    def scan():
+        cp_combine(s_loc, m, seq_seg, s_start, stream=stream)
+
+    for _ in range(3):
+        scan()
+    _, scan_ms = cuda_time_ms_queued(scan, 10, stream)
+    del s_loc, m, s_start
     return {"workload": f"one sequence T={T} H={heads} d={D} bf16, fp32 out and final state; "
                         f"segments of {seg_len} tokens",
             "plain_ms": plain_ms, "cp_ms": cp_ms, "speedup": plain_ms / cp_ms,
+            "scan_ms": scan_ms, "scan_segments": n_seg,
             "cp_tokens_per_s": T / (cp_ms / 1e3), "plain_tokens_per_s": T / (plain_ms / 1e3)}
 
 

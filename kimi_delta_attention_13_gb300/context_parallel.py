@@ -51,6 +51,35 @@ def auto_seg_len(total_tokens: int, heads: int, sms: int) -> int:
     return max(32, -(-per // 32) * 32)
 
 
+def cp_combine(s_loc, m, seq_seg, s_start, final_state=None, stream=None):
+    """The segment scan (kda_cp_combine): for every sequence n and segment j of
+    [seq_seg[n], seq_seg[n + 1]), S_start(j + 1) = M(j) S_start(j) + S_loc(j), starting from
+    S_loc of the sequence's first segment.  s_loc, m, s_start: fp32 [n_seg, H, 128, 128] on one
+    device; seq_seg: n_seqs + 1 segment indices, a host list or an int32 tensor on the device;
+    final_state: fp32 [n_seqs, H, 128, 128] or None.  s_start of each sequence's first segment is
+    left as it is."""
+    lib = _lib.load()
+    dev = s_loc.device
+    n_seg, H, D = s_loc.shape[0], s_loc.shape[1], s_loc.shape[2]
+    for name, t in (("s_loc", s_loc), ("m", m), ("s_start", s_start)):
+        _require(t, name, dev, torch.float32, (n_seg, H, D, D))
+    if isinstance(seq_seg, torch.Tensor):
+        _require(seq_seg, "seq_seg", dev, torch.int32)
+        if seq_seg.dim() != 1:
+            raise ValueError("seq_seg must be one-dimensional")
+    if final_state is not None:
+        _require(final_state, "final_state", dev, torch.float32, (len(seq_seg) - 1, H, D, D))
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.stream(s):
+        seq_seg_t = seq_seg if isinstance(seq_seg, torch.Tensor) else \
+            torch.tensor(list(seq_seg), dtype=torch.int32, device=dev)
+        rc = lib.kda_cp_combine(_ptr(s_loc), _ptr(m), _ptr(seq_seg_t), len(seq_seg) - 1, H, D,
+                                _ptr(s_start), _ptr(final_state) if final_state is not None else None,
+                                _stream(dev, s))
+    _lib.check(rc, "kda_cp_combine")
+    return s_start
+
+
 def prefill_cp(q, k, v, g, beta, cu_seqlens=None, init_state=None, *, seg_len: int,
                lengths: Optional[Sequence[int]] = None, out=None, final_state=True, stream=None):
     """Varlen KDA prefill with every sequence cut into segments of `seg_len` tokens that prefill
@@ -99,10 +128,7 @@ def prefill_cp(q, k, v, g, beta, cu_seqlens=None, init_state=None, *, seg_len: i
         del eye, scratch
         # 3. each segment's true start state (a first segment keeps its sequence's initial state)
         s_start = init_seg
-        seq_seg_t = torch.tensor(seq_seg, dtype=torch.int32, device=dev)
-        rc = lib.kda_cp_combine(_ptr(s_loc), _ptr(m), _ptr(seq_seg_t), N, H, D, _ptr(s_start),
-                                None, _stream(dev, s))
-        _lib.check(rc, "kda_cp_combine")
+        cp_combine(s_loc, m, seq_seg, s_start, stream=s)
         del m
         # 4. every segment from its true start: the outputs, and the sequences' final states
         out, seg_final, _ = prefill(q, k, v, g, beta, cu_seg, s_start, out=out, final_state=s_loc,
@@ -158,12 +184,7 @@ class _LibraryBackend:
         return out, fin
 
     def scan(self, s_loc, m, seq_seg, s_start):
-        lib = _lib.load()
-        H, D = s_loc.shape[1], s_loc.shape[2]
-        seq_seg_t = torch.tensor(seq_seg, dtype=torch.int32, device=self.device)
-        rc = lib.kda_cp_combine(_ptr(s_loc), _ptr(m), _ptr(seq_seg_t), len(seq_seg) - 1, H, D,
-                                _ptr(s_start), None, _stream(self.device, self.stream))
-        _lib.check(rc, "kda_cp_combine")
+        cp_combine(s_loc, m, seq_seg, s_start, stream=self.stream)
 
 
 def _prefill_cp_ranks(q, k, v, g, beta, lengths, init_state, seg_len, backend, group=None):

@@ -123,3 +123,37 @@ def test_cp_distributed_single_rank_equals_one_gpu(orc):
         assert kda.device_status() == 0
     finally:
         dist.destroy_process_group()
+
+
+def test_cp_combine_scan_against_fp64():
+    # the scan alone on random segment maps: S_start(j + 1) = M(j) S_start(j) + S_loc(j) over each
+    # sequence's segments, checked in fp64 on the host; sequences of 0, 1, 2 and 19 segments, and
+    # maps of norm about 1 so that every step carries the state forward
+    from kimi_delta_attention_13_gb300.context_parallel import cp_combine
+
+    H, D = 3, 128
+    seq_seg = [0, 1, 1, 3, 22]
+    n_seg = seq_seg[-1]
+    gen = torch.Generator().manual_seed(83)
+    s_loc = torch.randn(n_seg, H, D, D, generator=gen)
+    m = torch.randn(n_seg, H, D, D, generator=gen) / D ** 0.5
+    sentinel = 7.25
+    s_start = torch.full((n_seg, H, D, D), sentinel)
+    fin = torch.full((len(seq_seg) - 1, H, D, D), sentinel)
+    d_start, d_fin = s_start.to(DEV), fin.to(DEV)
+    cp_combine(s_loc.to(DEV), m.to(DEV), seq_seg, d_start, d_fin)
+    torch.cuda.synchronize()
+    got_start, got_fin = d_start.cpu(), d_fin.cpu()
+    for n in range(len(seq_seg) - 1):
+        lo, hi = seq_seg[n], seq_seg[n + 1]
+        if hi == lo:
+            assert torch.all(got_fin[n] == sentinel)   # no segment: nothing written
+            continue
+        assert torch.all(got_start[lo] == sentinel)    # a first segment keeps its own start
+        s = s_loc[lo].double()
+        for j in range(lo + 1, hi):
+            err = (got_start[j].double() - s).abs().max() / s.pow(2).mean().sqrt()
+            assert err < 1e-4, (n, j, float(err))
+            s = m[j].double() @ s + s_loc[j].double()
+        err = (got_fin[n].double() - s).abs().max() / s.pow(2).mean().sqrt()
+        assert err < 1e-4, (n, float(err))
