@@ -323,6 +323,15 @@ int kda_diag_device_timeout(int64_t timeout_cycles, void *stream);
  */
 int kda_diag_bounds_check(int32_t run_probe, int32_t *site, void *stream);
 
+/*
+ * kda_diag_staged_handles -- how many CUDA streams and events kda_prefill_staged and
+ * kda_prefill_staged_static have created in this process so far (host only, no CUDA call).  The
+ * first staged call on a device creates its two copy streams and four events, and the first static
+ * call on a device its one table event; later calls reuse them, so the count stays put across
+ * repeated calls.  The pages have no counterpart.  Errors: KDA_ERR_INVALID_ARG (created NULL).
+ */
+int kda_diag_staged_handles(int64_t *created);
+
 #ifdef __cplusplus
 }
 #endif

@@ -33,6 +33,7 @@ SIGNATURES = {
     "kda_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _vp]),
     "kda_diag_device_timeout": (ctypes.c_int, [_i64, _vp]),
     "kda_diag_bounds_check": (ctypes.c_int, [_i32, ctypes.POINTER(ctypes.c_int32), _vp]),
+    "kda_diag_staged_handles": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int64)]),
     "kda_premix": (ctypes.c_int, [_vp] * 7 + [_vp, _i32, _i64, _i32, _i32, ctypes.c_float, _i32]
                    + [_vp] * 5 + [_vp]),
     "kda_output_gate": (ctypes.c_int, [_vp, _i32, _vp, _i32, _vp, _i32, _i64, _vp]),

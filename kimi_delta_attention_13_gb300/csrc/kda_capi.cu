@@ -299,6 +299,13 @@ int kda_diag_device_timeout(int64_t timeout_cycles, void *stream)
     return kda::launch_wait_timeout_probe((long long)timeout_cycles, (cudaStream_t)stream);
 }
 
+int kda_diag_staged_handles(int64_t *created)
+{
+    if (!created) return KDA_ERR_INVALID_ARG;
+    *created = staged_handles_created();
+    return KDA_OK;
+}
+
 int kda_diag_bounds_check(int32_t run_probe, int32_t *site, void *stream)
 {
     if (!site) return KDA_ERR_INVALID_ARG;

@@ -63,6 +63,8 @@ int run_prefill_staged_static(const void *const h_in[5], const int32_t *h_cu, in
                               int H, int dtype, int out_dtype, const float *init_state,
                               void *const d_in[5], void *d_out, void *h_out, float *final_state,
                               long long chunk_tokens, cudaStream_t stream);
+// streams and events the staged calls have created so far in this process
+long long staged_handles_created();
 int launch_prefill_tc(const void *q, const void *k, const void *v, const void *g,
                       const void *beta, const int32_t *cu_seqlens, int n_seqs,
                       int64_t total_tokens, int n_heads, int out_dtype, const float *init_state,

@@ -11,6 +11,7 @@
 // address space (pinned host memory under unified addressing): on a GB300's host link, copy-engine
 // uploads next to SM-store downloads moved 303 GB/s together, against 285 GB/s with copy engines in
 // both directions.  Each direction alone runs at the same rate either way (211 GB/s up, 193 down).
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 #include <vector>
@@ -40,6 +41,7 @@ struct Resources {
 constexpr int kMaxDevices = 64;
 Resources g_resources[kMaxDevices];
 std::mutex g_resources_mu;
+std::atomic<long long> g_handles_created{0};   // streams and events created by the staged calls
 
 // The device that `stream` belongs to, which must be the current device (the kernels launch
 // there).  KDA_ERR_INVALID_ARG for another device's stream.
@@ -64,14 +66,20 @@ int device_resources(cudaStream_t stream, Resources **out)
         cudaStream_t *streams[2] = {&r.s_in, &r.s_out};
         cudaEvent_t *events[4] = {&r.start, &r.done, &r.landed, &r.computed};
         for (cudaStream_t *x : streams)
-            if (!*x && cudaStreamCreateWithFlags(x, cudaStreamNonBlocking) != cudaSuccess) {
-                *x = nullptr;
-                return KDA_ERR_CUDA;
+            if (!*x) {
+                if (cudaStreamCreateWithFlags(x, cudaStreamNonBlocking) != cudaSuccess) {
+                    *x = nullptr;
+                    return KDA_ERR_CUDA;
+                }
+                ++g_handles_created;
             }
         for (cudaEvent_t *x : events)
-            if (!*x && cudaEventCreateWithFlags(x, cudaEventDisableTiming) != cudaSuccess) {
-                *x = nullptr;
-                return KDA_ERR_CUDA;
+            if (!*x) {
+                if (cudaEventCreateWithFlags(x, cudaEventDisableTiming) != cudaSuccess) {
+                    *x = nullptr;
+                    return KDA_ERR_CUDA;
+                }
+                ++g_handles_created;
             }
         r.ready = true;
     }
@@ -259,9 +267,12 @@ int run_prefill_staged_static(const void *const h_in[5], const int32_t *h_cu, in
     if (cudaGetSymbolAddress(&tables, g_staged_tables) != cudaSuccess) return KDA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_tables_mu);
     cudaEvent_t &free_ev = g_tables_free[dev];
-    if (!free_ev && cudaEventCreateWithFlags(&free_ev, cudaEventDisableTiming) != cudaSuccess) {
-        free_ev = nullptr;
-        return KDA_ERR_CUDA;
+    if (!free_ev) {
+        if (cudaEventCreateWithFlags(&free_ev, cudaEventDisableTiming) != cudaSuccess) {
+            free_ev = nullptr;
+            return KDA_ERR_CUDA;
+        }
+        ++g_handles_created;
     }
     // the table upload below is ordered after the previous call's prefills (a fresh event counts
     // as complete)
@@ -273,5 +284,7 @@ int run_prefill_staged_static(const void *const h_in[5], const int32_t *h_cu, in
     if (cudaEventRecord(free_ev, stream) != cudaSuccess && rc == KDA_OK) return KDA_ERR_CUDA;
     return rc;
 }
+
+long long staged_handles_created() { return g_handles_created.load(); }
 
 }  // namespace kda

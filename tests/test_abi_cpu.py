@@ -125,6 +125,16 @@ def test_diag_timeout_rejects_out_of_range_cycles(lib):
     assert lib.kda_diag_device_timeout(4_000_000_001, None) == 1
 
 
+def test_diag_staged_handles_counts_without_cuda(lib):
+    import ctypes
+
+    n = ctypes.c_int64(-1)
+    assert lib.kda_diag_staged_handles(ctypes.byref(n)) == 0
+    # nothing creates the staged streams and events but a staged call (none runs without a GPU)
+    assert n.value == 0 or torch.cuda.is_available()
+    assert lib.kda_diag_staged_handles(None) == 1                 # KDA_ERR_INVALID_ARG
+
+
 def _premix(lib, **over):
     args = dict(xq=A, xk=A + 16, xv=A + 32, a=A + 48, b=A + 64, w=A + 80, hist=None, cu=None, n=1,
                 T=16, H=2, d=128, eps=1e-6, dtype=0, q=A + 4096, k=A + 4112, v=A + 4128,

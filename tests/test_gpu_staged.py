@@ -142,6 +142,16 @@ def test_unaligned_chunk_size_is_refused_before_any_work():
     assert kda.device_status() == 0
 
 
+def staged_handles() -> int:
+    import ctypes
+
+    from kimi_delta_attention_13_gb300 import _lib
+
+    n = ctypes.c_int64(-1)
+    assert _lib.load().kda_diag_staged_handles(ctypes.byref(n)) == 0
+    return n.value
+
+
 def test_repeated_calls_reuse_the_device_streams():
     # the staged call keeps two streams and four events per device after its first call; many
     # calls in a row (and from a second stream) stay exact against one kda_prefill
@@ -150,9 +160,13 @@ def test_repeated_calls_reuse_the_device_streams():
     h = host(x)
     bufs = None
     s2 = torch.cuda.Stream(device=DEV)
+    created = []
     for i in range(20):
         out, fin, bufs = kda.prefill_staged(h["q"], h["k"], h["v"], h["g"], h["beta"], None, x["state"],
                                             chunk_tokens=128, buffers=bufs, stream=s2 if i % 2 else None)
         torch.cuda.synchronize()
         assert torch.equal(out, ref_o.cpu()) and torch.equal(fin, ref_f)
+        created.append(staged_handles())
+    # the first call on the device may create the streams and events; no later call creates any
+    assert len(set(created)) == 1, created
     assert kda.device_status() == 0
