@@ -491,6 +491,9 @@ def run_gb300(args):
     cp = context_parallel_figure(dev, stream)
     assert kda.device_status() == 0
     torch.cuda.empty_cache()
+    named = named_workload_figures(dev, stream, hbm_peak)
+    assert kda.device_status() == 0
+    torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
@@ -548,6 +551,7 @@ def run_gb300(args):
                        "GB/s": cp_gbs, "frac": cp_gbs / hbm_peak, "ms": cp_ms},
         "prefix_reuse": reuse,
         "context_parallel": cp,
+        "other_workloads": named,
         "gpu_launches": args.steps,
         "clocks": clk,
         "cpu_baseline": base,
@@ -610,6 +614,48 @@ def prefix_reuse_figure(dev, stream, n_req: int = 4, prefix: int = 16384, new_to
             "cache_hit_tokens_per_s": served / (hit_ms / 1e3),
             "new_tokens_per_s": n_req * new_tokens / (hit_ms / 1e3),
             "speedup": miss_ms / hit_ms, "restored_from_tokens": covered}
+
+
+def named_workload_figures(dev, stream, hbm_peak):
+    """The other two prefill workloads beside the T=8192 step, timed the same way (CUDA events on
+    the launching stream, 2 warm-ups, 3 launches): varlen x8 (8 sequences of U[1024, 32768] tokens,
+    initial and final states) and one sequence of 262,144 tokens with a checkpoint every 4096.
+    Algorithmic bytes: 1,282 B per token-head (bf16 o) plus 64 KB per state read or written."""
+    import torch
+
+    import kimi_delta_attention_13_gb300 as kda
+    from kimi_delta_attention_13_gb300 import synth
+
+    res = {}
+    ws = synth.workloads()
+    for w, key in ((ws[2], "varlen8"), (ws[4], "long_T262144_ckpt4096")):
+        lengths = [int(L) for L in w.lengths]
+        T, N = sum(lengths), len(lengths)
+        x = synth.make_inputs(lengths, heads=H, dtype="bf16", seed=w.seed, device=dev,
+                              init_state=w.init_state)
+        n_ck = kda.num_checkpoints(lengths, w.ckpt_stride) if w.ckpt_stride else 0
+        o = torch.empty(T, H, D, device=dev)
+        fin = torch.empty(N, H, D, D, device=dev)
+        ck = torch.empty(n_ck, H, D, D, device=dev) if n_ck else None
+
+        def step():
+            kda.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], x["state"],
+                        out=o, final_state=fin, ckpt_stride=w.ckpt_stride, ckpts=ck,
+                        lengths=lengths, stream=stream)
+
+        for _ in range(2):
+            step()
+        _, ms = cuda_time_ms(step, 3, stream)
+        states = N * (2 if w.init_state else 1) + n_ck
+        b = T * H * BYTES_PER_TOKEN_HEAD + states * H * STATE_BYTES
+        res[key] = {"workload": f"{w.name}: {N} sequence(s), {T} tokens, H={H}, "
+                                f"{n_ck} checkpoints, fp32 out",
+                    "ms": ms, "tokens_per_s": T / (ms / 1e3), "bytes_alg": b,
+                    "GB/s": b / (ms / 1e3) / 1e9, "frac": b / (ms / 1e3) / 1e9 / hbm_peak,
+                    "longest_sequence": max(lengths)}
+        del x, o, fin, ck
+        torch.cuda.empty_cache()
+    return res
 
 
 def context_parallel_figure(dev, stream, T=262144, heads=8):
