@@ -300,6 +300,8 @@ def cpu_baseline(step, target_s: float = 10.0):
     ok = out_err <= TOL_OUT and (fin_err is None or fin_err <= TOL_STATE)
     parity = {"vs": "fp64 oracle, same inputs", "tokens": tokens, "heads": H,
               "metric": "max|gpu - oracle| / RMS(oracle)", "out": out_err, "final_state": fin_err,
+              "out_precise_mode": (rel_err(step["out_precise"][:tokens].numpy(), o)
+                                   if "out_precise" in step else None),
               "tolerance": {"out": TOL_OUT, "final_state": TOL_STATE}, "pass": ok}
     return base, parity
 
@@ -393,6 +395,18 @@ def run_gb300(args):
     t_flops = flops_alg / (float(peaks.get("bf16_tflops", 1900.0)) * 1e12)
     path = "tensor-core chunked" if kda.prefill_path(D, D, torch.bfloat16) == 1 else "per-token"
 
+    # the same step in the kernel's precise mode (kda_prefill_precise), timed beside it
+    out_p = torch.empty_like(out)
+
+    def precise_step():
+        kda.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], out=out_p, final_state=fin,
+                    stream=stream, precise=True)
+
+    for _ in range(3):
+        precise_step()
+    _, precise_ms = cuda_time_ms(precise_step, max(5, args.steps // 2), stream)
+    assert kda.device_status() == 0
+
     # ---- end to end through the public API: pinned host inputs -> device -> host outputs -----
     hx = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
     h_out = torch.empty(T1, H, D, dtype=torch.float32).pin_memory()
@@ -400,7 +414,9 @@ def run_gb300(args):
     del x
     # the timed step's inputs and results, for the oracle comparison of the CPU-baseline leg
     with_base = rank == 0 and world == 1 and not args.no_cpu_baseline
-    step = {"inputs": hx, "out": out.cpu(), "final": fin.cpu()} if with_base else None
+    step = {"inputs": hx, "out": out.cpu(), "final": fin.cpu(), "out_precise": out_p.cpu()} \
+        if with_base else None
+    del out_p
 
     # the staged prefill: chunks whose uploads, prefills and downloads overlap; device
     # staging buffers are allocated once, as a serving loop would
@@ -535,6 +551,11 @@ def run_gb300(args):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_per,
                 "path": f"kda_prefill_staged from pinned host buffers, {E2E_CHUNK}-token chunks whose "
                         "uploads, prefills and downloads overlap"},
+        "precise_mode": {"workload": "the same prefill through kda_prefill_precise (Aqk carried in "
+                                    "two fp16 parts; outputs' error in parity.out_precise_mode)",
+                         "ms": precise_ms, "tokens_per_s": world * T1 / (precise_ms / 1e3),
+                         "frac": bytes_alg / (precise_ms / 1e3) / 1e9 / hbm_peak,
+                         "time_vs_default": precise_ms / per_ms},
         "premix": {"workload": f"pre-mixer T={T1} H={H} d={D}: width-4 causal conv of xq/xk/xv, "
                                "q/k L2 norm, decay and write gates, bf16 in and out",
                    "GB/s": pm_bytes / (pm_ms / 1e3) / 1e9, "peak": hbm_peak,

@@ -107,6 +107,23 @@ int kda_prefill(const void *q, const void *k, const void *v, const void *g, cons
                 void *out, float *final_state, int32_t ckpt_stride, float *ckpts, void *stream);
 
 /*
+ * kda_prefill_precise -- the same operation, arguments and errors as kda_prefill, with a smaller
+ * output error on the tensor-core path (bf16 inputs, d_k = d_v = 128) at a higher cost.  The
+ * largest rounding in kda_prefill's outputs is that of Aqk (the q.k products of a step, masked
+ * lower-triangular) to fp16, the A operand of the product P = Aqk Bt.  Here Aqk is carried as
+ * fp16(Aqk) plus its fp16 low part through the same product, and P is rounded once after the two
+ * halves are added.  On the T = 8192, 96-head workload this takes the largest output error from
+ * 1.6-1.7e-2 to 0.9-1.1e-2 of RMS (three input draws) for about 1.25x the time; the state error is
+ * unchanged.  Other dtypes and shapes run the per-token path, as in kda_prefill.  Same value range
+ * as kda_prefill.
+ */
+int kda_prefill_precise(const void *q, const void *k, const void *v, const void *g,
+                        const void *beta, const int32_t *cu_seqlens, int32_t n_seqs,
+                        int64_t total_tokens, int32_t n_heads, int32_t d_k, int32_t d_v,
+                        int32_t dtype, int32_t out_dtype, const float *init_state, void *out,
+                        float *final_state, int32_t ckpt_stride, float *ckpts, void *stream);
+
+/*
  * kda_prefill_recurrent -- the same operation and arguments as kda_prefill, always evaluated
  * token by token on CUDA cores (fp32 state in registers).  It is the path kda_prefill takes
  * for fp32 inputs; for bf16 it is a slower second evaluation used to cross-check the

@@ -26,6 +26,7 @@ SIGNATURES = {
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kda_prefill": (ctypes.c_int, _PREFILL_ARGS),
     "kda_prefill_recurrent": (ctypes.c_int, _PREFILL_ARGS),
+    "kda_prefill_precise": (ctypes.c_int, _PREFILL_ARGS),
     "kda_prefill_path": (ctypes.c_int, [_i32, _i32, _i32]),
     "kda_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                    _vp]),

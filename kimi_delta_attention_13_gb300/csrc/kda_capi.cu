@@ -136,6 +136,25 @@ int kda_prefill(const void *q, const void *k, const void *v, const void *g, cons
                                     ckpt_stride, ckpts, (cudaStream_t)stream);
 }
 
+int kda_prefill_precise(const void *q, const void *k, const void *v, const void *g,
+                        const void *beta, const int32_t *cu_seqlens, int32_t n_seqs,
+                        int64_t total_tokens, int32_t n_heads, int32_t d_k, int32_t d_v,
+                        int32_t dtype, int32_t out_dtype, const float *init_state, void *out,
+                        float *final_state, int32_t ckpt_stride, float *ckpts, void *stream)
+{
+    const CallRange range("kda_prefill_precise");
+    int rc = check_prefill(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, n_heads, d_k, d_v,
+                           dtype, out_dtype, init_state, out, final_state, ckpt_stride, ckpts);
+    if (rc != KDA_OK) return rc;
+    if (tc_supported(d_k, d_v, dtype) && total_tokens > 0)
+        return launch_prefill_tc_precise(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens,
+                                         n_heads, out_dtype, init_state, out, final_state,
+                                         ckpt_stride, ckpts, (cudaStream_t)stream);
+    return launch_prefill_recurrent(q, k, v, g, beta, cu_seqlens, n_seqs, total_tokens, n_heads,
+                                    d_k, d_v, dtype, out_dtype, init_state, out, final_state,
+                                    ckpt_stride, ckpts, (cudaStream_t)stream);
+}
+
 int kda_prefill_recurrent(const void *q, const void *k, const void *v, const void *g,
                           const void *beta, const int32_t *cu_seqlens, int32_t n_seqs,
                           int64_t total_tokens, int32_t n_heads, int32_t d_k, int32_t d_v,
@@ -310,7 +329,12 @@ int kda_diag_bounds_check(int32_t run_probe, int32_t *site, void *stream)
 {
     if (!site) return KDA_ERR_INVALID_ARG;
     if (run_probe && kda::launch_bounds_check_probe((cudaStream_t)stream) != KDA_OK) return KDA_ERR_CUDA;
-    return kda::read_and_clear_debug_site((cudaStream_t)stream, site);
+    int32_t a = 0, b = 0;   // the default and the precise build of the tensor-core prefill
+    if (kda::read_and_clear_debug_site((cudaStream_t)stream, &a) != KDA_OK ||
+        kda::read_and_clear_debug_site_precise((cudaStream_t)stream, &b) != KDA_OK)
+        return KDA_ERR_CUDA;
+    *site = a != 0 ? a : b;
+    return KDA_OK;
 }
 
 int kda_device_status(int32_t *status, void *stream)
@@ -321,6 +345,10 @@ int kda_device_status(int32_t *status, void *stream)
     if (rc != KDA_OK) return rc;
     rc = read_and_clear_status_prefill_tc((cudaStream_t)stream, &b);
     if (rc != KDA_OK) return rc;
+    int32_t bp = 0;
+    rc = read_and_clear_status_prefill_tc_precise((cudaStream_t)stream, &bp);
+    if (rc != KDA_OK) return rc;
+    if (b == KDA_OK) b = bp;
     rc = read_and_clear_status_decode((cudaStream_t)stream, &c);
     if (rc != KDA_OK) return rc;
     *status = b != KDA_OK ? b : (c != KDA_OK ? c : a);

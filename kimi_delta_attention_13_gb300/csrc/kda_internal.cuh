@@ -26,6 +26,7 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Per-translation-unit readers of the sticky device error words (see kda_device_status).
 int read_and_clear_status_state_copy(cudaStream_t s, int32_t *status);
 int read_and_clear_status_prefill_tc(cudaStream_t s, int32_t *status);
+int read_and_clear_status_prefill_tc_precise(cudaStream_t s, int32_t *status);
 int read_and_clear_status_decode(cudaStream_t s, int32_t *status);
 // Launch the one-CTA probe whose bounded device wait expires after `cycles` SM cycles.
 int launch_wait_timeout_probe(long long cycles, cudaStream_t stream);
@@ -33,6 +34,7 @@ int launch_wait_timeout_probe(long long cycles, cudaStream_t stream);
 // (and clear) the site number of the first failed bounds check.
 int launch_bounds_check_probe(cudaStream_t stream);
 int read_and_clear_debug_site(cudaStream_t s, int32_t *site);
+int read_and_clear_debug_site_precise(cudaStream_t s, int32_t *site);
 
 // Kernel launchers (host side, no validation: the C ABI validates first).
 int launch_decode(const void *q, const void *k, const void *v, const void *g, const void *beta,
@@ -70,5 +72,11 @@ int launch_prefill_tc(const void *q, const void *k, const void *v, const void *g
                       int64_t total_tokens, int n_heads, int out_dtype, const float *init_state,
                       void *out, float *final_state, int ckpt_stride, float *ckpts,
                       cudaStream_t stream);
+// the same kernel in its precise mode (Aqk carried in two fp16 parts)
+int launch_prefill_tc_precise(const void *q, const void *k, const void *v, const void *g,
+                              const void *beta, const int32_t *cu_seqlens, int n_seqs,
+                              int64_t total_tokens, int n_heads, int out_dtype,
+                              const float *init_state, void *out, float *final_state,
+                              int ckpt_stride, float *ckpts, cudaStream_t stream);
 
 }  // namespace kda

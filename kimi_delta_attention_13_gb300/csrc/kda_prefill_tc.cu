@@ -50,9 +50,28 @@
 // product cancels) therefore run as kind::tf32 on fp32 operands, and every other product as fp16
 // (10-bit mantissa; all their operands are O(1) after the tile scalings); V enters exactly
 // (bf16 times an identity).
+//
+// Precise mode: this file is compiled a second time with KDA_PRECISE=1 (kda_prefill_tc_precise.cu)
+// for kda_prefill_precise.  There warp 3 also writes the low part Aqk - fp16(Aqk) of the output
+// product's A operand as rows 32..63 of the same slot, the P product (unchanged, M = 128) puts
+// fp16(Aqk) Bt in TMEM lanes 0..31 and Aqk_lo Bt in lanes 32..63, and chain warps 4 and 5 add the
+// two before P is rounded to fp16 once: the output error from the rounding of Aqk, the largest
+// term, goes away.  The extra 4 KB per slot comes from the output staging tile, which moves into
+// the step's state-read operand slot (dead once the state reads are done); that slot returns to
+// prep only after the output store has read it, one step later than in the default kernel.
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include <mutex>
+
+#ifndef KDA_PRECISE
+#define KDA_PRECISE 0
+#endif
+#if KDA_PRECISE
+#define KDA_TC_EXPORT(name) name##_precise
+#else
+#define KDA_TC_EXPORT(name) name
+#endif
 
 #include "kda_internal.cuh"
 #include "sm100_ptx.cuh"
@@ -82,37 +101,61 @@ constexpr uint32_t OFF_MMA1B = OFF_VRING + kVStages * TILE_BYTES;
 // rows 0..63 of buffer 1 hold the constant [-I | 0] (B of the V product).
 constexpr uint32_t OFF_KK = OFF_MMA1B + kSlots * 16384;
 // per slot, rows = token (32 rows): bytes 0..63 Aqk fp16 (A of the P product), then P fp16 (B of
-// the output product); bytes 64..127 Bt^T fp16 (B of the P and R products)
+// the output product); bytes 64..127 Bt^T fp16 (B of the P and R products).  Precise mode: 64
+// rows; rows 32..63 hold, in bytes 0..63, the low part Aqk - fp16(Aqk) in fp16 (A rows 32..63 of
+// the same P instructions, so TMEM lanes 32..63 receive Aqk_lo Bt); once P has left TMEM they carry
+// that low part of P in fp32 from chain warp 5 to chain warp 4.
+constexpr uint32_t AB_BYTES = KDA_PRECISE ? 64 * 128 : 32 * 128;
 constexpr uint32_t OFF_AB = OFF_KK + 2 * 16384;
 // Gram operands, fp32 K-major (tf32 product), 4 regions of 32 channels each.  A has M = 128 rows
 // of which 64 are real (32 k-rows, 32 q-rows): each region's descriptor starts 64 rows before
 // it, so the real rows land in TMEM lanes 64..127 (read by warps 2 and 3) and the 64 leading rows
 // read the previous region (or the AB buffers), whose results are ignored.
 constexpr uint32_t GA_REGION = 64 * 128, GB_REGION = 48 * 128;
-constexpr uint32_t OFF_GA = OFF_AB + kSlots * 4096;                  // Gram A: 4 x 8 KB
+constexpr uint32_t OFF_GA = OFF_AB + kSlots * AB_BYTES;              // Gram A: 4 x 8 KB
 constexpr uint32_t OFF_GB = OFF_GA + 4 * GA_REGION;                  // Gram B: 4 x 6 KB (N = 48)
 constexpr uint32_t OFF_BC = OFF_GB + 4 * GB_REGION;                  // step decay b_C, per slot
 constexpr uint32_t OFF_SA = OFF_BC + kSlots * D * 4;                 // A (fp32) 32 x 36
 constexpr uint32_t OFF_TOT = OFF_SA + C * 36 * 4;                    // per-quarter decay totals
 constexpr uint32_t OFF_TB = OFF_TOT + 4 * 64 * 8;                    // T00 | T11 blocks, x2
 constexpr uint32_t OFF_BETA = OFF_TB + 2 * 2048;                     // beta per step parity
+#if KDA_PRECISE
+// (the output tile of a full step is staged for its TMA store in the step's state-read operand
+// slot, dead once the state reads are done)
+constexpr uint32_t OFF_BARS = OFF_BETA + kVStages * C * 4;
+#else
 // output tile of a full step, [32 tokens][128 channels] of the output type, stored by one TMA
 constexpr uint32_t OFF_OSTAGE = OFF_BETA + kVStages * C * 4;
 constexpr uint32_t OFF_BARS = OFF_OSTAGE + C * D * 4;
+#endif
 constexpr uint32_t NUM_BARS = 40;
 constexpr uint32_t OFF_MISC = OFF_BARS + NUM_BARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;                   // alignment slack
 static_assert(SMEM_ALLOC <= 232448, "shared memory per block");
 static_assert(OFF_GA >= GA_REGION, "the first Gram region's leading rows stay inside the buffer");
+#if KDA_PRECISE
+static_assert(C * D * 4 <= 16384 && OFF_MMA1B % 1024 == 0, "an output tile fits a state-read slot");
+static_assert(OFF_AB + (kSlots - 1) * AB_BYTES + 128 * 128 <= OFF_GB, "rows the P product's A descriptor reads");
+#else
 static_assert(OFF_OSTAGE % 128 == 0, "TMA store source alignment");
+#endif
 
 // byte offsets of a slot's buffers; Kbar / R addresses add the slot's half-row offset before the
 // swizzle: kk_base(k) + sw128(row, kk_half(k) + byte)
 __host__ __device__ constexpr uint32_t mma1b_off(int k) { return OFF_MMA1B + k * 16384; }
 __host__ __device__ constexpr uint32_t kk_base(int k) { return OFF_KK + (k >> 1) * 16384; }
 __host__ __device__ constexpr uint32_t kk_half(int k) { return (k & 1) * 64; }
-__host__ __device__ constexpr uint32_t ab_off(int k) { return OFF_AB + k * 4096; }
+__host__ __device__ constexpr uint32_t ab_off(int k) { return OFF_AB + k * AB_BYTES; }
+// the staging tile of a full step's outputs
+__host__ __device__ constexpr uint32_t ostage_off(int slot)
+{
+#if KDA_PRECISE
+    return mma1b_off(slot);
+#else
+    return (void)slot, OFF_OSTAGE;
+#endif
+}
 constexpr int kEyeSlot = 3;   // the [-I | 0] constant sits where a fourth Kbar slot would be
 
 // TMEM column map
@@ -477,6 +520,39 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
                 for (int i = 0; i < 8; ++i) t[i] = __uint_as_float(r[8 * m + i]);
                 store_chunk_f16(kk + sw128(j, kk_half(slot) + 16 * m), t);   // R row = key channel j
             }
+#if KDA_PRECISE
+            if (wq <= 1) {
+                // P = fp16(Aqk) Bt (lanes 0..31, warp 4) + Aqk_lo Bt (lanes 32..63, warp 5): warp 5
+                // hands its rows over in fp32 through rows 32..63 of the slot (A operand rows the P
+                // product has read), warp 4 adds them and rounds P to fp16 once
+                tld32(tb + TM_DP, r);
+                tmem_wait_ld();
+                uint8_t *ab = smem + ab_off(slot);
+                const int rr = j & 31;
+                if (wq == 1) {
+#pragma unroll
+                    for (int m = 0; m < 8; ++m)
+                        if (KDA_SMEM_OK(ab + 32 * 128 + sw128(rr, 16 * m), 16, 19))
+                            *reinterpret_cast<uint4 *>(ab + 32 * 128 + sw128(rr, 16 * m)) =
+                                make_uint4(r[4 * m], r[4 * m + 1], r[4 * m + 2], r[4 * m + 3]);
+                }
+                named_bar_sync(3, 64);
+                if (wq == 0) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        uint4 l0 = make_uint4(0, 0, 0, 0), l1 = l0;
+                        if (KDA_SMEM_OK(ab + 32 * 128 + sw128(rr, 32 * m), 16, 20)) {
+                            l0 = *reinterpret_cast<const uint4 *>(ab + 32 * 128 + sw128(rr, 32 * m));
+                            l1 = *reinterpret_cast<const uint4 *>(ab + 32 * 128 + sw128(rr, 32 * m + 16));
+                        }
+                        const uint32_t lo[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) t[i] = __uint_as_float(r[8 * m + i]) + __uint_as_float(lo[i]);
+                        store_chunk_f16(ab + sw128(j, 16 * m), t);        // P row = token j
+                    }
+                }
+            }
+#else
             if (wq == 0) {
                 tld32(tb + TM_DP, r);
                 tmem_wait_ld();
@@ -488,6 +564,7 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
                     store_chunk_f16(ab + sw128(j, 16 * m), t);        // P row = token j
                 }
             }
+#endif
             fence_proxy_async_smem();
             if (j == 0) KDA_TRACE_EVENT(10, s);
         }
@@ -520,7 +597,9 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
         wait_bar(&bars[B_MMA3_DONE], ph, misc);
         tc_fence_after();
         if (j == 0) KDA_TRACE_EVENT(13, s);
+#if !KDA_PRECISE
         if (j == 0) mbar_arrive(&bars[B_OPS_FREE + slot]);   // this step's operand buffers are free
+#endif
         const long long done = (long long)(s + 1) * C;
         const bool ckpt = p.ckpt_stride > 0 && done <= end - start && (done % p.ckpt_stride) == 0;
         float *ck = nullptr;
@@ -546,6 +625,11 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
         if (j == 0) {
             KDA_TRACE_EVENT(14, s);
             bulk_wait_read_all();   // the previous output tile has left the staging buffer
+#if KDA_PRECISE
+            // that staging buffer is the previous step's state-read slot: every buffer of that
+            // step is now free for prep
+            if (s >= 1) mbar_arrive(&bars[B_OPS_FREE + (s - 1) % kSlots]);
+#endif
         }
         tmem_wait_st();
         tc_fence_before();
@@ -559,8 +643,8 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
             uint32_t r[32];
             tld32(tb + TM_D1 + 64 * buf + 32, r);
             tmem_wait_ld();
-            if (valid == C && KDA_SMEM_OK(reinterpret_cast<TO *>(smem + OFF_OSTAGE) + j, (31 * D + 1) * sizeof(TO), 17)) {
-                TO *st = reinterpret_cast<TO *>(smem + OFF_OSTAGE) + j;
+            if (valid == C && KDA_SMEM_OK(reinterpret_cast<TO *>(smem + ostage_off(slot)) + j, (31 * D + 1) * sizeof(TO), 17)) {
+                TO *st = reinterpret_cast<TO *>(smem + ostage_off(slot)) + j;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) store_out<TO>(st + i * D, __uint_as_float(r[i]));
                 fence_proxy_async_smem();
@@ -577,7 +661,7 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
             KDA_TRACE_EVENT(16, s);
             mbar_arrive(&bars[B_D1_FREE + buf]);   // outputs read: the V product two steps ahead
             if (valid == C) {
-                tma_store_3d(mo, smem + OFF_OSTAGE, 0, h, (int)t0);
+                tma_store_3d(mo, smem + ostage_off(slot), 0, h, (int)t0);
                 bulk_commit();
             }
         }
@@ -1013,6 +1097,11 @@ __device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nstep
 #pragma unroll
                 for (int i = 0; i < 8; ++i) t[i] = (8 * m + i <= r) ? g.at(r, 8 * m + i) : 0.f;
                 store_chunk_f16(ab + sw128(r, m * 16), t);          // Aqk row r
+#if KDA_PRECISE
+#pragma unroll
+                for (int i = 0; i < 8; ++i) t[i] -= __half2float(__float2half_rn(t[i]));   // exact in fp32
+                store_chunk_f16(ab + sw128(32 + r, m * 16), t);     // and what fp16(Aqk) rounded off
+#endif
             }
             ok = wait_bar(&bars[B_T_READY + buf], (s >> 1) & 1, misc);
             if (!__all_sync(0xffffffffu, ok)) break;
@@ -1265,6 +1354,7 @@ int launch_typed(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap
 
 }  // namespace
 
+#if !KDA_PRECISE
 namespace {
 
 // One CTA whose bounded wait is on a barrier that nothing ever completes: the same wait the prefill
@@ -1298,7 +1388,14 @@ int launch_bounds_check_probe(cudaStream_t stream)
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
-int read_and_clear_debug_site(cudaStream_t s, int32_t *site)
+int launch_wait_timeout_probe(long long cycles, cudaStream_t stream)
+{
+    wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(cycles);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+#endif
+
+int KDA_TC_EXPORT(read_and_clear_debug_site)(cudaStream_t s, int32_t *site)
 {
     int host = 0, zero = 0;
     if (cudaMemcpyFromSymbolAsync(&host, g_prefill_tc_debug_site, sizeof(int), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
@@ -1309,13 +1406,7 @@ int read_and_clear_debug_site(cudaStream_t s, int32_t *site)
     return KDA_OK;
 }
 
-int launch_wait_timeout_probe(long long cycles, cudaStream_t stream)
-{
-    wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(cycles);
-    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
-}
-
-int read_and_clear_status_prefill_tc(cudaStream_t s, int32_t *status)
+int KDA_TC_EXPORT(read_and_clear_status_prefill_tc)(cudaStream_t s, int32_t *status)
 {
     int host = 0, zero = 0;
     if (cudaMemcpyFromSymbolAsync(&host, g_prefill_tc_error, sizeof(int), 0,
@@ -1329,7 +1420,7 @@ int read_and_clear_status_prefill_tc(cudaStream_t s, int32_t *status)
     return KDA_OK;
 }
 
-int launch_prefill_tc(const void *q, const void *k, const void *v, const void *g,
+int KDA_TC_EXPORT(launch_prefill_tc)(const void *q, const void *k, const void *v, const void *g,
                       const void *beta, const int32_t *cu_seqlens, int n_seqs,
                       int64_t total_tokens, int n_heads, int out_dtype, const float *init_state,
                       void *out, float *final_state, int ckpt_stride, float *ckpts,
@@ -1358,7 +1449,7 @@ int launch_prefill_tc(const void *q, const void *k, const void *v, const void *g
     return launch_typed<float>(mq, mk, mg, mv, mo, p, (int)blocks, stream);
 }
 
-#ifdef KDA_TRACE
+#if defined(KDA_TRACE) && !KDA_PRECISE
 extern "C" int kda_trace_read(long long *dst)
 {
     return cudaMemcpyFromSymbol(dst, g_kda_trace, sizeof(g_kda_trace)) == cudaSuccess ? 0 : 1;

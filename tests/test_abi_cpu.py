@@ -60,12 +60,12 @@ def test_prefill_path(lib):
 A = 1 << 20  # a fake, 16-byte aligned "device address" that is never dereferenced
 
 
-def _prefill(lib, **over):
+def _prefill(lib, entry="kda_prefill", **over):
     args = dict(q=A, k=A + 16, v=A + 32, g=A + 48, beta=A + 64, cu=None, n=1, T=16, H=2, dk=128,
                 dv=128, dtype=0, odt=1, init=None, out=A + 80, fin=None, stride=0, ckpts=None,
                 stream=None)
     args.update(over)
-    return lib.kda_prefill(args["q"], args["k"], args["v"], args["g"], args["beta"], args["cu"],
+    return getattr(lib, entry)(args["q"], args["k"], args["v"], args["g"], args["beta"], args["cu"],
                            args["n"], args["T"], args["H"], args["dk"], args["dv"], args["dtype"],
                            args["odt"], args["init"], args["out"], args["fin"], args["stride"],
                            args["ckpts"], args["stream"])
@@ -82,8 +82,11 @@ def _prefill(lib, **over):
     (dict(q=A + 8), 3), (dict(fin=A + 100), 3), (dict(cu=A + 2), 3),
     (dict(dk=129, dtype=1), 2), (dict(dk=130, dtype=1), 2), (dict(dk=60, dv=64, dtype=0), 2),
 ])
-def test_prefill_rejects(lib, over, code):
-    assert _prefill(lib, **over) == code
+@pytest.mark.parametrize("entry", ["kda_prefill", "kda_prefill_precise", "kda_prefill_recurrent"])
+def test_prefill_rejects(lib, over, code, entry):
+    if entry == "kda_prefill_recurrent" and code == 2:
+        return   # the per-token path takes other head sizes; its own limits are checked below
+    assert _prefill(lib, entry, **over) == code
 
 
 def test_recurrent_rejects_unsupported_dv(lib):

@@ -6,7 +6,7 @@ and the lanes the executing warp may reach; a failed check skips the access and 
 KDA_ERR_DEVICE_BOUNDS (and the check's site) instead of trapping.  Here: the check records a
 failure (kda_diag_bounds_check runs it on an out-of-window offset, with no access), and the
 debug build runs the small cases, ragged tails and checkpoints included, without a failed check
-and within the oracle's bounds."""
+and within the oracle's bounds, in the default and the precise kernel."""
 import ctypes
 
 import pytest
@@ -59,8 +59,9 @@ def test_a_failed_check_is_recorded_and_cleared():
     assert_close("out", out, ro, TOL["bf16"]["out"])
 
 
+@pytest.mark.parametrize("entry", ["kda_prefill", "kda_prefill_precise"])
 @pytest.mark.parametrize("lengths", [[1], [15], [16], [17], [33], [100, 5, 0, 64]])
-def test_debug_build_small_cases(dlib, lengths):
+def test_debug_build_small_cases(dlib, lengths, entry):
     H, stride = 2, 32
     x = synth.make_inputs(lengths, heads=H, dtype="bf16", seed=112 + sum(lengths), device=DEV,
                           init_state=True)
@@ -70,9 +71,9 @@ def test_debug_build_small_cases(dlib, lengths):
     slots = kda.num_checkpoints(lengths, stride)
     ck = torch.empty((max(slots, 1), H, 128, 128), device=DEV)
     p = lambda t: None if t is None else t.data_ptr()  # noqa: E731
-    rc = dlib.kda_prefill(p(x["q"]), p(x["k"]), p(x["v"]), p(x["g"]), p(x["beta"]), p(x["cu_seqlens"]), n, T, H,
-                          128, 128, 0, 1, p(x["state"]), p(out), p(fin), stride if slots else 0,
-                          p(ck) if slots else None, None)
+    rc = getattr(dlib, entry)(p(x["q"]), p(x["k"]), p(x["v"]), p(x["g"]), p(x["beta"]), p(x["cu_seqlens"]), n,
+                              T, H, 128, 128, 0, 1, p(x["state"]), p(out), p(fin), stride if slots else 0,
+                              p(ck) if slots else None, None)
     assert rc == 0
     torch.cuda.synchronize()
     assert _status(dlib) == 0 and _site(dlib) == 0   # no bounds check failed
