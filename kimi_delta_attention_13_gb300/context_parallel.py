@@ -58,21 +58,28 @@ def cp_combine(s_loc, m, seq_seg, s_start, final_state=None, stream=None):
     device; seq_seg: n_seqs + 1 segment indices, a host list or an int32 tensor on the device;
     final_state: fp32 [n_seqs, H, 128, 128] or None.  s_start of each sequence's first segment is
     left as it is."""
-    lib = _lib.load()
     dev = s_loc.device
     n_seg, H, D = s_loc.shape[0], s_loc.shape[1], s_loc.shape[2]
+    if not isinstance(seq_seg, torch.Tensor):
+        seq_seg = [int(v) for v in seq_seg]
+        if not seq_seg or seq_seg[0] != 0 or seq_seg[-1] > n_seg or any(
+                b < a for a, b in zip(seq_seg, seq_seg[1:])):
+            raise ValueError(f"seq_seg must rise from 0 to at most {n_seg} segments")
     for name, t in (("s_loc", s_loc), ("m", m), ("s_start", s_start)):
         _require(t, name, dev, torch.float32, (n_seg, H, D, D))
     if isinstance(seq_seg, torch.Tensor):
+        # a device table is taken as it is (its values are not read back to the host), like
+        # cu_seqlens: non-decreasing, from 0 to at most n_seg
         _require(seq_seg, "seq_seg", dev, torch.int32)
-        if seq_seg.dim() != 1:
-            raise ValueError("seq_seg must be one-dimensional")
+        if seq_seg.dim() != 1 or seq_seg.numel() < 1:
+            raise ValueError("seq_seg must be one-dimensional and non-empty")
     if final_state is not None:
         _require(final_state, "final_state", dev, torch.float32, (len(seq_seg) - 1, H, D, D))
+    lib = _lib.load()
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     with torch.cuda.stream(s):
         seq_seg_t = seq_seg if isinstance(seq_seg, torch.Tensor) else \
-            torch.tensor(list(seq_seg), dtype=torch.int32, device=dev)
+            torch.tensor(seq_seg, dtype=torch.int32, device=dev)
         rc = lib.kda_cp_combine(_ptr(s_loc), _ptr(m), _ptr(seq_seg_t), len(seq_seg) - 1, H, D,
                                 _ptr(s_start), _ptr(final_state) if final_state is not None else None,
                                 _stream(dev, s))

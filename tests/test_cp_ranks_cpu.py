@@ -127,3 +127,15 @@ def test_two_ranks_match_the_whole_prefill():
     srms = float(np.sqrt(np.mean(rf ** 2)))
     for n, f in seen.items():
         assert float(np.max(np.abs(f - rf[n]))) <= 1e-9 * srms
+
+
+def test_cp_combine_refuses_a_bad_segment_table():
+    # checked on the host before anything reaches the device (no GPU needed to see the refusal)
+    import torch
+
+    from kimi_delta_attention_13_gb300.context_parallel import cp_combine
+
+    t = torch.zeros(3, 1, 128, 128)
+    for bad in ([1, 3], [0, 2, 1, 3], [0, 4], []):
+        with pytest.raises(ValueError, match="seq_seg"):
+            cp_combine(t, t, bad, t)
