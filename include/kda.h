@@ -111,10 +111,10 @@ int kda_prefill(const void *q, const void *k, const void *v, const void *g, cons
  * output error on the tensor-core path (bf16 inputs, d_k = d_v = 128) at a higher cost.  The
  * largest rounding in kda_prefill's outputs is that of Aqk (the q.k products of a step, masked
  * lower-triangular) to fp16, the A operand of the product P = Aqk Bt.  Here Aqk is carried as
- * fp16(Aqk) plus its fp16 low part through the same product, and P is rounded once after the two
- * halves are added.  On the T = 8192, 96-head workload this takes the largest output error from
- * 1.6-1.7e-2 to 0.9-1.1e-2 of RMS (three input draws) for about 1.25x the time; the state error is
- * unchanged.  Other dtypes and shapes run the per-token path, as in kda_prefill.  Same value range
+ * fp16(Aqk) plus its fp16 low part through two accumulating products, and P is rounded once.
+ * On the T = 8192, 96-head workload this takes the largest output error from 1.6-1.7e-2 to
+ * 0.9-1.1e-2 of RMS (three input draws) for about 1.09x the time; final states and checkpoints are
+ * bit-identical to kda_prefill's.  Other dtypes and shapes run the per-token path, as in kda_prefill.  Same value range
  * as kda_prefill.
  */
 int kda_prefill_precise(const void *q, const void *k, const void *v, const void *g,

@@ -133,7 +133,7 @@ def prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, *, out=None, fin
     [N, H, d_k, d_v] or None (zeros).  final_state: True to allocate, a tensor to fill, or
     None/False.  ckpt_stride: 0 or a multiple of 32.  out_dtype: float32 (default, the
     accumulation precision) or bfloat16.  precise: the tensor-core kernel's precise mode (about
-    40 % smaller output error, about 1.25x the time).  Returns (out, final_state, ckpts).
+    35 % smaller output error, about 1.09x the time).  Returns (out, final_state, ckpts).
     """
     return _prefill("kda_prefill_precise" if precise else "kda_prefill", q, k, v, g, beta,
                     cu_seqlens, init_state, out, final_state, ckpt_stride, ckpts, lengths, stream,

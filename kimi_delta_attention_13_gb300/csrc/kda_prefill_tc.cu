@@ -53,12 +53,11 @@
 //
 // Precise mode: this file is compiled a second time with KDA_PRECISE=1 (kda_prefill_tc_precise.cu)
 // for kda_prefill_precise.  There warp 3 also writes the low part Aqk - fp16(Aqk) of the output
-// product's A operand as rows 32..63 of the same slot, the P product (unchanged, M = 128) puts
-// fp16(Aqk) Bt in TMEM lanes 0..31 and Aqk_lo Bt in lanes 32..63, and chain warps 4 and 5 add the
-// two before P is rounded to fp16 once: the output error from the rounding of Aqk, the largest
-// term, goes away.  The extra 4 KB per slot comes from the output staging tile, which moves into
-// the step's state-read operand slot (dead once the state reads are done); that slot returns to
-// prep only after the output store has read it, one step later than in the default kernel.
+// product's A operand (exact in fp32, then rounded to fp16), and the P product accumulates
+// Aqk_lo Bt onto fp16(Aqk) Bt in TMEM with two more MMAs, before P is rounded to fp16 once: the
+// output error from the rounding of Aqk, the largest term, goes away.  The low parts take the
+// unused lower half of the [-I | 0] constant's buffer (two slots) and one v stage (the third
+// slot): the v ring is two deep in this mode.
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
@@ -89,7 +88,7 @@ constexpr long long kTimeout = 4000000000ll;     // bounded waits: 4e9 SM cycles
 // shared memory map (bytes from a 1024-aligned base)
 constexpr int kQStages = 1;                                // q, k, g stage (read by prep)
 constexpr int kSlots = 3;                                  // depth of the prep -> chain buffers
-constexpr int kVStages = 3;                                // v ring (read by the V product)
+constexpr int kVStages = KDA_PRECISE ? 2 : 3;              // v ring (read by the V product)
 constexpr uint32_t TILE_BYTES = 2 * C * 128;               // 64 channels x 32 rows x 2 halves
 constexpr uint32_t QSTAGE_BYTES = 3 * TILE_BYTES;          // q, k, g
 constexpr uint32_t OFF_QRING = 0;
@@ -101,45 +100,35 @@ constexpr uint32_t OFF_MMA1B = OFF_VRING + kVStages * TILE_BYTES;
 // rows 0..63 of buffer 1 hold the constant [-I | 0] (B of the V product).
 constexpr uint32_t OFF_KK = OFF_MMA1B + kSlots * 16384;
 // per slot, rows = token (32 rows): bytes 0..63 Aqk fp16 (A of the P product), then P fp16 (B of
-// the output product); bytes 64..127 Bt^T fp16 (B of the P and R products).  Precise mode: 64
-// rows; rows 32..63 hold, in bytes 0..63, the low part Aqk - fp16(Aqk) in fp16 (A rows 32..63 of
-// the same P instructions, so TMEM lanes 32..63 receive Aqk_lo Bt); once P has left TMEM they carry
-// that low part of P in fp32 from chain warp 5 to chain warp 4.
-constexpr uint32_t AB_BYTES = KDA_PRECISE ? 64 * 128 : 32 * 128;
+// the output product); bytes 64..127 Bt^T fp16 (B of the P and R products)
+constexpr uint32_t AB_BYTES = 32 * 128;
 constexpr uint32_t OFF_AB = OFF_KK + 2 * 16384;
+// precise mode: the third slot's Aqk low part (32 rows of 128 bytes, bytes 0..63 used)
+constexpr uint32_t OFF_ALO2 = OFF_AB + kSlots * AB_BYTES;
+constexpr uint32_t ALO2_BYTES = KDA_PRECISE ? 32 * 128 : 0;
 // Gram operands, fp32 K-major (tf32 product), 4 regions of 32 channels each.  A has M = 128 rows
 // of which 64 are real (32 k-rows, 32 q-rows): each region's descriptor starts 64 rows before
 // it, so the real rows land in TMEM lanes 64..127 (read by warps 2 and 3) and the 64 leading rows
 // read the previous region (or the AB buffers), whose results are ignored.
 constexpr uint32_t GA_REGION = 64 * 128, GB_REGION = 48 * 128;
-constexpr uint32_t OFF_GA = OFF_AB + kSlots * AB_BYTES;              // Gram A: 4 x 8 KB
+constexpr uint32_t OFF_GA = OFF_ALO2 + ALO2_BYTES;                   // Gram A: 4 x 8 KB
 constexpr uint32_t OFF_GB = OFF_GA + 4 * GA_REGION;                  // Gram B: 4 x 6 KB (N = 48)
 constexpr uint32_t OFF_BC = OFF_GB + 4 * GB_REGION;                  // step decay b_C, per slot
 constexpr uint32_t OFF_SA = OFF_BC + kSlots * D * 4;                 // A (fp32) 32 x 36
 constexpr uint32_t OFF_TOT = OFF_SA + C * 36 * 4;                    // per-quarter decay totals
 constexpr uint32_t OFF_TB = OFF_TOT + 4 * 64 * 8;                    // T00 | T11 blocks, x2
 constexpr uint32_t OFF_BETA = OFF_TB + 2 * 2048;                     // beta per step parity
-#if KDA_PRECISE
-// (the output tile of a full step is staged for its TMA store in the step's state-read operand
-// slot, dead once the state reads are done)
-constexpr uint32_t OFF_BARS = OFF_BETA + kVStages * C * 4;
-#else
 // output tile of a full step, [32 tokens][128 channels] of the output type, stored by one TMA
-constexpr uint32_t OFF_OSTAGE = OFF_BETA + kVStages * C * 4;
+constexpr uint32_t OFF_OSTAGE = OFF_BETA + 3 * C * 4;
 constexpr uint32_t OFF_BARS = OFF_OSTAGE + C * D * 4;
-#endif
 constexpr uint32_t NUM_BARS = 40;
 constexpr uint32_t OFF_MISC = OFF_BARS + NUM_BARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;                   // alignment slack
 static_assert(SMEM_ALLOC <= 232448, "shared memory per block");
 static_assert(OFF_GA >= GA_REGION, "the first Gram region's leading rows stay inside the buffer");
-#if KDA_PRECISE
-static_assert(C * D * 4 <= 16384 && OFF_MMA1B % 1024 == 0, "an output tile fits a state-read slot");
-static_assert(OFF_AB + (kSlots - 1) * AB_BYTES + 128 * 128 <= OFF_GB, "rows the P product's A descriptor reads");
-#else
 static_assert(OFF_OSTAGE % 128 == 0, "TMA store source alignment");
-#endif
+static_assert(OFF_MMA1B % 1024 == 0 && OFF_ALO2 % 1024 == 0, "128-byte swizzle atoms");
 
 // byte offsets of a slot's buffers; Kbar / R addresses add the slot's half-row offset before the
 // swizzle: kk_base(k) + sw128(row, kk_half(k) + byte)
@@ -147,16 +136,18 @@ __host__ __device__ constexpr uint32_t mma1b_off(int k) { return OFF_MMA1B + k *
 __host__ __device__ constexpr uint32_t kk_base(int k) { return OFF_KK + (k >> 1) * 16384; }
 __host__ __device__ constexpr uint32_t kk_half(int k) { return (k & 1) * 64; }
 __host__ __device__ constexpr uint32_t ab_off(int k) { return OFF_AB + k * AB_BYTES; }
-// the staging tile of a full step's outputs
-__host__ __device__ constexpr uint32_t ostage_off(int slot)
-{
-#if KDA_PRECISE
-    return mma1b_off(slot);
-#else
-    return (void)slot, OFF_OSTAGE;
-#endif
-}
 constexpr int kEyeSlot = 3;   // the [-I | 0] constant sits where a fourth Kbar slot would be
+// precise mode: where slot k's Aqk low part starts (rows of 128 bytes; add alo_half(k) to a byte
+// offset before the swizzle).  Slots 0 and 1: rows 64..95 and 96..127 of the constant's half of
+// the second Kbar buffer, which the constant (rows 0..63) leaves free; slot 2: its own region.
+// As an M = 128 A operand each descriptor also reads the 96 rows after its slot (ignored lanes),
+// all inside shared memory.
+__host__ __device__ constexpr uint32_t alo_rows(int k)
+{
+    return k < 2 ? OFF_KK + 16384 + (64 + 32 * k) * 128 : OFF_ALO2;
+}
+__host__ __device__ constexpr uint32_t alo_half(int k) { return k < 2 ? 64 : 0; }
+static_assert(kk_base(kEyeSlot) == OFF_KK + 16384 && kk_half(kEyeSlot) == 64, "low parts beside the constant");
 
 // TMEM column map
 constexpr uint32_t TM_S32 = 0;      // fp32 state S^T (lane j, column = key channel)
@@ -455,6 +446,11 @@ __device__ __forceinline__ void issue_pr(uint32_t tm, uint32_t sb, int slot, uin
     const uint64_t bt = desc_at(ab, 64);
     mma_ss(tm + TM_DP, ab, bt, I_PR, 0);
     mma_ss(tm + TM_DP, desc_at(ab, 32), desc_at(bt, 32), I_PR, 1);
+#if KDA_PRECISE
+    const uint64_t lo = smem_desc(sb + alo_rows(slot) + alo_half(slot), 0, 1024);   // + Aqk_lo Bt
+    mma_ss(tm + TM_DP, lo, bt, I_PR, 1);
+    mma_ss(tm + TM_DP, desc_at(lo, 32), desc_at(bt, 32), I_PR, 1);
+#endif
     mma_ss(tm + TM_DR, kk, bt, I_PR, 0);
     mma_ss(tm + TM_DR, desc_at(kk, 32), desc_at(bt, 32), I_PR, 1);
     mma_commit(done);
@@ -520,39 +516,6 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
                 for (int i = 0; i < 8; ++i) t[i] = __uint_as_float(r[8 * m + i]);
                 store_chunk_f16(kk + sw128(j, kk_half(slot) + 16 * m), t);   // R row = key channel j
             }
-#if KDA_PRECISE
-            if (wq <= 1) {
-                // P = fp16(Aqk) Bt (lanes 0..31, warp 4) + Aqk_lo Bt (lanes 32..63, warp 5): warp 5
-                // hands its rows over in fp32 through rows 32..63 of the slot (A operand rows the P
-                // product has read), warp 4 adds them and rounds P to fp16 once
-                tld32(tb + TM_DP, r);
-                tmem_wait_ld();
-                uint8_t *ab = smem + ab_off(slot);
-                const int rr = j & 31;
-                if (wq == 1) {
-#pragma unroll
-                    for (int m = 0; m < 8; ++m)
-                        if (KDA_SMEM_OK(ab + 32 * 128 + sw128(rr, 16 * m), 16, 19))
-                            *reinterpret_cast<uint4 *>(ab + 32 * 128 + sw128(rr, 16 * m)) =
-                                make_uint4(r[4 * m], r[4 * m + 1], r[4 * m + 2], r[4 * m + 3]);
-                }
-                named_bar_sync(3, 64);
-                if (wq == 0) {
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        uint4 l0 = make_uint4(0, 0, 0, 0), l1 = l0;
-                        if (KDA_SMEM_OK(ab + 32 * 128 + sw128(rr, 32 * m), 16, 20)) {
-                            l0 = *reinterpret_cast<const uint4 *>(ab + 32 * 128 + sw128(rr, 32 * m));
-                            l1 = *reinterpret_cast<const uint4 *>(ab + 32 * 128 + sw128(rr, 32 * m + 16));
-                        }
-                        const uint32_t lo[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) t[i] = __uint_as_float(r[8 * m + i]) + __uint_as_float(lo[i]);
-                        store_chunk_f16(ab + sw128(j, 16 * m), t);        // P row = token j
-                    }
-                }
-            }
-#else
             if (wq == 0) {
                 tld32(tb + TM_DP, r);
                 tmem_wait_ld();
@@ -564,7 +527,6 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
                     store_chunk_f16(ab + sw128(j, 16 * m), t);        // P row = token j
                 }
             }
-#endif
             fence_proxy_async_smem();
             if (j == 0) KDA_TRACE_EVENT(10, s);
         }
@@ -597,9 +559,7 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
         wait_bar(&bars[B_MMA3_DONE], ph, misc);
         tc_fence_after();
         if (j == 0) KDA_TRACE_EVENT(13, s);
-#if !KDA_PRECISE
         if (j == 0) mbar_arrive(&bars[B_OPS_FREE + slot]);   // this step's operand buffers are free
-#endif
         const long long done = (long long)(s + 1) * C;
         const bool ckpt = p.ckpt_stride > 0 && done <= end - start && (done % p.ckpt_stride) == 0;
         float *ck = nullptr;
@@ -625,11 +585,6 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
         if (j == 0) {
             KDA_TRACE_EVENT(14, s);
             bulk_wait_read_all();   // the previous output tile has left the staging buffer
-#if KDA_PRECISE
-            // that staging buffer is the previous step's state-read slot: every buffer of that
-            // step is now free for prep
-            if (s >= 1) mbar_arrive(&bars[B_OPS_FREE + (s - 1) % kSlots]);
-#endif
         }
         tmem_wait_st();
         tc_fence_before();
@@ -643,8 +598,8 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
             uint32_t r[32];
             tld32(tb + TM_D1 + 64 * buf + 32, r);
             tmem_wait_ld();
-            if (valid == C && KDA_SMEM_OK(reinterpret_cast<TO *>(smem + ostage_off(slot)) + j, (31 * D + 1) * sizeof(TO), 17)) {
-                TO *st = reinterpret_cast<TO *>(smem + ostage_off(slot)) + j;
+            if (valid == C && KDA_SMEM_OK(reinterpret_cast<TO *>(smem + OFF_OSTAGE) + j, (31 * D + 1) * sizeof(TO), 17)) {
+                TO *st = reinterpret_cast<TO *>(smem + OFF_OSTAGE) + j;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) store_out<TO>(st + i * D, __uint_as_float(r[i]));
                 fence_proxy_async_smem();
@@ -661,7 +616,7 @@ __device__ void chain_role(const Params &p, const CUtensorMap *mo, uint8_t *smem
             KDA_TRACE_EVENT(16, s);
             mbar_arrive(&bars[B_D1_FREE + buf]);   // outputs read: the V product two steps ahead
             if (valid == C) {
-                tma_store_3d(mo, smem + ostage_off(slot), 0, h, (int)t0);
+                tma_store_3d(mo, smem + OFF_OSTAGE, 0, h, (int)t0);
                 bulk_commit();
             }
         }
@@ -1100,7 +1055,7 @@ __device__ void solver_role(uint8_t *smem, uint64_t *bars, Misc *misc, int nstep
 #if KDA_PRECISE
 #pragma unroll
                 for (int i = 0; i < 8; ++i) t[i] -= __half2float(__float2half_rn(t[i]));   // exact in fp32
-                store_chunk_f16(ab + sw128(32 + r, m * 16), t);     // and what fp16(Aqk) rounded off
+                store_chunk_f16(smem + alo_rows(slot) + sw128(r, alo_half(slot) + m * 16), t);   // Aqk_lo
 #endif
             }
             ok = wait_bar(&bars[B_T_READY + buf], (s >> 1) & 1, misc);
@@ -1247,7 +1202,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         for (int b = 0; b < 2; ++b) mbar_init(&bars[B_EXTR_DONE + b], 2);   // warps 2 and 3
         mbar_init(&bars[B_SA_FREE], 2);                                      // solver warps 1 and 3
         for (int b = 0; b < kSlots; ++b) mbar_init(&bars[B_BT_READY + b], 2);
-        static_assert(B_OPS_READY == B_VEMPTY + kVStages, "barrier layout");
+        static_assert(B_VEMPTY >= B_VFULL + kVStages && B_OPS_READY >= B_VEMPTY + kVStages, "barrier layout");
         fence_barrier_init();
     }
     if (warp == 0) {
