@@ -3,9 +3,12 @@
 decode state GB/s (N=256, H=96), against the HBM roofline.
 
 One step = one kda_prefill of the 8192-token, 96-head workload (inputs resident in HBM).
-The decode (256 sequences x 96 heads, 1.6 GB fp32 state updated in place), a checkpoint
-restore (kda_state_copy of 64 states), the pre-mixer and the output gate on the same token grid,
-and a prefix-reuse (cache-hit) prefill are timed in the same run and reported beside it.
+The same step through kda_prefill_precise, the decode (256 sequences x 96 heads, 1.6 GB fp32
+state updated in place), a checkpoint restore (kda_state_copy of 64 states), the pre-mixer and the
+output gate on the same token grid, a prefix-reuse (cache-hit) prefill, the context-parallel
+prefill of one 262,144-token sequence at 8 heads (and its scan alone), and the varlen x8 and
+262,144-token (64 checkpoints) prefills at 96 heads are timed in the same run and reported beside
+it.
 
     python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 
