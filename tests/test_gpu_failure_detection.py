@@ -60,7 +60,7 @@ def _guards_intact(buf):
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("path", ["prefill", "recurrent"])
+@pytest.mark.parametrize("path", ["prefill", "precise", "recurrent"])
 def test_writes_stay_inside_their_buffers(path, out_dtype):
     # sequences ending on a full step, on a ragged tail, shorter than a step, and empty
     lengths, H, stride = [128, 100, 5, 0, 64], 3, 64
@@ -70,9 +70,10 @@ def test_writes_stay_inside_their_buffers(path, out_dtype):
     obuf, out = _guarded((T, H, 128), out_dtype)
     fbuf, fin = _guarded((N, H, 128, 128), torch.float32)
     cbuf, ck = _guarded((n_ck, H, 128, 128), torch.float32)
-    fn = kda.prefill if path == "prefill" else kda.prefill_recurrent
+    fn = kda.prefill_recurrent if path == "recurrent" else kda.prefill
+    kw = {"precise": True} if path == "precise" else {}
     fn(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], x["state"], out=out,
-       final_state=fin, ckpts=ck, ckpt_stride=stride, lengths=lengths, out_dtype=out_dtype)
+       final_state=fin, ckpts=ck, ckpt_stride=stride, lengths=lengths, out_dtype=out_dtype, **kw)
     torch.cuda.synchronize()
     assert kda.device_status() == 0
     for name, b in (("out", obuf), ("final_state", fbuf), ("ckpts", cbuf)):

@@ -34,13 +34,14 @@ def capture(fn):
     return graph
 
 
-def test_prefill_graph_replays_bit_identically():
+@pytest.mark.parametrize("precise", [False, True])
+def test_prefill_graph_replays_bit_identically(precise):
     x = synth.make_inputs([300, 1, 700], heads=4, dtype="bf16", seed=91, device=DEV, init_state=True)
     args = lambda: (x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], x["state"])  # noqa: E731
-    ref_o, ref_f, ref_c = kda.prefill(*args(), ckpt_stride=128, lengths=x["lengths"])
+    ref_o, ref_f, ref_c = kda.prefill(*args(), ckpt_stride=128, lengths=x["lengths"], precise=precise)
     out, fin, ck = torch.empty_like(ref_o), torch.empty_like(ref_f), torch.empty_like(ref_c)
     graph = capture(lambda: kda.prefill(*args(), out=out, final_state=fin, ckpt_stride=128, ckpts=ck,
-                                        lengths=x["lengths"]))
+                                        lengths=x["lengths"], precise=precise))
     for t in (out, fin, ck):
         t.fill_(float("nan"))
     graph.replay()
@@ -49,7 +50,7 @@ def test_prefill_graph_replays_bit_identically():
     # new values in the same input buffers: the replay computes with them
     x["v"].mul_(0.5)
     x["state"].mul_(-1.0)
-    ref2_o, ref2_f, _ = kda.prefill(*args(), ckpt_stride=128, lengths=x["lengths"])
+    ref2_o, ref2_f, _ = kda.prefill(*args(), ckpt_stride=128, lengths=x["lengths"], precise=precise)
     graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, ref2_o) and torch.equal(fin, ref2_f)
