@@ -191,7 +191,9 @@ class ClockSampler:
                     parts = [x.strip() for x in line.split(",")]
                     if len(parts) >= 9:
                         rows.append(parts)
+        if self.path is not None and os.path.exists(self.path):   # also when nvidia-smi never ran
             os.unlink(self.path)
+        self.path = None
         return summarize_clocks(rows, fast, self.nvml.max_mhz)
 
 

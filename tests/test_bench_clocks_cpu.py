@@ -37,3 +37,21 @@ def test_sampler_without_driver_library_degrades():
     s.start()
     out = s.stop()
     assert "sm_mhz" in out and "reasons" in out
+
+
+def test_sampler_leaves_no_temp_file(monkeypatch):
+    # without nvidia-smi (or with it) the sampler's temp file is gone after stop()
+    import os
+
+    import bench
+
+    def no_smi(*a, **k):
+        raise FileNotFoundError("nvidia-smi")
+
+    monkeypatch.setattr(bench.subprocess, "Popen", no_smi)
+    c = bench.ClockSampler(0)
+    c.start()
+    path = c.path
+    assert path is not None and os.path.exists(path)
+    c.stop()
+    assert not os.path.exists(path)
