@@ -311,6 +311,33 @@ def cpu_baseline(step, target_s: float = 10.0):
     return base, parity
 
 
+def other_parity(named) -> None:
+    """The CPU-baseline leg's oracle comparison for the other workloads: each figure's kept head
+    sample against the fp64 oracle on the same inputs (outputs, final states, checkpoints), as
+    max|gpu - oracle| / RMS(oracle) against the same bounds."""
+    import oracle
+
+    orc = oracle.default()
+    cores = int(os.cpu_count() or 1)
+    for fig in named.values():
+        c = fig.pop("_check", None)
+        if c is None:
+            continue
+        x = c["inputs"]
+        t0 = time.perf_counter()
+        ro, rf, rc = orc.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], c["cu"], c["init"],
+                                 ckpt_stride=c["ckpt_stride"], threads=cores)
+        par = {"vs": "fp64 oracle, same inputs", "heads": c["heads"],
+               "metric": "max|gpu - oracle| / RMS(oracle)",
+               "out": rel_err(c["out"].numpy(), ro), "final_state": rel_err(c["final"].numpy(), rf),
+               "oracle_s": time.perf_counter() - t0}
+        if c["ckpts"] is not None and rc is not None:
+            par["ckpts"] = rel_err(c["ckpts"].numpy(), rc)
+        par["pass"] = (par["out"] <= TOL_OUT and par["final_state"] <= TOL_STATE and
+                       par.get("ckpts", 0.0) <= TOL_STATE)
+        fig["parity"] = par
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -512,7 +539,7 @@ def run_gb300(args):
     cp = context_parallel_figure(dev, stream)
     assert kda.device_status() == 0
     torch.cuda.empty_cache()
-    named = named_workload_figures(dev, stream, hbm_peak)
+    named = named_workload_figures(dev, stream, hbm_peak, keep=with_base)
     assert kda.device_status() == 0
     torch.cuda.empty_cache()
 
@@ -522,6 +549,8 @@ def run_gb300(args):
         return 0
 
     base, parity = cpu_baseline(step) if with_base else (None, None)
+    if with_base:
+        other_parity(named)
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "prefill_traffic.json")
     if os.path.exists(tpath):
@@ -642,11 +671,13 @@ def prefix_reuse_figure(dev, stream, n_req: int = 4, prefix: int = 16384, new_to
             "speedup": miss_ms / hit_ms, "restored_from_tokens": covered}
 
 
-def named_workload_figures(dev, stream, hbm_peak):
+def named_workload_figures(dev, stream, hbm_peak, keep: bool = False):
     """The other two prefill workloads beside the T=8192 step, timed the same way (CUDA events on
     the launching stream, 2 warm-ups, 3 launches): varlen x8 (8 sequences of U[1024, 32768] tokens,
     initial and final states) and one sequence of 262,144 tokens with a checkpoint every 4096.
-    Algorithmic bytes: 1,282 B per token-head (bf16 o) plus 64 KB per state read or written."""
+    Algorithmic bytes: 1,282 B per token-head (bf16 o) plus 64 KB per state read or written.
+    With `keep`, each figure also keeps host copies of its inputs and GPU results on 8 sampled heads
+    (the long workload's oracle heads) for the oracle comparison of the CPU-baseline leg."""
     import torch
 
     import kimi_delta_attention_13_gb300 as kda
@@ -674,11 +705,22 @@ def named_workload_figures(dev, stream, hbm_peak):
         _, ms = cuda_time_ms(step, 3, stream)
         states = N * (2 if w.init_state else 1) + n_ck
         b = T * H * BYTES_PER_TOKEN_HEAD + states * H * STATE_BYTES
+        if keep:
+            hs = synth.long_context_oracle_heads() if H == 96 else list(range(min(H, 8)))
+            idx = torch.tensor(hs, device=dev)
+            check = {"heads": hs, "ckpt_stride": w.ckpt_stride,
+                     "inputs": {k_: x[k_].index_select(1, idx).cpu() for k_ in ("q", "k", "v", "g", "beta")},
+                     "cu": x["cu_seqlens"].cpu().long(),
+                     "init": None if x["state"] is None else x["state"].index_select(1, idx).cpu(),
+                     "out": o.index_select(1, idx).cpu(), "final": fin.index_select(1, idx).cpu(),
+                     "ckpts": ck.index_select(1, idx).cpu() if ck is not None else None}
         res[key] = {"workload": f"{w.name}: {N} sequence(s), {T} tokens, H={H}, "
                                 f"{n_ck} checkpoints, fp32 out",
                     "ms": ms, "tokens_per_s": T / (ms / 1e3), "bytes_alg": b,
                     "GB/s": b / (ms / 1e3) / 1e9, "frac": b / (ms / 1e3) / 1e9 / hbm_peak,
                     "longest_sequence": max(lengths)}
+        if keep:
+            res[key]["_check"] = check
         del x, o, fin, ck
         torch.cuda.empty_cache()
     return res

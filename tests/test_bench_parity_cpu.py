@@ -43,3 +43,25 @@ def test_rel_err_metric():
     ref = np.array([3.0, -4.0])                                  # RMS = sqrt(12.5)
     assert bench.rel_err(ref + np.array([0.0, 0.5]), ref) == pytest.approx(0.5 / np.sqrt(12.5))
     assert bench.rel_err(np.zeros(0), np.zeros(0)) == 0.0
+
+
+def test_other_workloads_parity_leg():
+    # a kept head sample (varlen, initial states, checkpoints) with the oracle's own results as
+    # the GPU's: it passes; a planted error in a checkpoint fails it; the kept data is dropped
+    lengths, stride = [70, 0, 130], 32
+    x = synth.make_inputs(lengths, heads=2, dtype="bf16", seed=3, device="cpu", init_state=True)
+    cu = x["cu_seqlens"].long()
+    o, f, c = oracle.default().prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, x["state"],
+                                       ckpt_stride=stride)
+    check = {"heads": [0, 1], "ckpt_stride": stride,
+             "inputs": {k: x[k] for k in ("q", "k", "v", "g", "beta")}, "cu": cu, "init": x["state"],
+             "out": torch.from_numpy(o).float(), "final": torch.from_numpy(f).float(),
+             "ckpts": torch.from_numpy(c).float()}
+    named = {"w": {"ms": 1.0, "_check": check}}
+    bench.other_parity(named)
+    par = named["w"]["parity"]
+    assert "_check" not in named["w"] and par["pass"] and par["ckpts"] < 1e-6
+    check["ckpts"][1, 0, 3, 4] += 1.0
+    named = {"w": {"ms": 1.0, "_check": check}}
+    bench.other_parity(named)
+    assert not named["w"]["parity"]["pass"] and named["w"]["parity"]["ckpts"] > bench.TOL_STATE

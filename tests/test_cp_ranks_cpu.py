@@ -92,7 +92,7 @@ def test_two_ranks_match_the_whole_prefill():
     import oracle
 
     world = 2
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         results = mgr.dict()
         mp.spawn(_worker, args=(world, _free_port(), results), nprocs=world, join=True)
         res = dict(results)

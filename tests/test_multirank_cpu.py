@@ -36,7 +36,7 @@ def _worker(rank, world, port, local_ms, results):
 @pytest.mark.timeout(120)
 def test_two_replicas_time_is_the_slowest_rank():
     world, local_ms = 2, [12.5, 20.0]
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         results = mgr.dict()
         mp.spawn(_worker, args=(world, _free_port(), local_ms, results), nprocs=world, join=True)
         res = dict(results)
