@@ -1,9 +1,10 @@
 """Seeded random cases of the prefill against the fp64 oracle: varlen batches whose lengths sit on
 and around the 16-token tiles and 32-token steps (and random ones), 1 to 5 heads, with or without
 initial states, checkpoint strides 0/32/64/96, fp32 or bf16 outputs, the default and the precise
-build; seeded random decode batches; and the staged prefill from pinned host buffers with random
-chunk sizes.  Bounds as everywhere (bf16 inputs: 2e-2 x RMS on outputs, 1e-2 on states and
-checkpoints; bf16 outputs add their own rounding, 2^-8 relative)."""
+build; seeded random decode batches; the staged prefill from pinned host buffers with random chunk
+sizes; and the context-parallel prefill with random segment lengths.  Bounds as everywhere (bf16
+inputs: 2e-2 x RMS on outputs, 1e-2 on states and checkpoints; bf16 outputs add their own
+rounding, 2^-8 relative)."""
 import numpy as np
 import pytest
 import torch
@@ -105,4 +106,24 @@ def test_fuzz_staged(orc, i):
     ro, rf, _ = orc.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"].cpu().long(),
                             x["state"])
     assert_close("out", h_out, ro, TOL["bf16"]["out"])
+    assert_close("final", fin, rf, TOL["bf16"]["state"])
+
+
+@pytest.mark.parametrize("i", range(6))
+def test_fuzz_context_parallel(orc, i):
+    from kimi_delta_attention_13_gb300.context_parallel import prefill_cp
+
+    rng = np.random.default_rng(5000 + i)
+    lengths = [int(rng.integers(0, 2500)) for _ in range(int(rng.integers(1, 4)))]
+    H = int(rng.integers(1, 4))
+    seg_len = int(rng.choice([32, 100, 256, 777]))
+    x = synth.make_inputs(lengths, heads=H, dtype="bf16", seed=5000 + i, device=DEV,
+                          init_state=bool(rng.random() < 0.5))
+    out, fin = prefill_cp(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"], x["state"],
+                          seg_len=seg_len, lengths=lengths)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    ro, rf, _ = orc.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"].cpu().long(),
+                            x["state"])
+    assert_close("out", out, ro, TOL["bf16"]["out"])
     assert_close("final", fin, rf, TOL["bf16"]["state"])
