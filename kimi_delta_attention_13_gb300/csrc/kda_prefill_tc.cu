@@ -28,9 +28,10 @@
 // Work split: one CTA per (sequence, head), 512 threads.  tcgen05.mma issue costs the issuing
 // thread tens of cycles per instruction, so the MMAs are spread over threads that would otherwise
 // wait:
-//   warp 0 lane 0  asynchronous issuer: TMA loads of q, k, g (one stage) and v (three stages), the
-//                  V products, the state reads and the P / R^T products, each as soon as its
-//                  inputs are ready (the q, k, g load first: prep waits on it)
+//   warp 0 lane 0  asynchronous issuer: TMA loads of q, k, g (one stage) and v (three stages; two
+//                  in the precise build), the V products, the state reads and the P / R^T
+//                  products, each as soon as its inputs are ready (the q, k, g load first: prep
+//                  waits on it)
 //   warp 1         TMEM allocation; the solve's diagonal blocks T00, T11 and half of T10
 //   warp 2         issues the step's Gram product and reads -A out of it (with beta, loaded one
 //                  step ahead)
@@ -1142,7 +1143,7 @@ __device__ void issuer_role(const Params &p, const CUtensorMap *mq, const CUtens
             ++cvi;
             prog = true;
         }
-        // v of step sv (three stages: free once the V product of step sv-3 has completed)
+        // v of step sv (kVStages stages: free once the V product of step sv - kVStages has completed)
         if (sv < nsteps && (sv < kVStages || mbar_test_wait(&bars[B_VEMPTY + sv % kVStages], ((sv / kVStages) - 1) & 1))) {
             const int t0 = (int)(start + (long long)sv * C);
             uint8_t *vt = smem + OFF_VRING + (sv % kVStages) * TILE_BYTES;
