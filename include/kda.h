@@ -268,9 +268,12 @@ int64_t kda_prefill_staged_scratch(const int32_t *h_cu_seqlens, int32_t n_seqs, 
 /*
  * kda_prefill_staged_static -- kda_prefill_staged without caller scratch: the chunks' sequence
  * tables go to a fixed device array of the library (2^20 int32 entries per device, a file-scope
- * __device__ array), so the caller provides no scratch and the library allocates nothing.  Calls
+ * __device__ array), so the caller provides no scratch and the library allocates no memory.  Calls
  * share that array: each call's `stream` first waits for the previous call's last prefill, so
- * calls from several streams or threads are safe and run one after another on the device.
+ * calls from several streams or threads are safe and run one after another on the device.  The
+ * first call on a device creates the staged path's two copy streams and four events (shared with
+ * kda_prefill_staged) and one event that orders calls on the array; later calls reuse them
+ * (kda_diag_staged_handles counts them).
  * Arguments and errors as for kda_prefill_staged; KDA_ERR_INVALID_ARG also when the tables need
  * more than 2^20 entries (kda_prefill_staged_scratch tells).
  */
