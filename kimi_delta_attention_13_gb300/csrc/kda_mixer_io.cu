@@ -13,7 +13,7 @@
 //
 // Every kernel here streams HBM once (the roofline is bytes / bandwidth): 16-byte vector loads
 // and stores of 8 channels per thread, fp32 arithmetic.  The pre-mixer is two launches: the
-// convolution of q, k and v, whose threads walk a 128-token chunk with a 3-token register window
+// convolution of q, k and v, whose threads walk a 256-token chunk with a 3-token register window
 // and keep the next 8 (bf16) or 4 (fp32) tokens' loads in flight (the chunk's first tokens read a
 // 3-token halo that the neighbouring chunk, scheduled next to it, has just brought into L2); and
 // the gates, elementwise at full occupancy (their exp/log chains kept the convolution's warps
@@ -24,7 +24,7 @@ namespace kda {
 namespace {
 
 constexpr int kMixThreads = 128;   // 8 channels per thread: 1024 channels per block
-constexpr int kMixTokens = 128;    // tokens per pre-mixer block (fewer block start-ups)
+constexpr int kMixTokens = 256;    // tokens per pre-mixer block (fewer block start-ups and halos)
 // tokens each pre-mixer thread keeps in flight: 8 of bf16 (16 B each), 4 of fp32 (32 B each)
 template <typename T>
 constexpr int mix_depth() { return sizeof(T) == 2 ? 8 : 4; }

@@ -69,18 +69,20 @@ def run_premix(orc, x, dtype, heads=None):
     ("bf16", [100, 1, 37, 2, 64], 3, 128, False),
     ("bf16", [100, 1, 37, 2, 64], 3, 128, True),
     ("bf16", [31, 32, 33], 4, 128, True),
-    ("bf16", [127, 1, 129, 3], 2, 128, True),       # sequence edges next to 128-token chunk edges
+    ("bf16", [127, 1, 129, 3], 2, 128, True),       # sequence edges next to 128-token boundaries
+    ("bf16", [255, 1, 257, 3], 2, 128, True),       # sequence edges next to 256-token chunk edges
+    ("bf16", [253, 6, 300], 3, 128, True),          # a sequence start inside a chunk's 3-token halo
     ("bf16", [0, 5, 0, 40, 0], 2, 128, True),       # empty sequences
     ("f32", [45, 3, 70], 5, 64, True),              # 320 channels: a partial channel block
     ("f32", [9], 2, 8, False),
     ("f32", [33], 1, 16, True),
     ("f32", [40, 40], 3, 32, True),
     ("f32", [17, 2], 9, 256, True),                 # 2304 channels: three channel blocks
-    # bf16 with H*d a multiple of 1024: the bulk-staged convolution
+    # bf16 with H*d a multiple of 1024 (whole channel blocks)
     ("bf16", [100, 1, 37, 2, 64], 8, 128, False),
-    ("bf16", [127, 1, 129, 3], 8, 128, True),       # sequence edges next to chunk and stage edges
+    ("bf16", [255, 1, 257, 3], 8, 128, True),       # sequence edges next to chunk edges
     ("bf16", [0, 5, 0, 40, 0], 16, 64, True),       # empty sequences
-    ("bf16", [300], 4, 256, True),                  # last chunk of 44 tokens: a partial stage
+    ("bf16", [300], 4, 256, True),                  # last chunk of 44 tokens: a partial prefetch group
     ("bf16", [77, 200], 32, 64, False),             # two channel blocks
     ("bf16", [20, 13], 128, 8, True),               # one thread per head
 ])
