@@ -71,7 +71,8 @@ def run_premix(orc, x, dtype, heads=None):
     ("bf16", [31, 32, 33], 4, 128, True),
     ("bf16", [127, 1, 129, 3], 2, 128, True),       # sequence edges next to 128-token boundaries
     ("bf16", [255, 1, 257, 3], 2, 128, True),       # sequence edges next to 256-token chunk edges
-    ("bf16", [253, 6, 300], 3, 128, True),          # a sequence start inside a chunk's 3-token halo
+    ("bf16", [253, 6, 300], 3, 128, True),          # a sequence starting exactly at a chunk's halo
+    ("bf16", [254, 5, 300], 3, 128, True),          # a sequence start inside a chunk's 3-token halo
     ("bf16", [0, 5, 0, 40, 0], 2, 128, True),       # empty sequences
     ("f32", [45, 3, 70], 5, 64, True),              # 320 channels: a partial channel block
     ("f32", [9], 2, 8, False),
