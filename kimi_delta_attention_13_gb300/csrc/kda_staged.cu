@@ -26,7 +26,8 @@ namespace {
 constexpr int64_t kStaticTableInts = 1 << 20;
 static __device__ __align__(256) int32_t g_staged_tables[kStaticTableInts];
 std::mutex g_tables_mu;
-cudaEvent_t g_tables_free[64] = {};   // (indexed like g_resources)   // per device: recorded after the last call that read the table
+constexpr int kMaxDevices = 64;
+cudaEvent_t g_tables_free[kMaxDevices] = {};   // per device: recorded after the last call that read the table
 
 // Streams and events of the staged calls, created on a device's first call and kept until the
 // process exits: two non-blocking streams (uploads, downloads) and four events, reused by every
@@ -38,7 +39,6 @@ struct Resources {
     cudaStream_t s_in = nullptr, s_out = nullptr;
     cudaEvent_t start = nullptr, done = nullptr, landed = nullptr, computed = nullptr;
 };
-constexpr int kMaxDevices = 64;
 Resources g_resources[kMaxDevices];
 std::mutex g_resources_mu;
 std::atomic<long long> g_handles_created{0};   // streams and events created by the staged calls
