@@ -536,7 +536,7 @@ def run_gb300(args):
     reuse = prefix_reuse_figure(dev, stream)
     assert kda.device_status() == 0
     torch.cuda.empty_cache()
-    cp = context_parallel_figure(dev, stream)
+    cp = context_parallel_figure(dev, stream, hbm_peak=hbm_peak)
     assert kda.device_status() == 0
     torch.cuda.empty_cache()
     named = named_workload_figures(dev, stream, hbm_peak, keep=with_base)
@@ -726,14 +726,16 @@ def named_workload_figures(dev, stream, hbm_peak, keep: bool = False):
     return res
 
 
-def context_parallel_figure(dev, stream, T=262144, heads=8):
+def context_parallel_figure(dev, stream, T=262144, heads=8, hbm_peak=None):
     """One long sequence at a low head count: the plain prefill runs one CTA per head; the
-    context-parallel prefill cuts the sequence into segments that prefill side by side."""
+    context-parallel prefill cuts the sequence into segments that prefill side by side.  The scan
+    and the output correction are also timed alone."""
     import torch
 
     import kimi_delta_attention_13_gb300 as kda
     from kimi_delta_attention_13_gb300 import synth
-    from kimi_delta_attention_13_gb300.context_parallel import auto_seg_len, cp_combine, prefill_cp
+    from kimi_delta_attention_13_gb300.context_parallel import (auto_seg_len, cp_combine, cp_correct,
+                                                                prefill_cp)
 
     seg_len = auto_seg_len(T, heads, torch.cuda.get_device_properties(dev).multi_processor_count)
 
@@ -765,12 +767,29 @@ def context_parallel_figure(dev, stream, T=262144, heads=8):
     for _ in range(3):
         scan()
     _, scan_ms = cuda_time_ms_queued(scan, 10, stream)
-    del s_loc, m, s_start
-    return {"workload": f"one sequence T={T} H={heads} d={D} bf16, fp32 out and final state; "
-                        f"segments of {seg_len} tokens",
-            "plain_ms": plain_ms, "cp_ms": cp_ms, "speedup": plain_ms / cp_ms,
-            "scan_ms": scan_ms, "scan_segments": n_seg,
-            "cp_tokens_per_s": T / (cp_ms / 1e3), "plain_tokens_per_s": T / (plain_ms / 1e3)}
+    del s_loc, m
+    # the output correction alone: every segment but the first; its bytes are u read and the
+    # outputs read and written, fp32
+    u = torch.randn(T, heads, D, device=dev, generator=gen)
+    o = torch.zeros(T, heads, D, device=dev)
+    cu_seg = torch.tensor(list(range(0, T, seg_len)) + [T], dtype=torch.int32, device=dev)
+
+    def correct():
+        cp_correct(o, u, s_start, cu_seg, [0], stream=stream)
+
+    correct()
+    _, corr_ms = cuda_time_ms(correct, 5, stream)
+    corr_bytes = (T - min(seg_len, T)) * heads * D * 4 * 3
+    del u, o, s_start
+    fig = {"workload": f"one sequence T={T} H={heads} d={D} bf16, fp32 out and final state; "
+                       f"segments of {seg_len} tokens",
+           "plain_ms": plain_ms, "cp_ms": cp_ms, "speedup": plain_ms / cp_ms,
+           "scan_ms": scan_ms, "scan_segments": n_seg,
+           "correct_ms": corr_ms, "correct_GB/s": corr_bytes / (corr_ms / 1e3) / 1e9,
+           "cp_tokens_per_s": T / (cp_ms / 1e3), "plain_tokens_per_s": T / (plain_ms / 1e3)}
+    if hbm_peak:
+        fig["correct_frac"] = fig["correct_GB/s"] / hbm_peak
+    return fig
 
 
 def kbuild_source_hash() -> str:

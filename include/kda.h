@@ -293,8 +293,9 @@ int kda_prefill_staged_static(const void *h_q, const void *h_k, const void *h_v,
  * (a kda_prefill of the segment) and M = A_L ... A_1 is its final state when prefilled with v = 0
  * from the identity (a kda_prefill with d_v = d_k).  Splitting a sequence into segments lets
  * those two prefills run every segment side by side; this call turns their end states into each
- * segment's true initial state, and one more kda_prefill of the segments from those states gives
- * the sequence's outputs and final state.
+ * segment's true initial state and each sequence's final state; kda_cp_correct then turns the two
+ * prefills' outputs into the sequence's outputs (or one more kda_prefill of the segments from their
+ * start states gives them).
  *
  * For every sequence n and head, over its segments j in [seq_seg[n], seq_seg[n+1]) (at least one;
  * the first prefilled from the sequence's own initial state, so S_loc(first) is its true end state):
@@ -309,6 +310,34 @@ int kda_prefill_staged_static(const void *h_q, const void *h_k, const void *h_v,
  */
 int kda_cp_combine(const float *s_loc, const float *m, const int32_t *seq_seg, int32_t n_seqs,
                    int32_t n_heads, int32_t d, float *s_start, float *final_state, void *stream);
+
+/*
+ * kda_cp_correct -- the outputs of a context-parallel prefill, without prefilling the segments a
+ * third time.
+ *
+ * Within a segment the true state is S_t = P_t S_start + S_loc,t, with P_t = A_t ... A_1 the
+ * segment's prefix map (the affine form of kda_cp_combine).  So the true output is
+ *     o_t = S_t^T q_t = o_loc,t + S_start^T u_t,   u_t = P_t^T q_t,
+ * where o_loc,t are the outputs of the segment prefilled from zeros and u_t the outputs of the
+ * segment prefilled with v = 0 from the identity (the two kda_prefill calls whose final states
+ * kda_cp_combine takes).  For every segment but those listed in skip_seg, this call adds
+ * S_start(seg)^T u_t to out[t] for each of its tokens and heads, as one tensor-core product per
+ * (segment, head): tf32 operands (S_start rounded to nearest, u read as tf32), fp32 accumulation
+ * and addition.  List a sequence's first segment in skip_seg: prefilled from the sequence's own
+ * initial state, its outputs are already the true ones.
+ *   u            fp32 [total_tokens, H, d], 16-byte aligned: the identity prefill's outputs.
+ *   s_start      fp32 [n_seg, H, d, d]: kda_cp_combine's segment start states (S[key][value]).
+ *   cu_seg       device int32 [n_seg + 1]: the segments' token ranges in the packed token axis.
+ *   skip_seg     device int32 [n_skip], increasing: the segments left as they are (NULL iff
+ *                n_skip == 0).
+ *   out          fp32 [total_tokens, H, d], updated in place; must alias neither u nor s_start.
+ *   d            128.  Device tables are taken as they are (not validated on the host).
+ * Errors: KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED_SHAPE, KDA_ERR_MISALIGNED, KDA_ERR_CUDA; a
+ * bounded device wait that expired shows up as KDA_ERR_DEVICE_TIMEOUT in kda_device_status.
+ */
+int kda_cp_correct(const float *u, const float *s_start, const int32_t *cu_seg, int32_t n_seg,
+                   const int32_t *skip_seg, int32_t n_skip, int64_t total_tokens, int32_t n_heads,
+                   int32_t d, float *out, void *stream);
 
 /*
  * kda_device_status -- synchronize `stream`, then read and clear the current device's sticky

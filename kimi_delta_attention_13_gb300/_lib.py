@@ -39,6 +39,7 @@ SIGNATURES = {
                    + [_vp] * 5 + [_vp]),
     "kda_output_gate": (ctypes.c_int, [_vp, _i32, _vp, _i32, _vp, _i32, _i64, _vp]),
     "kda_cp_combine": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
+    "kda_cp_correct": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp, _i32, _i64, _i32, _i32, _vp, _vp]),
     "kda_prefill_staged": (ctypes.c_int, [_vp] * 6 + [_i32, _i64, _i32, _i32, _i32, _vp] + [_vp] * 9
                            + [_i64, _i64, _vp]),
     "kda_prefill_staged_scratch": (ctypes.c_int64, [_vp, _i32, _i64, _i64]),

@@ -3,16 +3,19 @@
 A (sequence, head) chain is serial, so a prefill of few heads keeps few SMs busy (8 heads: 8 of
 152).  The recurrence is affine in the state (page "Kimi K3 im Detail", section "Sequenz-Mixing:
 KDA-Zustand und globale MLA": per token S_t = A_t S_(t-1) + beta_t k_t v_t^T with
-A_t = (I - beta_t k_t k_t^T) diag(exp(g_t))), so over a segment S_end = M S_start + S_loc, and
+A_t = (I - beta_t k_t k_t^T) diag(exp(g_t))), so within a segment S_t = P_t S_start + S_loc,t with
+P_t = A_t ... A_1, and
   1. kda_prefill of every segment as its own sequence, from zeros (a sequence's first segment from
-     the sequence's own initial state), gives S_loc;
-  2. kda_prefill of every segment with v = 0 from the identity gives M;
-  3. kda_cp_combine scans S_start(j + 1) = M(j) S_start(j) + S_loc(j) over each sequence;
-  4. kda_prefill of every segment from its true start state gives the outputs and, in each
-     sequence's last segment, its final state.
-Each of the three prefills runs segments x heads CTAs at once instead of heads, at about three
-times a plain prefill's work.  Everything runs in the library's kernels through its C ABI; this
-module builds the segment table and moves states between the passes.
+     the sequence's own initial state), gives S_loc and the outputs o_loc;
+  2. kda_prefill of every segment with v = 0 from the identity gives M = P_L and the outputs
+     u_t = P_t^T q_t;
+  3. kda_cp_combine scans S_start(j + 1) = M(j) S_start(j) + S_loc(j) over each sequence, and
+     gives each sequence's final state;
+  4. kda_cp_correct adds S_start^T u_t to o_loc,t in every segment that does not start its
+     sequence: o_t = S_t^T q_t = o_loc,t + S_start^T u_t.
+Each of the two prefills runs segments x heads CTAs at once instead of heads, at about twice a
+plain prefill's work.  Everything runs in the library's kernels through its C ABI; this module
+builds the segment tables and moves states between the passes.
 """
 from __future__ import annotations
 
@@ -87,6 +90,36 @@ def cp_combine(s_loc, m, seq_seg, s_start, final_state=None, stream=None):
     return s_start
 
 
+def cp_correct(out, u, s_start, cu_seg, skip_seg, stream=None):
+    """The output correction (kda_cp_correct): out[t] += S_start(seg)^T u_t for the tokens of every
+    segment seg not in skip_seg.  out, u: fp32 [T, H, 128] on one device; s_start: fp32
+    [n_seg, H, 128, 128]; cu_seg: int32 [n_seg + 1] token offsets on the device; skip_seg: the
+    segments left as they are, an increasing host list or int32 device tensor.  Returns out."""
+    dev = out.device
+    T, H, D = out.shape
+    n_seg = s_start.shape[0]
+    _require(out, "out", dev, torch.float32, (T, H, D))
+    _require(u, "u", dev, torch.float32, (T, H, D))
+    _require(s_start, "s_start", dev, torch.float32, (n_seg, H, D, D))
+    _require(cu_seg, "cu_seg", dev, torch.int32, (n_seg + 1,))
+    lib = _lib.load()
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.stream(s):
+        if not isinstance(skip_seg, torch.Tensor):
+            skip = [int(j) for j in skip_seg]
+            if any(b <= a for a, b in zip(skip, skip[1:])):
+                raise ValueError("skip_seg must be increasing")
+            skip_seg = torch.tensor(skip, dtype=torch.int32, device=dev)
+        else:
+            _require(skip_seg, "skip_seg", dev, torch.int32)
+        n_skip = int(skip_seg.numel())
+        rc = lib.kda_cp_correct(_ptr(u), _ptr(s_start), _ptr(cu_seg), n_seg,
+                                _ptr(skip_seg) if n_skip else None, n_skip, T, H, D, _ptr(out),
+                                _stream(dev, s))
+    _lib.check(rc, "kda_cp_correct")
+    return out
+
+
 def prefill_cp(q, k, v, g, beta, cu_seqlens=None, init_state=None, *, seg_len: int,
                lengths: Optional[Sequence[int]] = None, out=None, final_state=True, stream=None):
     """Varlen KDA prefill with every sequence cut into segments of `seg_len` tokens that prefill
@@ -116,7 +149,6 @@ def prefill_cp(q, k, v, g, beta, cu_seqlens=None, init_state=None, *, seg_len: i
         n_seg = len(bounds)
         cu_seg = torch.tensor([b for b, _ in bounds] + [T], dtype=torch.int32, device=dev)
         first = torch.tensor(seq_seg[:-1], dtype=torch.int64, device=dev)
-        last = torch.tensor([i - 1 for i in seq_seg[1:]], dtype=torch.int64, device=dev)
         seqs = torch.arange(N, device=dev)
         # 1. every segment from zeros; a sequence's first segment from its own initial state
         init_seg = torch.zeros((n_seg, H, D, D), device=dev, dtype=torch.float32)
@@ -127,29 +159,27 @@ def prefill_cp(q, k, v, g, beta, cu_seqlens=None, init_state=None, *, seg_len: i
             if final_state is not None and N > 0:
                 state_copy(final_state, s_loc, stream=s)
             return out, final_state
-        # 2. every segment with v = 0 from the identity: the segment maps M (outputs unused)
+        # 2. every segment with v = 0 from the identity: the segment maps M and the outputs u
         eye = torch.eye(D, device=dev, dtype=torch.float32).expand(n_seg, H, D, D).contiguous()
-        scratch = torch.empty_like(out)
-        _, m, _ = prefill(q, k, torch.zeros_like(v), g, beta, cu_seg, eye, out=scratch,
-                          final_state=True, stream=s)
-        del eye, scratch
+        u = torch.empty((T, H, D), device=dev, dtype=torch.float32)
+        _, m, _ = prefill(q, k, torch.zeros_like(v), g, beta, cu_seg, eye, out=u, final_state=True,
+                          stream=s)
+        del eye
         # 3. each segment's true start state (a first segment keeps its sequence's initial state)
+        # and each sequence's final state
         s_start = init_seg
-        cp_combine(s_loc, m, seq_seg, s_start, stream=s)
+        cp_combine(s_loc, m, seq_seg, s_start, final_state=final_state, stream=s)
         del m
-        # 4. every segment from its true start: the outputs, and the sequences' final states
-        out, seg_final, _ = prefill(q, k, v, g, beta, cu_seg, s_start, out=out, final_state=s_loc,
-                                    stream=s)
-        if final_state is not None and N > 0:
-            state_copy(final_state, seg_final, seqs, last, stream=s)
+        # 4. the outputs of every segment that does not start its sequence
+        cp_correct(out, u, s_start, cu_seg, seq_seg[:-1], stream=s)
         return out, final_state
 
 
 # --------------------------------------------------------------------------------------------
 # Across ranks: each rank owns a contiguous block of the segments.  Passes 1 and 2 run on a
 # rank's own segments; one all-gather hands every rank every segment's (M, S_loc); each rank
-# runs the (cheap) scan over all segments and pass 3 on its own.  The only data crossing ranks is
-# that exchange: 2 x H x d x d fp32 per segment.
+# runs the (cheap) scan over all segments and the output correction on its own.  The only data
+# crossing ranks is that exchange: 2 x H x d x d fp32 per segment.
 
 
 def assign_segments(n_seg: int, world_size: int) -> List[range]:
@@ -191,7 +221,14 @@ class _LibraryBackend:
         return out, fin
 
     def scan(self, s_loc, m, seq_seg, s_start):
-        cp_combine(s_loc, m, seq_seg, s_start, stream=self.stream)
+        """The scan; returns every sequence's final state."""
+        fin = torch.empty((len(seq_seg) - 1,) + tuple(s_loc.shape[1:]), device=s_loc.device,
+                          dtype=s_loc.dtype)
+        cp_combine(s_loc, m, seq_seg, s_start, final_state=fin, stream=self.stream)
+        return fin
+
+    def correct(self, out, u, s_start, cu, skip):
+        return cp_correct(out, u, s_start, cu, skip, stream=self.stream)
 
 
 def _prefill_cp_ranks(q, k, v, g, beta, lengths, init_state, seg_len, backend, group=None):
@@ -221,10 +258,11 @@ def _prefill_cp_ranks(q, k, v, g, beta, lengths, init_state, seg_len, backend, g
         for j in mine:
             if j in first_of and init_state is not None:
                 init[j - mine.start] = init_state[first_of[j]]
-        # 1. own segments from their local starts: S_loc;  2. with v = 0 from the identity: M
-        _, s_loc_mine = backend.prefill(xq, xk, xv, xg, xb, cu, init)
+        # 1. own segments from their local starts: o_loc and S_loc;  2. with v = 0 from the
+        # identity: u and M
+        o_mine, s_loc_mine = backend.prefill(xq, xk, xv, xg, xb, cu, init)
         eye = torch.eye(D, device=dev, dtype=f32).expand(len(mine), H, D, D).contiguous()
-        _, m_mine = backend.prefill(xq, xk, torch.zeros_like(xv), xg, xb, cu, eye)
+        u_mine, m_mine = backend.prefill(xq, xk, torch.zeros_like(xv), xg, xb, cu, eye)
     else:
         s_loc_mine = torch.zeros((0, H, D, D), device=dev, dtype=f32)
         m_mine = torch.zeros((0, H, D, D), device=dev, dtype=f32)
@@ -236,16 +274,16 @@ def _prefill_cp_ranks(q, k, v, g, beta, lengths, init_state, seg_len, backend, g
     if init_state is not None:
         for j, n in first_of.items():
             s_start[j] = init_state[n]
-    backend.scan(s_loc, m, seq_seg, s_start)
-    # 4. own segments from their true starts: outputs of the own tokens, and the final state of
-    # every sequence whose last segment is here
+    fin_all = backend.scan(s_loc, m, seq_seg, s_start)
+    # 4. the outputs of the own tokens (a segment that starts its sequence is already exact), and
+    # the final state of every sequence whose last segment is here
     out_mine, finals = None, {}
     if len(mine):
-        out_mine, seg_final = backend.prefill(xq, xk, xv, xg, xb, cu, s_start[mine.start:mine.stop].contiguous())
+        skip = [j - mine.start for j in mine if j in first_of]
+        out_mine = backend.correct(o_mine, u_mine, s_start[mine.start:mine.stop].contiguous(), cu, skip)
         for n in range(N):
-            last = seq_seg[n + 1] - 1
-            if last in mine:
-                finals[n] = seg_final[last - mine.start]
+            if seq_seg[n + 1] - 1 in mine:
+                finals[n] = fin_all[n]
     return out_mine, (tok_lo, tok_hi), finals
 
 
@@ -257,7 +295,7 @@ def prefill_cp_distributed(q, k, v, g, beta, init_state=None, *, seg_len: int, l
     [N, H, 128, 128] or None) and the same `lengths` and `seg_len`.  The sequences are cut into
     segments of `seg_len` tokens; rank r prefills the r-th contiguous block of them (passes 1 and
     2), one all-gather shares every segment's (M, S_loc) (the only exchange, 2 x H x 128 x 128 fp32
-    per segment), and every rank runs the scan and the final pass over its own block.  Returns
+    per segment), and every rank runs the scan and the output correction over its own block.  Returns
     (out, (t0, t1), finals): the outputs of the rank's tokens t0..t1-1 (fp32 [t1 - t0, H, 128]),
     and {sequence index: final state [H, 128, 128]} for the sequences ending on this rank."""
     dev = q.device

@@ -264,6 +264,25 @@ int kda_cp_combine(const float *s_loc, const float *m, const int32_t *seq_seg, i
                              (cudaStream_t)stream);
 }
 
+int kda_cp_correct(const float *u, const float *s_start, const int32_t *cu_seg, int32_t n_seg,
+                   const int32_t *skip_seg, int32_t n_skip, int64_t total_tokens, int32_t n_heads,
+                   int32_t d, float *out, void *stream)
+{
+    const CallRange range("kda_cp_correct");
+    if (n_seg < 0 || n_skip < 0 || total_tokens < 0 || n_heads < 1 || d < 1) return KDA_ERR_INVALID_ARG;
+    if (d != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (n_seg > 0 && (!u || !s_start || !cu_seg || !out || (n_skip > 0 && !skip_seg)))
+        return KDA_ERR_INVALID_ARG;
+    const void *ptrs[] = {u, s_start, out};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(cu_seg) & 3u) != 0 || (reinterpret_cast<uintptr_t>(skip_seg) & 3u) != 0)
+        return KDA_ERR_MISALIGNED;
+    if (out && (out == u || reinterpret_cast<const void *>(out) == s_start)) return KDA_ERR_INVALID_ARG;
+    return launch_cp_correct(u, s_start, cu_seg, n_seg, skip_seg, n_skip, n_heads, (long long)total_tokens,
+                             out, (cudaStream_t)stream);
+}
+
 int64_t kda_prefill_staged_scratch(const int32_t *h_cu_seqlens, int32_t n_seqs, int64_t total_tokens,
                                    int64_t chunk_tokens)
 {
@@ -351,6 +370,10 @@ int kda_device_status(int32_t *status, void *stream)
     if (b == KDA_OK) b = bp;
     rc = read_and_clear_status_decode((cudaStream_t)stream, &c);
     if (rc != KDA_OK) return rc;
+    int32_t cp = 0;
+    rc = read_and_clear_status_cp((cudaStream_t)stream, &cp);
+    if (rc != KDA_OK) return rc;
+    if (c == KDA_OK) c = cp;
     *status = b != KDA_OK ? b : (c != KDA_OK ? c : a);
     return KDA_OK;
 }

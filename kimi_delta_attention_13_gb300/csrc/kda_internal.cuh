@@ -28,6 +28,7 @@ int read_and_clear_status_state_copy(cudaStream_t s, int32_t *status);
 int read_and_clear_status_prefill_tc(cudaStream_t s, int32_t *status);
 int read_and_clear_status_prefill_tc_precise(cudaStream_t s, int32_t *status);
 int read_and_clear_status_decode(cudaStream_t s, int32_t *status);
+int read_and_clear_status_cp(cudaStream_t s, int32_t *status);
 // Launch the one-CTA probe whose bounded device wait expires after `cycles` SM cycles.
 int launch_wait_timeout_probe(long long cycles, cudaStream_t stream);
 // Launch the one-thread run of the shared-memory bounds check on an out-of-window offset; read
@@ -54,6 +55,9 @@ int launch_premix(const void *xq, const void *xk, const void *xv, const void *a,
                   void *k, void *v, void *g, void *beta, cudaStream_t stream);
 int launch_output_gate(const void *o, int o_dtype, const void *z, int z_dtype, void *out,
                        int out_dtype, long long n, cudaStream_t stream);
+int launch_cp_correct(const float *u, const float *s_start, const int32_t *cu_seg, int n_seg,
+                      const int32_t *skip_seg, int n_skip, int H, long long T, float *out,
+                      cudaStream_t stream);
 int launch_cp_combine(const float *s_loc, const float *m, const int32_t *seq_seg, int n_seqs, int H,
                       float *s_start, float *final_state, cudaStream_t stream);
 int64_t staged_scratch_ints(const int32_t *h_cu, int n_seqs, long long T, long long chunk_tokens);

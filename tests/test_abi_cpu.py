@@ -161,6 +161,28 @@ def test_premix_rejects(lib, over, code):
     assert _premix(lib, **over) == code
 
 
+def test_cp_correct_rejects(lib):
+    f = lib.kda_cp_correct
+    ok = dict(u=A, s=A + 4096, cu=A + 8192, n_seg=2, skip=A + 8208, n_skip=1, T=64, H=2, d=128,
+              out=A + 16384)
+
+    def call(**over):
+        a = dict(ok, **over)
+        return f(a["u"], a["s"], a["cu"], a["n_seg"], a["skip"], a["n_skip"], a["T"], a["H"], a["d"],
+                 a["out"], None)
+    assert call(n_seg=-1) == 1
+    assert call(n_skip=-1) == 1
+    assert call(H=0) == 1
+    assert call(d=64) == 2                     # the tensor-core correction is for d = 128
+    assert call(skip=None) == 1                # n_skip > 0 needs the list
+    assert call(u=None) == 1
+    assert call(u=A + 4) == 3
+    assert call(cu=A + 8194) == 3
+    assert call(skip=A + 8210) == 3
+    assert call(out=A) == 1                    # out aliases u
+    assert call(out=A + 4096) == 1             # out aliases s_start
+
+
 def test_output_gate_rejects(lib):
     f = lib.kda_output_gate
     assert f(A, 1, A + 16, 0, A + 32, 0, -1, None) == 1           # negative count

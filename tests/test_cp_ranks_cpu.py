@@ -1,7 +1,7 @@
 """The cross-rank context-parallel prefill on CPU: two gloo ranks on 127.0.0.1.
 
 Each rank prefills its own contiguous block of segments, one all-gather shares every segment's
-(M, S_loc), and each rank scans and runs the final pass on its block.  Here the segment prefills
+(M, S_loc), and each rank scans and corrects the outputs of its block.  Here the segment prefills
 are the fp64 oracle's and the scan a plain fp64 loop, so the assembled outputs and final states
 must equal the oracle's prefill of the whole batch up to fp64 rounding: this checks the segment
 assignment, the ordering of the gathered slots, the start states handed to each block and the
@@ -42,12 +42,24 @@ class _OracleBackend:
         return torch.from_numpy(o), torch.from_numpy(f)
 
     def scan(self, s_loc, m, seq_seg, s_start):
+        fin = []
         for n in range(len(seq_seg) - 1):
             lo, hi = seq_seg[n], seq_seg[n + 1]
             s = s_loc[lo]
             for j in range(lo + 1, hi):
                 s_start[j] = s
                 s = torch.matmul(m[j], s) + s_loc[j]
+            fin.append(s)
+        return torch.stack(fin)
+
+    def correct(self, out, u, s_start, cu, skip):
+        # out[t, h, :] += u[t, h, :] S_start[seg, h] for the tokens of every segment not skipped
+        for j in range(s_start.shape[0]):
+            if j in skip:
+                continue
+            a, b = int(cu[j]), int(cu[j + 1])
+            out[a:b] += torch.einsum("thm,hmj->thj", u[a:b], s_start[j])
+        return out
 
 
 def _inputs():

@@ -1,6 +1,7 @@
 """Context-parallel prefill on the GPU against the fp64 oracle's plain (token by token) prefill:
-segments prefilled side by side and joined by kda_cp_combine's scan must give the outputs and
-final states of the whole sequences (bf16 inputs: 2e-2 x RMS on outputs, 1e-2 on states)."""
+segments prefilled side by side, joined by kda_cp_combine's scan and kda_cp_correct's output
+correction, must give the outputs and final states of the whole sequences (bf16 inputs: 2e-2 x RMS
+on outputs, 1e-2 on states)."""
 import pytest
 import torch
 
@@ -157,3 +158,37 @@ def test_cp_combine_scan_against_fp64():
             s = m[j].double() @ s + s_loc[j].double()
         err = (got_fin[n].double() - s).abs().max() / s.pow(2).mean().sqrt()
         assert err < 1e-4, (n, float(err))
+
+
+def test_cp_correct_against_fp64():
+    """kda_cp_correct alone: out[t] += S_start(seg)^T u_t over ragged segments (an empty one, one
+    of exactly two 128-token tiles, one ending at the tensor's last token), three heads, two
+    segments skipped.  tf32 operands bound the error of the added term per element by
+    (2^-10 + 2^-11) sum_m |u_m| |S_mj| (u truncated, S rounded to nearest); the test allows 2^-9."""
+    from kimi_delta_attention_13_gb300.context_parallel import cp_correct
+
+    gen = torch.Generator().manual_seed(71)
+    H, D = 3, 128
+    bounds = [0, 300, 300, 333, 589, 845, 1130]
+    T, n_seg = bounds[-1], len(bounds) - 1
+    u = torch.randn(T, H, D, generator=gen)
+    out0 = torch.randn(T, H, D, generator=gen)
+    s_start = 0.1 * torch.randn(n_seg, H, D, D, generator=gen)
+    skip = [0, 3]
+    ref, bound = out0.double().clone(), torch.zeros(T, H, D, dtype=torch.float64)
+    for j in range(n_seg):
+        a, b = bounds[j], bounds[j + 1]
+        if j in skip:
+            continue
+        ref[a:b] += torch.einsum("thm,hmj->thj", u[a:b].double(), s_start[j].double())
+        bound[a:b] = 2.0 ** -9 * torch.einsum("thm,hmj->thj", u[a:b].abs().double(), s_start[j].abs().double())
+    out = out0.to(DEV)
+    cp_correct(out, u.to(DEV), s_start.to(DEV), torch.tensor(bounds, dtype=torch.int32, device=DEV), skip)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    got = out.cpu()
+    for j in skip:   # left as they were, bit for bit
+        a, b = bounds[j], bounds[j + 1]
+        assert torch.equal(got[a:b], out0[a:b])
+    err = (got.double() - ref).abs()
+    assert torch.all(err <= bound + 1e-6 * ref.abs()), float((err - bound).max())
