@@ -160,21 +160,24 @@ def test_cp_combine_scan_against_fp64():
         assert err < 1e-4, (n, float(err))
 
 
-def test_cp_correct_against_fp64():
-    """kda_cp_correct alone: out[t] += S_start(seg)^T u_t over ragged segments (an empty one, one
-    of exactly two 128-token tiles, one ending at the tensor's last token), three heads, two
-    segments skipped.  tf32 operands bound the error of the added term per element by
+@pytest.mark.parametrize("bounds,H,skip", [
+    ([0, 300, 300, 333, 589, 845, 1130], 3, [0, 3]),   # empty, two exact tiles, ends at the last token
+    ([0, 5, 37], 1, []),                               # less than one tile in all
+    ([0, 100, 300], 70, [0]),                          # many heads
+    ([0, 1, 2, 3, 130], 2, [1]),                       # one-token segments
+])
+def test_cp_correct_against_fp64(bounds, H, skip):
+    """kda_cp_correct alone: out[t] += S_start(seg)^T u_t over ragged segments, with the skipped
+    segments left bit for bit.  tf32 operands bound the error of the added term per element by
     (2^-10 + 2^-11) sum_m |u_m| |S_mj| (u truncated, S rounded to nearest); the test allows 2^-9."""
     from kimi_delta_attention_13_gb300.context_parallel import cp_correct
 
-    gen = torch.Generator().manual_seed(71)
-    H, D = 3, 128
-    bounds = [0, 300, 300, 333, 589, 845, 1130]
+    gen = torch.Generator().manual_seed(71 + H)
+    D = 128
     T, n_seg = bounds[-1], len(bounds) - 1
     u = torch.randn(T, H, D, generator=gen)
     out0 = torch.randn(T, H, D, generator=gen)
     s_start = 0.1 * torch.randn(n_seg, H, D, D, generator=gen)
-    skip = [0, 3]
     ref, bound = out0.double().clone(), torch.zeros(T, H, D, dtype=torch.float64)
     for j in range(n_seg):
         a, b = bounds[j], bounds[j + 1]
