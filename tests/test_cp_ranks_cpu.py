@@ -19,7 +19,8 @@ import torch.multiprocessing as mp
 from kimi_delta_attention_13_gb300.context_parallel import (_prefill_cp_ranks, assign_segments,
                                                              gather_segments, segments)
 
-# 13 segments: ranks own 7 and 6, and the third sequence (330 tokens, 6 segments) crosses the boundary
+# 13 segments: two ranks own 7 and 6, and the third sequence (330 tokens, 6 segments) crosses the
+# boundary; three ranks own 5, 4 and 4, the middle block inside that sequence
 LENGTHS, HEADS, SEG_LEN, SEED = [150, 0, 330, 97, 1], 2, 64, 61
 
 
@@ -100,10 +101,10 @@ def test_assign_segments_covers_each_segment_once():
 
 
 @pytest.mark.timeout(300)
-def test_two_ranks_match_the_whole_prefill():
+@pytest.mark.parametrize("world", [2, 3])
+def test_ranks_match_the_whole_prefill(world):
     import oracle
 
-    world = 2
     with mp.get_context("spawn").Manager() as mgr:
         results = mgr.dict()
         mp.spawn(_worker, args=(world, _free_port(), results), nprocs=world, join=True)
@@ -117,8 +118,13 @@ def test_two_ranks_match_the_whole_prefill():
                                          x["cu_seqlens"].long(), x["state"])
     bounds, seq_seg = segments(LENGTHS, SEG_LEN)
     owned = assign_segments(len(bounds), world)
-    # the case is meant to have a sequence split across the two ranks
-    assert any(seq_seg[n] in owned[0] and seq_seg[n + 1] - 1 in owned[1] for n in range(len(LENGTHS)))
+    # the case is meant to have, with two ranks, a sequence split across them, and with three, a
+    # rank that holds only middle segments of one sequence (no start to skip, no final state)
+    if world == 2:
+        assert any(seq_seg[n] in owned[0] and seq_seg[n + 1] - 1 in owned[1] for n in range(len(LENGTHS)))
+    if world == 3:
+        starts, ends = set(seq_seg[:-1]), {j - 1 for j in seq_seg[1:]}
+        assert not (set(owned[1]) & starts) and not (set(owned[1]) & ends)
     T = sum(LENGTHS)
     out = np.full((T, HEADS, 128), np.nan)
     seen = {}
