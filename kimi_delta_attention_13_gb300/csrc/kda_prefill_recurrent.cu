@@ -8,8 +8,10 @@
 //
 // Grid: one block per (sequence, head, 32-wide slice of the value channels); value columns
 // are independent given k, g, beta, so slices never exchange data.  Block = 4 warps; in warp w,
-// lane l owns column j = 8w + (l & 7) of the slice and key rows i = 4m + (l >> 3), so the
-// column sums over i are two xor-shuffles.  Tokens are staged 16 at a time in shared memory.
+// lane l owns column j = 8w + (l & 7) of the slice and the key rows i = 16 g + 4 (l >> 3) + c
+// (g = 0..7, c = 0..3): four consecutive rows per group, read from shared memory as one float4,
+// and the column sums over i are two xor-shuffles.  Tokens are staged 16 at a time in shared
+// memory.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -38,7 +40,7 @@ prefill_recurrent_kernel(const T *__restrict__ q, const T *__restrict__ k, const
     const int j = slice * kSlice + jj;      // value channel
     const int iq = lane >> 3;               // row phase: rows i = 4m + iq
 
-    __shared__ float s_k[kStage][kMaxDk], s_q[kStage][kMaxDk], s_a[kStage][kMaxDk];
+    __shared__ __align__(16) float s_k[kStage][kMaxDk], s_q[kStage][kMaxDk], s_a[kStage][kMaxDk];
     __shared__ float s_v[kStage][kSlice];
     __shared__ float s_b[kStage];
     __shared__ int64_t s_first_ckpt;
@@ -57,7 +59,7 @@ prefill_recurrent_kernel(const T *__restrict__ q, const T *__restrict__ k, const
     float S[kRows];
 #pragma unroll
     for (int m = 0; m < kRows; ++m) {
-        const int i = 4 * m + iq;
+        const int i = 16 * (m >> 2) + 4 * iq + (m & 3);
         S[m] = (init && i < dk) ? init[sbase + (int64_t)i * dv + j] : 0.f;
     }
 
@@ -85,21 +87,31 @@ prefill_recurrent_kernel(const T *__restrict__ q, const T *__restrict__ k, const
 
         for (int r = 0; r < cnt; ++r) {
             float rp = 0.f;
+            float4 kr[kRows / 4];
 #pragma unroll
-            for (int m = 0; m < kRows; ++m) {
-                const int i = 4 * m + iq;
-                S[m] *= s_a[r][i];
-                rp += S[m] * s_k[r][i];
+            for (int gq = 0; gq < kRows / 4; ++gq) {
+                const int i0 = 16 * gq + 4 * iq;
+                const float4 a4 = *reinterpret_cast<const float4 *>(&s_a[r][i0]);
+                kr[gq] = *reinterpret_cast<const float4 *>(&s_k[r][i0]);
+                S[4 * gq + 0] *= a4.x; S[4 * gq + 1] *= a4.y; S[4 * gq + 2] *= a4.z; S[4 * gq + 3] *= a4.w;
+                rp += S[4 * gq + 0] * kr[gq].x;
+                rp += S[4 * gq + 1] * kr[gq].y;
+                rp += S[4 * gq + 2] * kr[gq].z;
+                rp += S[4 * gq + 3] * kr[gq].w;
             }
             rp += __shfl_xor_sync(0xffffffffu, rp, 8);
             rp += __shfl_xor_sync(0xffffffffu, rp, 16);
             const float u = s_b[r] * (s_v[r][jj] - rp);
             float op = 0.f;
 #pragma unroll
-            for (int m = 0; m < kRows; ++m) {
-                const int i = 4 * m + iq;
-                S[m] += s_k[r][i] * u;
-                op += S[m] * s_q[r][i];
+            for (int gq = 0; gq < kRows / 4; ++gq) {
+                const float4 q4 = *reinterpret_cast<const float4 *>(&s_q[r][16 * gq + 4 * iq]);
+                S[4 * gq + 0] += kr[gq].x * u; S[4 * gq + 1] += kr[gq].y * u;
+                S[4 * gq + 2] += kr[gq].z * u; S[4 * gq + 3] += kr[gq].w * u;
+                op += S[4 * gq + 0] * q4.x;
+                op += S[4 * gq + 1] * q4.y;
+                op += S[4 * gq + 2] * q4.z;
+                op += S[4 * gq + 3] * q4.w;
             }
             op += __shfl_xor_sync(0xffffffffu, op, 8);
             op += __shfl_xor_sync(0xffffffffu, op, 16);
@@ -111,7 +123,7 @@ prefill_recurrent_kernel(const T *__restrict__ q, const T *__restrict__ k, const
                 float *dst = ckpts + (slot * H + h) * (int64_t)dk * dv;
 #pragma unroll
                 for (int m = 0; m < kRows; ++m) {
-                    const int i = 4 * m + iq;
+                    const int i = 16 * (m >> 2) + 4 * iq + (m & 3);
                     if (i < dk) dst[(int64_t)i * dv + j] = S[m];
                 }
             }
@@ -120,7 +132,7 @@ prefill_recurrent_kernel(const T *__restrict__ q, const T *__restrict__ k, const
     if (final_state) {
 #pragma unroll
         for (int m = 0; m < kRows; ++m) {
-            const int i = 4 * m + iq;
+            const int i = 16 * (m >> 2) + 4 * iq + (m & 3);
             if (i < dk) final_state[sbase + (int64_t)i * dv + j] = S[m];
         }
     }
