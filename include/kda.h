@@ -15,10 +15,13 @@
  * of the chunked prefill inside the fp32/bf16 range.
  *
  * Conventions shared by every entry point
- *   - All tensor pointers are DEVICE pointers owned by the caller; the library allocates no
- *     memory, keeps no per-call state and never synchronizes the stream.  Every call only
- *     validates its host-side arguments and enqueues kernels on `stream` (a cudaStream_t;
- *     NULL = the legacy default stream) of the current device.  Calls are thread-safe.
+ *   - All tensor pointers are DEVICE pointers owned by the caller (the staged calls also take
+ *     host buffers); the library allocates no memory and keeps no per-call state.  A compute
+ *     call only validates its host-side arguments and enqueues kernels on `stream` (a
+ *     cudaStream_t; NULL = the legacy default stream) of the current device, without
+ *     synchronizing.  The exceptions are documented at their entry points: kda_device_status
+ *     synchronizes `stream`, and the staged calls create two streams and four events per device
+ *     on first use and keep them.  Calls are thread-safe.
  *   - Layouts are row-major with the last index contiguous:
  *       q, k, g : [T_total, H, d_k]     v, out : [T_total, H, d_v]     beta : [T_total, H]
  *       states  : [N, H, d_k, d_v] fp32, S[i][j] with i = key channel, j = value channel.
