@@ -21,7 +21,8 @@
  *     cudaStream_t; NULL = the legacy default stream) of the current device, without
  *     synchronizing.  The exceptions are documented at their entry points: kda_device_status
  *     synchronizes `stream`, and the staged calls create two streams and four events per device
- *     on first use and keep them.  Calls are thread-safe.
+ *     on first use (the no-scratch variant one more event) and keep them.  Calls are
+ *     thread-safe.
  *   - Layouts are row-major with the last index contiguous:
  *       q, k, g : [T_total, H, d_k]     v, out : [T_total, H, d_v]     beta : [T_total, H]
  *       states  : [N, H, d_k, d_v] fp32, S[i][j] with i = key channel, j = value channel.
