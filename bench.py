@@ -536,7 +536,7 @@ def run_gb300(args):
     reuse = prefix_reuse_figure(dev, stream)
     assert kda.device_status() == 0
     torch.cuda.empty_cache()
-    cp = context_parallel_figure(dev, stream, hbm_peak=hbm_peak)
+    cp = context_parallel_figure(dev, stream, hbm_peak=hbm_peak, keep=with_base)
     assert kda.device_status() == 0
     torch.cuda.empty_cache()
     named = named_workload_figures(dev, stream, hbm_peak, keep=with_base)
@@ -551,6 +551,7 @@ def run_gb300(args):
     base, parity = cpu_baseline(step) if with_base else (None, None)
     if with_base:
         other_parity(named)
+        other_parity({"context_parallel": cp})
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "prefill_traffic.json")
     if os.path.exists(tpath):
@@ -726,10 +727,11 @@ def named_workload_figures(dev, stream, hbm_peak, keep: bool = False):
     return res
 
 
-def context_parallel_figure(dev, stream, T=262144, heads=8, hbm_peak=None):
+def context_parallel_figure(dev, stream, T=262144, heads=8, hbm_peak=None, keep=False):
     """One long sequence at a low head count: the plain prefill runs one CTA per head; the
     context-parallel prefill cuts the sequence into segments that prefill side by side.  The scan
-    and the output correction are also timed alone."""
+    and the output correction are also timed alone.  With `keep`, 4 of the heads' inputs and
+    results stay on the host for the CPU-baseline leg's oracle comparison."""
     import torch
 
     import kimi_delta_attention_13_gb300 as kda
@@ -752,6 +754,17 @@ def context_parallel_figure(dev, stream, T=262144, heads=8, hbm_peak=None):
     split()
     _, plain_ms = cuda_time_ms(plain, 2, stream)
     _, cp_ms = cuda_time_ms(split, 3, stream)
+    check = None
+    if keep:
+        out, fin = prefill_cp(*args, seg_len=seg_len, lengths=[T], stream=stream)
+        hs = [0, 3, 5, 7][: heads]
+        idx = torch.tensor(hs, device=dev)
+        check = {"heads": hs, "ckpt_stride": 0,
+                 "inputs": {k_: x[k_].index_select(1, idx).cpu() for k_ in ("q", "k", "v", "g", "beta")},
+                 "cu": torch.tensor([0, T], dtype=torch.int64), "init": None,
+                 "out": out.index_select(1, idx).cpu(), "final": fin.index_select(1, idx).cpu(),
+                 "ckpts": None}
+        del out, fin
     del x, args
     # the scan alone, on states of the same shape (its time does not depend on the values)
     n_seg = -(-T // seg_len)
@@ -789,6 +802,8 @@ def context_parallel_figure(dev, stream, T=262144, heads=8, hbm_peak=None):
            "cp_tokens_per_s": T / (cp_ms / 1e3), "plain_tokens_per_s": T / (plain_ms / 1e3)}
     if hbm_peak:
         fig["correct_frac"] = fig["correct_GB/s"] / hbm_peak
+    if check is not None:
+        fig["_check"] = check
     return fig
 
 
