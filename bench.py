@@ -6,9 +6,11 @@ One step = one kda_prefill of the 8192-token, 96-head workload (inputs resident 
 The same step through kda_prefill_precise, the decode (256 sequences x 96 heads, 1.6 GB fp32
 state updated in place), a checkpoint restore (kda_state_copy of 64 states), the pre-mixer and the
 output gate on the same token grid, a prefix-reuse (cache-hit) prefill, the context-parallel
-prefill of one 262,144-token sequence at 8 heads (and its scan alone), and the varlen x8 and
-262,144-token (64 checkpoints) prefills at 96 heads are timed in the same run and reported beside
-it.
+prefill of one 262,144-token sequence at 8 heads (and its scan and output correction alone), and
+the varlen x8 and 262,144-token (64 checkpoints) prefills at 96 heads are timed in the same run
+and reported beside it.  The CPU-baseline leg times the fp64 oracle on the step's own inputs and
+compares the step's results with it, and those of the varlen x8, 262,144-token and
+context-parallel figures on sampled heads.
 
     python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 
