@@ -468,7 +468,20 @@ def run_gb300(args):
     for _ in range(2):
         e2e_step()
     barrier()
-    e2e_ms, e2e_per = cuda_time_ms(e2e_step, max(3, args.steps // 2), stream)
+    # one event pair per step on the caller's stream (a step's copies and prefills all finish
+    # before the stream moves on): the mean over the steps is the figure, the spread is reported
+    # beside it, since a shared host's memory traffic can slow single steps
+    n_e2e = max(3, args.steps // 2)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e + 1)]
+    torch.cuda.synchronize()
+    marks[0].record(stream)
+    for i in range(n_e2e):
+        e2e_step()
+        marks[i + 1].record(stream)
+    torch.cuda.synchronize()
+    e2e_steps = sorted(marks[i].elapsed_time(marks[i + 1]) for i in range(n_e2e))
+    e2e_ms = marks[0].elapsed_time(marks[-1])
+    e2e_per = e2e_ms / n_e2e
     if world > 1:
         e2e_per = max_over_ranks(e2e_per, dev)
     h2d = sum(v.numel() * v.element_size() for v in hx.values())
@@ -586,6 +599,8 @@ def run_gb300(args):
                      "roofline_fraction": max(t_bytes, t_flops) / (per_ms / 1e3)},
         "e2e": {"value": world * T1 / (e2e_per / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_per,
+                "step_ms": {"steps": len(e2e_steps), "min": e2e_steps[0],
+                            "median": e2e_steps[len(e2e_steps) // 2], "max": e2e_steps[-1]},
                 "path": f"kda_prefill_staged from pinned host buffers, {E2E_CHUNK}-token chunks whose "
                         "uploads, prefills and downloads overlap"},
         "precise_mode": {"workload": "the same prefill through kda_prefill_precise (Aqk carried in "
