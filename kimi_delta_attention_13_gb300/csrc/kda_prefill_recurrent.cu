@@ -11,7 +11,8 @@
 // lane l owns column j = 8w + (l & 7) of the slice and the key rows i = 16 g + 4 (l >> 3) + c
 // (g = 0..7, c = 0..3): four consecutive rows per group, read from shared memory as one float4,
 // and the column sums over i are two xor-shuffles.  Tokens are staged 16 at a time in shared
-// memory.
+// memory, by fully unrolled loops so that each thread's global loads of a stage are in flight
+// together.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -67,6 +68,7 @@ prefill_recurrent_kernel(const T *__restrict__ q, const T *__restrict__ k, const
     for (int64_t t0 = start; t0 < end; t0 += kStage) {
         const int cnt = (int)((end - t0) < kStage ? (end - t0) : kStage);
         __syncthreads();  // previous stage fully consumed
+#pragma unroll 16
         for (int e = tid; e < kStage * kMaxDk; e += kThreads) {
             const int r = e / kMaxDk, c = e % kMaxDk;
             float kv = 0.f, qv = 0.f, av = 1.f;
@@ -78,6 +80,7 @@ prefill_recurrent_kernel(const T *__restrict__ q, const T *__restrict__ k, const
             }
             s_k[r][c] = kv; s_q[r][c] = qv; s_a[r][c] = av;
         }
+#pragma unroll
         for (int e = tid; e < kStage * kSlice; e += kThreads) {
             const int r = e / kSlice, c = e % kSlice;
             s_v[r][c] = r < cnt ? to_f32(v[(t0 + r) * row_stride_v + (int64_t)h * dv + slice * kSlice + c]) : 0.f;
